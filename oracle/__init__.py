@@ -1,0 +1,165 @@
+"""CPU oracle for packed variable-length QK-RoPE (test infrastructure only).
+
+This package is the plain, slow definition the CUDA library is checked against.
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+and reference arms may import it; the product path never does.  It shares no code
+with the CUDA library: its arithmetic lives in ``rope_oracle.c`` (plain C, built
+with ``-ffp-contract=off``), and this module only marshals numpy arrays.
+
+What each function follows (restated, not copied):
+
+* ``positions`` -- unsloth.ai "3x faster training with packing", section
+  "Packing non contaminé": position ids restart at each packed-sample boundary.
+* ``inv_freq`` / ``cos_sin`` -- rotary base ``rope_theta`` as named in the TRL
+  "training beyond 1M tokens" page, YaRN section; the RoFormer frequency form is a
+  reading (the pages print no formula).
+* ``rope_rows`` / ``rope_packed`` -- unsloth.ai page, section "Kernel Triton QK
+  RoPE fusionné avec packing": ``x*cos + rotate_half(x)*sin``; backward is the same
+  with sin negated (``R^T``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "rope_oracle.c")
+LIB_PATH = os.path.join(_HERE, "librope_oracle.so")
+CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-shared", "-fPIC"]
+
+
+def compile_source(src: str, out: str) -> str:
+    """Compile one oracle C source into a shared library (no FMA contraction)."""
+    tmp = out + ".tmp%d" % os.getpid()
+    subprocess.check_call(["gcc", *CFLAGS, src, "-o", tmp, "-lm"])
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle if its library is missing or older than its source."""
+    if force or not os.path.exists(LIB_PATH) or os.path.getmtime(LIB_PATH) < os.path.getmtime(SOURCE):
+        compile_source(SOURCE, LIB_PATH)
+    return LIB_PATH
+
+
+def _ptr(a: np.ndarray, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+class Oracle:
+    """ctypes view of one compiled oracle library (the default one, or a test build)."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        f32p = ctypes.POINTER(ctypes.c_float)
+        lib.oracle_positions.argtypes = [i32p, ctypes.c_int32, ctypes.c_int64, i32p]
+        lib.oracle_positions.restype = ctypes.c_int
+        lib.oracle_inv_freq.argtypes = [ctypes.c_double, ctypes.c_int32, f32p]
+        lib.oracle_inv_freq.restype = None
+        lib.oracle_cos_sin.argtypes = [ctypes.c_int32, ctypes.c_double, ctypes.c_int32, f32p, f32p]
+        lib.oracle_cos_sin.restype = None
+        lib.oracle_rope_rows.argtypes = [u16p, u16p, ctypes.c_int64, i32p, ctypes.c_int32,
+                                         ctypes.c_int32, ctypes.c_double, ctypes.c_int32]
+        lib.oracle_rope_rows.restype = None
+        lib.oracle_rope_packed.argtypes = [u16p, u16p, i32p, ctypes.c_int32, ctypes.c_int64,
+                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
+                                           ctypes.c_int32, i32p]
+        lib.oracle_rope_packed.restype = ctypes.c_int
+        lib.oracle_float_to_bf16.argtypes = [ctypes.c_float]
+        lib.oracle_float_to_bf16.restype = ctypes.c_uint16
+        self.lib = lib
+        self.path = lib_path
+
+    def positions(self, cu_seqlens, total_tokens: int) -> np.ndarray:
+        """int32 position of every token in its packed sample; -1 outside every sample."""
+        cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+        out = np.empty(int(total_tokens), dtype=np.int32)
+        rc = self.lib.oracle_positions(_ptr(cu, ctypes.c_int32), cu.size - 1, int(total_tokens),
+                                       _ptr(out, ctypes.c_int32))
+        if rc != 0:
+            raise ValueError("cu_seqlens is not non-decreasing within [0, total_tokens]")
+        return out
+
+    def inv_freq(self, theta: float, head_dim: int) -> np.ndarray:
+        w = np.empty(head_dim // 2, dtype=np.float32)
+        self.lib.oracle_inv_freq(float(theta), int(head_dim), _ptr(w, ctypes.c_float))
+        return w
+
+    def cos_sin(self, pos: int, theta: float, head_dim: int):
+        """(c, s) float32 arrays of length head_dim/2 for one position."""
+        c = np.empty(head_dim // 2, dtype=np.float32)
+        s = np.empty(head_dim // 2, dtype=np.float32)
+        self.lib.oracle_cos_sin(int(pos), float(theta), int(head_dim), _ptr(c, ctypes.c_float),
+                                _ptr(s, ctypes.c_float))
+        return c, s
+
+    def rope_rows(self, x_bits: np.ndarray, pos, theta: float, bwd: bool = False) -> np.ndarray:
+        """Rotate token rows.  x_bits: uint16 bf16 bit patterns [rows, H, d]; pos: int32
+        [rows] (-1 leaves a row unchanged).  Returns a new uint16 array."""
+        x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+        rows, H, d = x.shape
+        p = np.ascontiguousarray(pos, dtype=np.int32)
+        assert p.shape == (rows,) and d % 2 == 0 and d <= 1024
+        y = np.empty_like(x)
+        self.lib.oracle_rope_rows(_ptr(x, ctypes.c_uint16), _ptr(y, ctypes.c_uint16), rows,
+                                  _ptr(p, ctypes.c_int32), H, d, float(theta), 1 if bwd else 0)
+        return y
+
+    def rope_packed(self, x_bits: np.ndarray, cu_seqlens, theta: float, bwd: bool = False) -> np.ndarray:
+        """Whole packed tensor [T, H, d] (uint16 bf16 bits), positions from cu_seqlens."""
+        x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+        T, H, d = x.shape
+        cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+        y = np.empty_like(x)
+        scratch = np.empty(T, dtype=np.int32)
+        rc = self.lib.oracle_rope_packed(_ptr(x, ctypes.c_uint16), _ptr(y, ctypes.c_uint16),
+                                         _ptr(cu, ctypes.c_int32), cu.size - 1, T, H, d,
+                                         float(theta), 1 if bwd else 0,
+                                         _ptr(scratch, ctypes.c_int32))
+        if rc != 0:
+            raise ValueError("cu_seqlens is not non-decreasing within [0, total_tokens]")
+        return y
+
+    def float_to_bf16_bits(self, v: float) -> int:
+        return int(self.lib.oracle_float_to_bf16(float(v)))
+
+
+_default = None
+
+
+def get() -> Oracle:
+    """The oracle built from ``rope_oracle.c`` (compiled on first use)."""
+    global _default
+    if _default is None:
+        _default = Oracle(build())
+    return _default
+
+
+def positions(cu_seqlens, total_tokens):
+    return get().positions(cu_seqlens, total_tokens)
+
+
+def inv_freq(theta, head_dim):
+    return get().inv_freq(theta, head_dim)
+
+
+def cos_sin(pos, theta, head_dim):
+    return get().cos_sin(pos, theta, head_dim)
+
+
+def rope_rows(x_bits, pos, theta, bwd=False):
+    return get().rope_rows(x_bits, pos, theta, bwd)
+
+
+def rope_packed(x_bits, cu_seqlens, theta, bwd=False):
+    return get().rope_packed(x_bits, cu_seqlens, theta, bwd)
+
+
+def float_to_bf16_bits(v):
+    return get().float_to_bf16_bits(v)

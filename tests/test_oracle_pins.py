@@ -1,0 +1,11 @@
+"""The CPU oracle against what the source pages and plain mathematics fix (no GPU)."""
+import pytest
+
+import oracle_pins
+
+
+@pytest.mark.parametrize("pin", oracle_pins.ALL_PINS, ids=lambda p: p.__name__)
+def test_oracle_pin(oracle_mod, pin):
+    if pin is oracle_pins.pin_cos_sin_mpmath:
+        pytest.importorskip("mpmath")
+    pin(oracle_mod)

@@ -1,0 +1,445 @@
+#!/usr/bin/env python
+"""Benchmark of fused packed-varlen QK-RoPE, forward + backward, on GB300.
+
+One step = the forward rotation of Q and K and the backward (transpose) rotation of
+dQ and dK of one packed batch, in place, through the C ABI of librope_qk.so.  The
+default workload is the Qwen3-32B attention shape: 65,536 tokens packed from
+50% U[16,256] / 50% U[1024,4096] samples, Q 64 heads, K 8 heads, head_dim 128,
+theta 1e6.  The four tensors hold 2.4 GB, far more than the 129 MB L2, so no flush
+is needed between steps.  The cos/sin cache is built once before timing, as a model
+builds its rotary cache once for all layers and steps.
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank rotates its own pack (weak
+scaling, no collective on the data path); the value is the tokens of all ranks over
+the slowest rank's time.  ``--impl reference`` times the CPU oracle on the host cores
+instead (bounded samples of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "QK-RoPE fwd+bwd tokens/s and HBM GB/s (% of GB300 peak), packed varlen"
+UNIT = "tokens/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCE = os.path.join(ROOT, "packed_varlen_rope_gb300", "csrc", "rope_qk.cu")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "rope_qk_tile_kernel_qwen3-32b-64k.md")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=4)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target seconds of oracle work for the CPU baseline sample")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- environment
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source; else None."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    t = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    if not h or not t or h.group(1) != kernel_source_hash():
+        return None
+    return int(t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while the GPU works."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+                except ValueError:
+                    continue
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "none"}
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        window = "timed"
+        if len(inside) < 3:
+            inside = [r for r in rows if r[0] <= t1 + 0.2]
+            window = "warmup+timed"
+        reasons = sorted({name for r in inside for name, v in zip(self.REASONS, r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value of x over all ranks (the slowest rank's time); x itself when alone."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tokens_per_s(world: int, tokens_per_rank: int, ms_per_step: float) -> float:
+    """Weak scaling: every rank processes its own pack of tokens_per_rank tokens."""
+    return world * tokens_per_rank / (ms_per_step / 1e3)
+
+
+def physical_gpu_index(local_rank: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [v for v in vis.split(",") if v.strip()]
+    if ids and local_rank < len(ids) and ids[local_rank].strip().isdigit():
+        return int(ids[local_rank])
+    return local_rank
+
+
+# ---------------------------------------------------------------- reference arm (CPU oracle)
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import numpy as np
+
+    import oracle
+    from packed_varlen_rope_gb300 import workloads as wl
+
+    oracle.build()
+    w = wl.WORKLOADS[args.workload]
+    pack = wl.make_pack(w)
+    pos = oracle.positions(pack.cu_seqlens, pack.total_tokens)
+    import torch
+
+    def bits(shape, kind):
+        t = wl.normal_bf16(shape, wl.seed(args.workload, kind), device="cpu")
+        return t.view(torch.int16).numpy().view(np.uint16)
+
+    def step(a, n):
+        idx = np.arange(a, a + n) % pack.total_tokens
+        p = pos[idx]
+        oracle.rope_rows(qs[:n], p, w.theta)
+        oracle.rope_rows(ks[:n], p, w.theta)
+        oracle.rope_rows(qs[:n], p, w.theta, bwd=True)
+        oracle.rope_rows(ks[:n], p, w.theta, bwd=True)
+
+    cal = 64
+    qs = bits((4096, w.n_q_heads, w.head_dim), "q")
+    ks = bits((4096, w.n_kv_heads, w.head_dim), "k")
+    t = time.perf_counter()
+    step(0, cal)
+    per_token = (time.perf_counter() - t) / cal
+    budget = 90.0
+    n = int(max(1, min(4096, budget / max(1, args.steps + args.warmup) / per_token)))
+    a = 0
+    for _ in range(args.warmup):
+        step(a, n)
+        a += n
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step(a, n)
+        a += n
+    el = time.perf_counter() - t0
+    value = args.steps * n / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 math, bf16 I/O",
+        "data": "synthetic",
+        "config": {"workload": w.name, "tokens_per_step": n, "n_q_heads": w.n_q_heads,
+                   "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "theta": w.theta},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "%d consecutive tokens of the %s pack per step (fwd+bwd of Q and K)"
+                                   % (n, w.name)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def cpu_baseline(args, w, pack, q_sample, k_sample, dq_sample, dk_sample):
+    """The oracle as it stands, single-threaded, on a contiguous token sample."""
+    import oracle
+
+    oracle.build()
+    pos = oracle.positions(pack.cu_seqlens, pack.total_tokens)
+    n_all = q_sample.shape[0]
+
+    def run(n):
+        p = pos[:n]
+        oracle.rope_rows(q_sample[:n], p, w.theta)
+        oracle.rope_rows(k_sample[:n], p, w.theta)
+        oracle.rope_rows(dq_sample[:n], p, w.theta, bwd=True)
+        oracle.rope_rows(dk_sample[:n], p, w.theta, bwd=True)
+
+    cal = min(256, n_all)
+    t = time.perf_counter()
+    run(cal)
+    per_token = (time.perf_counter() - t) / cal
+    n = int(max(cal, min(n_all, args.cpu_seconds / per_token)))
+    t = time.perf_counter()
+    run(n)
+    el = time.perf_counter() - t
+    return {"value": n / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "first %d tokens of the %s pack, fwd+bwd of Q and K, %.1f s on one host core"
+                      % (n, w.name, el)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    from packed_varlen_rope_gb300 import build as _build
+
+    _build.build()
+    import packed_varlen_rope_gb300 as pr
+    from packed_varlen_rope_gb300 import workloads as wl
+
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = wl.WORKLOADS[args.workload]
+    pack = wl.make_pack(w, rank=rank)
+    T = pack.total_tokens
+    shape_q, shape_k = (T, w.n_q_heads, w.head_dim), (T, w.n_kv_heads, w.head_dim)
+    q = wl.normal_bf16(shape_q, wl.seed(args.workload, "q", rank), device=dev)
+    k = wl.normal_bf16(shape_k, wl.seed(args.workload, "k", rank), device=dev)
+    dq = wl.normal_bf16(shape_q, wl.seed(args.workload, "dq", rank), device=dev)
+    dk = wl.normal_bf16(shape_k, wl.seed(args.workload, "dk", rank), device=dev)
+    cu = torch.from_numpy(pack.cu_seqlens).to(dev)
+    cache = pr.new_cos_sin_cache(max(pack.lengths), w.head_dim, w.theta, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    do_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    samples = None
+    if do_cpu:
+        n = min(T, 65536)
+        to_np = lambda t: t[:n].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)  # noqa: E731
+        samples = (to_np(q), to_np(k), to_np(dq), to_np(dk))
+
+    bytes_per_pass = 4 * (w.n_q_heads + w.n_kv_heads) * w.head_dim * pack.valid_tokens
+
+    def step():
+        pr.rope_qk_fwd(q, k, cu, w.theta, cos_sin_cache=cache)
+        pr.rope_qk_bwd(dq, dk, cu, w.theta, cos_sin_cache=cache)
+
+    sampler = ClockSampler(physical_gpu_index(local))
+    sampler.start()
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4 * K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        ev[4 * i].record(stream)
+        pr.rope_qk_fwd(q, k, cu, w.theta, cos_sin_cache=cache)
+        ev[4 * i + 1].record(stream)
+        ev[4 * i + 2].record(stream)
+        pr.rope_qk_bwd(dq, dk, cu, w.theta, cos_sin_cache=cache)
+        ev[4 * i + 3].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t_wall1 = time.time()
+    sampler.stop()
+    total_ms = start.elapsed_time(end)
+    launch_ms = [ev[2 * j].elapsed_time(ev[2 * j + 1]) for j in range(2 * K)]
+    total_ms = max_over_ranks(total_ms, world, dev)
+    ms_per_step = total_ms / K
+    value = whole_job_tokens_per_s(world, pack.valid_tokens, ms_per_step)
+    avg_launch_s = statistics.mean(launch_ms) / 1e3
+    achieved = bytes_per_pass / avg_launch_s / 1e9
+    peak, peak_kind = measured_peak()
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev)
+
+    cpu = None
+    if do_cpu:
+        cpu = cpu_baseline(args, w, pack, *samples)
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": w.name, "total_tokens": T, "valid_tokens": pack.valid_tokens,
+            "n_seqs": pack.n_seqs, "max_seq_len": max(pack.lengths), "n_q_heads": w.n_q_heads,
+            "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "theta": w.theta,
+            "layout": "packed [T, H, d] bf16, in place", "parallelism": "dp%d (independent packs)" % world,
+            "l2": "no flush: Q, K, dQ, dK = %.2f GB per step > 129 MB L2" % (bytes_per_pass / 1e9),
+            "cos_sin": "fp32 cache of %d positions built once before timing" % max(pack.lengths),
+        },
+        "hbm_gbs": 2 * bytes_per_pass / (ms_per_step / 1e3) / 1e9,
+        "hbm_frac_of_measured": 2 * bytes_per_pass / (ms_per_step / 1e3) / 1e9 / peak,
+        "hbm_frac_of_nominal_8tbs": 2 * bytes_per_pass / (ms_per_step / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": profiled_traffic(),
+                     "kernel": "rope_qk_tile_kernel<128,false>",
+                     "algorithmic_bytes_per_launch": bytes_per_pass,
+                     "avg_launch_us": avg_launch_s * 1e6, "peak_kind": peak_kind + " (hbm_gbs)"},
+        "clocks": clocks,
+        "gpu_launches": 2 * K,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev):
+    """Same metric through the public call with the inputs in pinned host memory:
+    every step copies Q, K, dQ, dK host->device, runs forward and backward, and copies
+    the four results device->host."""
+    import torch
+
+    host_in = [t.to("cpu").pin_memory() for t in (q, k, dq, dk)]
+    host_out = [torch.empty_like(t).pin_memory() for t in host_in]
+    dev_buf = [torch.empty_like(t) for t in (q, k, dq, dk)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def step():
+        for d, h in zip(dev_buf, host_in):
+            d.copy_(h, non_blocking=True)
+        pr.rope_qk_fwd(dev_buf[0], dev_buf[1], cu, w.theta, cos_sin_cache=cache)
+        pr.rope_qk_bwd(dev_buf[2], dev_buf[3], cu, w.theta, cos_sin_cache=cache)
+        for h, d in zip(host_out, dev_buf):
+            h.copy_(d, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    E = max(1, args.e2e_steps)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    s.record(stream)
+    for _ in range(E):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(s.elapsed_time(e) / E, world, dev)
+    return {"value": whole_job_tokens_per_s(world, pack.valid_tokens, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": E}
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.gpus != world and world == 1 and args.gpus > 1:
+        print("--gpus %d needs torchrun with %d processes" % (args.gpus, args.gpus), file=sys.stderr)
+        return 2
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,158 @@
+/*
+ * rope_qk.h -- C ABI of the packed variable-length QK rotary position embedding
+ * (RoPE) library for GB300 (sm_103a), librope_qk.so.
+ *
+ * The operation.  Q and K of one padding-free pack of samples are rotated in place in
+ * one pass (unsloth.ai, "3x faster training with packing", section "Kernel Triton QK
+ * RoPE fusionné avec packing"):
+ *
+ *     y = x*cos + rotate_half(x)*sin  ==  x*cos + (x @ R)*sin,  R = [[0, I], [-I, 0]]
+ *
+ * with the half-split pairing (element i pairs with element i + d/2 of the same head).
+ * The backward is the same rotation with sin negated, dX = dY*cos + (dY @ R^T)*sin.
+ * Positions restart at every packed-sample boundary (same page, section "Packing non
+ * contaminé"): token t of sample s has position t - cu_seqlens[s].  Flat offsets
+ * switch to 64-bit arithmetic when an element count reaches 2^31 (same page, section
+ * "Indexage int64 pour les kernels Triton").  The rotary base theta is the model's
+ * `rope_theta` (TRL "training beyond 1M tokens", YaRN section).
+ *
+ * Arithmetic, exactly (identical bits to a plain CPU evaluation of the same steps):
+ *   w_j   = (float) pow(theta, -(2.0*j)/d)            binary64 on the host, j < d/2
+ *   phi   = (float)pos * w_j                          one binary32 multiply
+ *   c, s  = cos(phi), sin(phi) in binary64, each rounded once to binary32
+ *   y_i     = bf16( (a*c) - (b*s) ),  y_{i+d/2} = bf16( (b*c) + (a*s) )
+ *           every product and sum rounded to binary32, no fused multiply-add,
+ *           one round-to-nearest-even to bf16; a = x_i, b = x_{i+d/2}.
+ *
+ * Layouts.  Q is bf16 [total_tokens, n_q_heads, head_dim], K is bf16
+ * [total_tokens, n_kv_heads, head_dim], both row-major and contiguous.  cu_seqlens is
+ * int32 [n_seqs + 1], non-decreasing, cu_seqlens[n_seqs] <= total_tokens.  A token
+ * with no sample (t < cu_seqlens[0] or t >= cu_seqlens[n_seqs]) is outside the pack:
+ * in place it is left untouched; out of place its rows are copied unchanged.
+ *
+ * Ownership.  Every pointer is owned by the caller.  Q, K, outputs, cu_seqlens, the
+ * cos/sin cache and pos/err buffers are DEVICE pointers; the library keeps no pointer
+ * after a call returns, allocates no device memory, and never synchronises.  Calls are
+ * asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *
+ * Errors.  Every entry point returns ROPE_OK (0) or a negative rope_status.  Arguments
+ * are checked on the host before anything is launched; a rejected call launches
+ * nothing.  The values inside cu_seqlens are not read on the host (that would need a
+ * synchronisation): rope_validate_cu_seqlens checks them on the device.  With invalid
+ * values the kernels still stay inside the Q/K/cache bounds and skip the tokens whose
+ * position cannot be derived.  No kernel traps, asserts or spins.
+ */
+#ifndef ROPE_QK_H
+#define ROPE_QK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ROPE_QK_ABI_VERSION 1
+
+typedef enum rope_status {
+    ROPE_OK = 0,
+    ROPE_ERR_NULL = -1,         /* a required pointer is NULL */
+    ROPE_ERR_SHAPE = -2,        /* total_tokens < 0, n_seqs < 0, a head count < 1, rows < 0 */
+    ROPE_ERR_HEAD_DIM = -3,     /* head_dim not a multiple of 16 in [16, 256] */
+    ROPE_ERR_ALIGN = -4,        /* Q/K/output not 16-byte aligned, cache not 8-byte aligned */
+    ROPE_ERR_OVERLAP = -5,      /* Q and K overlap, or an output overlaps an input */
+    ROPE_ERR_UNSUPPORTED = -6,  /* total_tokens >= 2^24 (positions no longer exact in fp32) */
+    ROPE_ERR_LAUNCH = -7,       /* the CUDA runtime refused a launch or copy */
+    ROPE_ERR_THETA = -8         /* theta not finite and > 0 */
+} rope_status;
+
+/* Bits of the word rope_validate_cu_seqlens writes. */
+#define ROPE_CU_NEGATIVE_START   0x1   /* cu_seqlens[0] < 0 */
+#define ROPE_CU_DECREASING       0x2   /* cu_seqlens[s+1] < cu_seqlens[s] for some s */
+#define ROPE_CU_PAST_END         0x4   /* cu_seqlens[n_seqs] > total_tokens */
+#define ROPE_CU_NONZERO_START    0x8   /* cu_seqlens[0] != 0 (allowed; tokens before it are outside) */
+
+/*
+ * Forward: rotate Q and K of every token of the pack (unsloth.ai page, section "Kernel
+ * Triton QK RoPE fusionné avec packing"; positions per section "Packing non contaminé").
+ *
+ *   q, k            device bf16 [total_tokens, n_q_heads, head_dim] and
+ *                   [total_tokens, n_kv_heads, head_dim]; 16-byte aligned; disjoint.
+ *   cu_seqlens      device int32 [n_seqs + 1] sample offsets in the token stream.
+ *   n_seqs          number of samples (>= 0; 0 means nothing is inside the pack).
+ *   total_tokens    T, rows of Q and K (0 <= T < 2^24; T == 0 launches nothing).
+ *   n_q_heads, n_kv_heads   >= 1 (grouped-query attention: any ratio).
+ *   head_dim        d, a multiple of 16 in [16, 256].
+ *   theta           rotary base (> 0, finite).
+ *   in_place        nonzero: write the result over q and k (q_out/k_out ignored);
+ *                   zero: write to q_out/k_out (same shapes, 16-byte aligned, disjoint
+ *                   from q and k); q and k are then only read.
+ *   cos_sin_cache   optional device float [cache_rows][head_dim/2][2] holding (c, s)
+ *                   per position as rope_cos_sin_cache_build writes them for the same
+ *                   theta and head_dim; 8-byte aligned.  Positions >= cache_rows, and
+ *                   every position when the cache is NULL, are evaluated on the fly
+ *                   with identical results.
+ *   cache_rows      rows of the cache (>= 0).
+ *   stream          cudaStream_t or NULL.
+ */
+int rope_qk_fwd(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs,
+                int64_t total_tokens, int32_t n_q_heads, int32_t n_kv_heads,
+                int32_t head_dim, double theta, int32_t in_place,
+                void *q_out, void *k_out, const float *cos_sin_cache, int64_t cache_rows,
+                void *stream);
+
+/*
+ * Backward: q and k hold dL/dY for Q and K and receive dL/dX, the transpose rotation
+ * (sin negated; unsloth.ai page, same section, the backward note with R^T).
+ * Arguments exactly as rope_qk_fwd.
+ */
+int rope_qk_bwd(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs,
+                int64_t total_tokens, int32_t n_q_heads, int32_t n_kv_heads,
+                int32_t head_dim, double theta, int32_t in_place,
+                void *q_out, void *k_out, const float *cos_sin_cache, int64_t cache_rows,
+                void *stream);
+
+/*
+ * Fill a cos/sin cache: cache[p][j] = (c, s) of position p and frequency j, for
+ * p < cache_rows, j < head_dim/2, by the arithmetic above (binary64 cos/sin on the
+ * device, rounded to binary32).  cache: device float, cache_rows*head_dim floats,
+ * 8-byte aligned, owned by the caller.  Build it once per (theta, head_dim) with
+ * cache_rows >= the longest sample; every layer and step can reuse it.
+ */
+int rope_cos_sin_cache_build(float *cache, int64_t cache_rows, int32_t head_dim,
+                             double theta, void *stream);
+
+/* Bytes a cache of `cache_rows` rows takes (cache_rows * head_dim * 4), or -1. */
+int64_t rope_cos_sin_cache_bytes(int64_t cache_rows, int32_t head_dim);
+
+/*
+ * Positions exactly as the rotation kernels derive them from cu_seqlens (section
+ * "Packing non contaminé": reset at each boundary): pos_out[t] = t - cu_seqlens[s]
+ * for the last s with cu_seqlens[s] <= t, or -1 for a token outside the pack.
+ * pos_out: device int32 [total_tokens].
+ */
+int rope_qk_positions(const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_tokens,
+                      int32_t *pos_out, void *stream);
+
+/*
+ * Check the values of cu_seqlens on the device.  Writes to the device word *err_word
+ * the OR of the ROPE_CU_* bits that apply (0 = valid).  The word is cleared on
+ * `stream` first; read it after the stream reaches this point.
+ */
+int rope_validate_cu_seqlens(const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_tokens,
+                             int32_t *err_word, void *stream);
+
+/* Host-side inverse frequencies w_j (head_dim/2 floats) exactly as the kernels use
+ * them.  w_out: HOST float[head_dim/2].  No CUDA call. */
+int rope_qk_inv_freq(double theta, int32_t head_dim, float *w_out);
+
+/* Static text for a status code. */
+const char *rope_strerror(int status);
+
+/* ROPE_QK_ABI_VERSION of the loaded library. */
+int rope_qk_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROPE_QK_H */

@@ -1,0 +1,209 @@
+"""ctypes binding of librope_qk.so: argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does no arithmetic
+of the method: it checks tensor dtypes/devices, turns tensors into pointers and the
+current torch stream into a ``cudaStream_t``, and raises ``RopeError`` on a non-zero
+status.  There is no fallback: if the library is missing, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "librope_qk.so")
+
+EXPORTS = (
+    "rope_qk_fwd", "rope_qk_bwd", "rope_cos_sin_cache_build", "rope_cos_sin_cache_bytes",
+    "rope_qk_positions", "rope_validate_cu_seqlens", "rope_qk_inv_freq", "rope_strerror",
+    "rope_qk_abi_version",
+)
+
+ROPE_CU_NEGATIVE_START = 0x1
+ROPE_CU_DECREASING = 0x2
+ROPE_CU_PAST_END = 0x4
+ROPE_CU_NONZERO_START = 0x8
+
+_lib = None
+
+
+class RopeError(RuntimeError):
+    def __init__(self, fn: str, status: int, text: str):
+        super().__init__("%s failed with status %d: %s" % (fn, status, text))
+        self.status = status
+
+
+def load_library(path: Optional[str] = None):
+    """Load librope_qk.so (built by ``packed_varlen_rope_gb300.build``) and declare its
+    signatures.  Raises ``OSError`` when the library has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise OSError("librope_qk.so is not built (%s); run packed_varlen_rope_gb300.build.build()" % p)
+    lib = ctypes.CDLL(p)
+    vp, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+    rope_args = [vp, vp, vp, i32, i64, i32, i32, i32, dbl, i32, vp, vp, vp, i64, vp]
+    for name in ("rope_qk_fwd", "rope_qk_bwd"):
+        getattr(lib, name).argtypes = rope_args
+        getattr(lib, name).restype = ctypes.c_int
+    lib.rope_cos_sin_cache_build.argtypes = [vp, i64, i32, dbl, vp]
+    lib.rope_cos_sin_cache_build.restype = ctypes.c_int
+    lib.rope_cos_sin_cache_bytes.argtypes = [i64, i32]
+    lib.rope_cos_sin_cache_bytes.restype = ctypes.c_int64
+    lib.rope_qk_positions.argtypes = [vp, i32, i64, vp, vp]
+    lib.rope_qk_positions.restype = ctypes.c_int
+    lib.rope_validate_cu_seqlens.argtypes = [vp, i32, i64, vp, vp]
+    lib.rope_validate_cu_seqlens.restype = ctypes.c_int
+    lib.rope_qk_inv_freq.argtypes = [dbl, i32, ctypes.POINTER(ctypes.c_float)]
+    lib.rope_qk_inv_freq.restype = ctypes.c_int
+    lib.rope_strerror.argtypes = [ctypes.c_int]
+    lib.rope_strerror.restype = ctypes.c_char_p
+    lib.rope_qk_abi_version.argtypes = []
+    lib.rope_qk_abi_version.restype = ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def rope_strerror(status: int) -> str:
+    return load_library().rope_strerror(int(status)).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise RopeError(fn, status, rope_strerror(status))
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else int(t.data_ptr())
+
+
+def _stream(stream, device) -> int:
+    import torch
+
+    if stream is None:
+        return int(torch.cuda.current_stream(device).cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _check_qk(q, k):
+    import torch
+
+    for name, t in (("q", q), ("k", k)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 3:
+            raise ValueError("%s must be a contiguous CUDA bf16 tensor [tokens, heads, head_dim]" % name)
+    if q.shape[0] != k.shape[0] or q.shape[2] != k.shape[2] or q.device != k.device:
+        raise ValueError("q and k must share tokens, head_dim and device")
+
+
+def _check_cu(cu_seqlens, device):
+    import torch
+
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.device != device or not cu_seqlens.is_contiguous():
+        raise ValueError("cu_seqlens must be a contiguous int32 tensor on the device of q")
+
+
+def _rope(fn_name, q, k, cu_seqlens, theta, in_place, q_out, k_out, cos_sin_cache, stream):
+    _check_qk(q, k)
+    _check_cu(cu_seqlens, q.device)
+    T, hq, d = q.shape
+    hkv = k.shape[1]
+    if not in_place:
+        if q_out is None or k_out is None:
+            raise ValueError("q_out and k_out are required when in_place is False")
+        _check_qk(q_out, k_out)
+        if q_out.shape != q.shape or k_out.shape != k.shape:
+            raise ValueError("q_out/k_out must have the shapes of q/k")
+    rows = 0
+    if cos_sin_cache is not None:
+        if cos_sin_cache.dim() != 3 or cos_sin_cache.shape[1:] != (d // 2, 2) or \
+                not cos_sin_cache.is_contiguous() or cos_sin_cache.device != q.device:
+            raise ValueError("cos_sin_cache must be a contiguous float32 [rows, head_dim/2, 2] tensor")
+        rows = cos_sin_cache.shape[0]
+    fn = getattr(load_library(), fn_name)
+    st = fn(_ptr(q), _ptr(k), _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, hq, hkv, d,
+            float(theta), 1 if in_place else 0, _ptr(q_out) if not in_place else None,
+            _ptr(k_out) if not in_place else None, _ptr(cos_sin_cache), rows,
+            _stream(stream, q.device))
+    _check(fn_name, st)
+    return (q, k) if in_place else (q_out, k_out)
+
+
+def rope_qk_fwd(q, k, cu_seqlens, theta: float, in_place: bool = True, q_out=None, k_out=None,
+                cos_sin_cache=None, stream=None):
+    """Rotate Q [T, Hq, d] and K [T, Hkv, d] (bf16, CUDA) by their packed positions.
+    Returns (q, k) in place, else (q_out, k_out)."""
+    return _rope("rope_qk_fwd", q, k, cu_seqlens, theta, in_place, q_out, k_out, cos_sin_cache, stream)
+
+
+def rope_qk_bwd(dq, dk, cu_seqlens, theta: float, in_place: bool = True, dq_out=None, dk_out=None,
+                cos_sin_cache=None, stream=None):
+    """Transpose rotation of the gradients dY_q, dY_k (sin negated)."""
+    return _rope("rope_qk_bwd", dq, dk, cu_seqlens, theta, in_place, dq_out, dk_out, cos_sin_cache, stream)
+
+
+def rope_cos_sin_cache_build(cache, theta: float, stream=None):
+    """Fill a float32 [rows, head_dim/2, 2] CUDA tensor with (cos, sin) per position."""
+    import torch
+
+    if cache.dtype != torch.float32 or not cache.is_cuda or not cache.is_contiguous() or \
+            cache.dim() != 3 or cache.shape[2] != 2:
+        raise ValueError("cache must be a contiguous CUDA float32 [rows, head_dim/2, 2] tensor")
+    st = load_library().rope_cos_sin_cache_build(_ptr(cache), cache.shape[0], 2 * cache.shape[1],
+                                                  float(theta), _stream(stream, cache.device))
+    _check("rope_cos_sin_cache_build", st)
+    return cache
+
+
+def new_cos_sin_cache(rows: int, head_dim: int, theta: float, device="cuda", stream=None):
+    """Allocate (through torch) and fill a cos/sin cache of ``rows`` positions."""
+    import torch
+
+    cache = torch.empty((rows, head_dim // 2, 2), dtype=torch.float32, device=device)
+    return rope_cos_sin_cache_build(cache, theta, stream)
+
+
+def rope_qk_positions(cu_seqlens, total_tokens: int, pos_out=None, stream=None):
+    """int32 [total_tokens] positions exactly as the kernels derive them (-1 outside)."""
+    import torch
+
+    if pos_out is None:
+        pos_out = torch.empty(int(total_tokens), dtype=torch.int32, device=cu_seqlens.device)
+    _check_cu(cu_seqlens, pos_out.device)
+    st = load_library().rope_qk_positions(_ptr(cu_seqlens), cu_seqlens.numel() - 1, int(total_tokens),
+                                          _ptr(pos_out), _stream(stream, cu_seqlens.device))
+    _check("rope_qk_positions", st)
+    return pos_out
+
+
+def rope_validate_cu_seqlens(cu_seqlens, total_tokens: int, err_word=None, stream=None):
+    """Device check of cu_seqlens; returns the int32 [1] device word of ROPE_CU_* bits."""
+    import torch
+
+    if err_word is None:
+        err_word = torch.empty(1, dtype=torch.int32, device=cu_seqlens.device)
+    st = load_library().rope_validate_cu_seqlens(_ptr(cu_seqlens), cu_seqlens.numel() - 1,
+                                                 int(total_tokens), _ptr(err_word),
+                                                 _stream(stream, cu_seqlens.device))
+    _check("rope_validate_cu_seqlens", st)
+    return err_word
+
+
+def rope_qk_inv_freq(theta: float, head_dim: int):
+    """Host-side inverse frequencies (numpy float32 [head_dim/2]) as the kernels use them."""
+    import numpy as np
+
+    w = np.empty(int(head_dim) // 2, dtype=np.float32)
+    st = load_library().rope_qk_inv_freq(float(theta), int(head_dim),
+                                         w.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
+    _check("rope_qk_inv_freq", st)
+    return w
+
+
+def rope_qk_abi_version() -> int:
+    return int(load_library().rope_qk_abi_version())

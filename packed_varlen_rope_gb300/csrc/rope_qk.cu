@@ -1,0 +1,521 @@
+// Packed variable-length QK rotary position embedding for GB300 (sm_103a).
+//
+// One CTA owns a tile of consecutive tokens and rotates every Q head and every K head
+// of those tokens (grouped-query attention: any n_q_heads / n_kv_heads).  Per tile:
+//   1. the first warp finds each token's sample by binary search over cu_seqlens, so
+//      positions restart at every packed-sample boundary (unsloth.ai "3x faster
+//      training with packing", section "Packing non contaminé");
+//   2. the (cos, sin) rows of the tile's positions are staged once in shared memory,
+//      from the caller's cache or evaluated on the fly (both give the same bits), and
+//      shared by all heads;
+//   3. all threads stream Q then K rows with 16-byte loads and stores: each thread
+//      takes 8 elements from each half of a head and applies
+//        y = x*cos + rotate_half(x)*sin    (section "Kernel Triton QK RoPE fusionné
+//      avec packing"), the backward being the same with sin negated (R^T).
+// The work is HBM-bound (about 0.75 flop per byte), so there are no tensor cores and
+// no fusion into a contraction.  64-bit flat offsets are a compile-time
+// specialisation, used only when an element count reaches 2^31 (section "Indexage
+// int64 pour les kernels Triton").
+//
+// Every floating-point step is an explicit round-to-nearest intrinsic so that the
+// compiler cannot contract a multiply and an add; results are bit-identical to a plain
+// sequential evaluation of the same steps on a CPU.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <type_traits>
+
+#include "rope_qk.h"
+
+namespace {
+
+constexpr int kThreads = 256;           // threads per CTA
+constexpr int kUnroll = 4;              // pair units in flight per thread (8 x 16 B loads)
+constexpr int kMaxHalf = 128;           // head_dim <= 256
+constexpr int kMaxTileTokens = 32;      // one warp resolves the tile's positions
+constexpr int64_t kMaxTokens = int64_t(1) << 24;   // fp32 positions are exact below 2^24
+
+// Division by a runtime constant for 0 <= n < 2^31 (Granlund & Montgomery, "Division
+// by invariant integers using multiplication", PLDI 1994): q = (mulhi(n, m) + n) >> l.
+struct FastDiv {
+    uint32_t d, m, l;
+};
+
+FastDiv make_fastdiv(uint32_t d)
+{
+    uint32_t l = 0;
+    while ((uint64_t(1) << l) < d) ++l;
+    uint64_t m = ((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1;
+    return FastDiv{d, uint32_t(m), l};
+}
+
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv &f)
+{
+    return (__umulhi(n, f.m) + n) >> f.l;
+}
+
+struct RopeArgs {
+    const __nv_bfloat16 *q_in;
+    const __nv_bfloat16 *k_in;
+    __nv_bfloat16 *q_out;
+    __nv_bfloat16 *k_out;
+    const int32_t *cu;
+    const float2 *cache;
+    int32_t n_seqs;
+    int32_t n_tokens;
+    int32_t hq;
+    int32_t hkv;
+    int32_t h_tot;
+    int32_t head_dim;
+    int32_t cache_rows;
+    int32_t tile_tokens;
+    int32_t in_place;
+    int32_t bwd;
+    FastDiv div_htot;
+    FastDiv div_cph;
+    float w[kMaxHalf];
+};
+
+// Position of token t: t - cu[s] for the last s in [0, n) with cu[s] <= t, or -1 when
+// t lies outside [cu[0], cu[n]).  The loop is bounded by log2(n) steps whatever cu
+// holds; a result that would not be a valid position (start < 0 or start > t, only
+// possible for a cu that is not non-decreasing) is reported as outside.
+__device__ __forceinline__ int token_position(const int32_t *__restrict__ cu, int n, int t)
+{
+    if (n <= 0) return -1;
+    const int first = __ldg(cu);
+    const int last = __ldg(cu + n);
+    if (t < first || t >= last) return -1;
+    int lo = 0, hi = n;
+    while (hi - lo > 1) {
+        const int mid = lo + ((hi - lo) >> 1);
+        if (__ldg(cu + mid) <= t) lo = mid;
+        else hi = mid;
+    }
+    const int start = __ldg(cu + lo);
+    if (start < 0 || start > t) return -1;
+    return t - start;
+}
+
+// (cos phi, sin phi) with phi = RN32(pos * w): the angle is one binary32 multiply; the
+// cosine and sine are taken in binary64 and rounded once to binary32.
+__device__ __forceinline__ float2 cos_sin_at(int pos, float w)
+{
+    const float phi = __fmul_rn(__int2float_rn(pos), w);
+    double s, c;
+    sincos(static_cast<double>(phi), &s, &c);
+    return make_float2(__double2float_rn(c), __double2float_rn(s));
+}
+
+__device__ __forceinline__ uint4 load_stream(const __nv_bfloat16 *p)
+{
+    return __ldcs(reinterpret_cast<const uint4 *>(p));
+}
+
+__device__ __forceinline__ void store_stream(__nv_bfloat16 *p, uint4 v)
+{
+    __stcs(reinterpret_cast<uint4 *>(p), v);
+}
+
+__device__ __forceinline__ uint32_t bf162_bits(__nv_bfloat162 v)
+{
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ __nv_bfloat162 bits_bf162(uint32_t u)
+{
+    return *reinterpret_cast<__nv_bfloat162 *>(&u);
+}
+
+// Rotate two bf16 pairs: a = first-half elements, b = second-half elements, with
+// (c0, s0, c1, s1) for the two frequencies.  lo' = a*c - b*s, hi' = b*c + a*s.
+__device__ __forceinline__ void rotate2(uint32_t &lo, uint32_t &hi, float4 cs)
+{
+    const __nv_bfloat162 a = bits_bf162(lo);
+    const __nv_bfloat162 b = bits_bf162(hi);
+    const float a0 = __low2float(a), a1 = __high2float(a);
+    const float b0 = __low2float(b), b1 = __high2float(b);
+    const float y0 = __fsub_rn(__fmul_rn(a0, cs.x), __fmul_rn(b0, cs.y));
+    const float z0 = __fadd_rn(__fmul_rn(b0, cs.x), __fmul_rn(a0, cs.y));
+    const float y1 = __fsub_rn(__fmul_rn(a1, cs.z), __fmul_rn(b1, cs.w));
+    const float z1 = __fadd_rn(__fmul_rn(b1, cs.z), __fmul_rn(a1, cs.w));
+    lo = bf162_bits(__floats2bfloat162_rn(y0, y1));
+    hi = bf162_bits(__floats2bfloat162_rn(z0, z1));
+}
+
+// Shared-memory (cos, sin) layout for a tile: float4 chunks indexed
+// [token][quad][chunk], where chunk c covers frequencies 8c..8c+7 and quad q holds the
+// pairs of frequencies 8c+2q and 8c+2q+1.  The eight threads of a 16-byte load phase
+// read eight consecutive float4, so the reads are free of bank conflicts.
+__device__ __forceinline__ int cs_slot(int token, int j, int cph)
+{
+    const int c = j >> 3, quad = (j >> 1) & 3, e = j & 1;
+    return ((token * 4 + quad) * cph + c) * 2 + e;
+}
+
+template <int D, bool LONG>
+__global__ void __launch_bounds__(kThreads)
+rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
+{
+    using Index = typename std::conditional<LONG, int64_t, uint32_t>::type;
+    extern __shared__ __align__(16) float2 s_cs[];
+    __shared__ int s_pos[kMaxTileTokens];
+
+    const int d = D > 0 ? D : a.head_dim;
+    const int h = d >> 1;
+    const int cph = d >> 4;
+    const int t0 = blockIdx.x * a.tile_tokens;
+    const int tt = min(a.tile_tokens, a.n_tokens - t0);
+
+    // 1. positions of the tile's tokens (one lane per token)
+    if (threadIdx.x < kMaxTileTokens) {
+        int pos = -1;
+        if (static_cast<int>(threadIdx.x) < tt)
+            pos = token_position(a.cu, a.n_seqs, t0 + static_cast<int>(threadIdx.x));
+        s_pos[threadIdx.x] = pos;
+    }
+    __syncthreads();
+
+    // 2. (cos, sin) rows of the tile, sin negated for the backward
+    for (int idx = threadIdx.x; idx < tt * h; idx += kThreads) {
+        const int i = idx / h;
+        const int j = idx - i * h;
+        const int pos = s_pos[i];
+        float2 cs = make_float2(1.0f, 0.0f);
+        if (pos >= 0) {
+            if (a.cache != nullptr && pos < a.cache_rows)
+                cs = __ldg(a.cache + static_cast<int64_t>(pos) * h + j);
+            else
+                cs = cos_sin_at(pos, a.w[j]);
+            if (a.bwd) cs.y = -cs.y;
+        }
+        s_cs[cs_slot(i, j, cph)] = cs;
+    }
+    __syncthreads();
+
+    // 3. stream the Q and K rows of the tile
+    const float4 *s_cs4 = reinterpret_cast<const float4 *>(s_cs);
+    const uint32_t units = static_cast<uint32_t>(tt) * static_cast<uint32_t>(a.h_tot * cph);
+    for (uint32_t base = threadIdx.x; base < units; base += kUnroll * kThreads) {
+        uint4 lo[kUnroll], hi[kUnroll];
+        __nv_bfloat16 *dst[kUnroll];
+        int tok[kUnroll], chunk[kUnroll];
+        bool live[kUnroll];
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+            const uint32_t u = base + k * kThreads;
+            live[k] = false;
+            tok[k] = -1;
+            chunk[k] = 0;
+            dst[k] = nullptr;
+            if (u < units) {
+                const uint32_t hr = D > 0 ? u / static_cast<uint32_t>(D >> 4) : fast_div(u, a.div_cph);
+                const uint32_t c = u - hr * static_cast<uint32_t>(cph);
+                const uint32_t i = fast_div(hr, a.div_htot);
+                const uint32_t vh = hr - i * static_cast<uint32_t>(a.h_tot);
+                const int pos = s_pos[i];
+                if (pos >= 0 || !a.in_place) {
+                    const Index t = static_cast<Index>(t0) + static_cast<Index>(i);
+                    const __nv_bfloat16 *src;
+                    Index off;
+                    if (vh < static_cast<uint32_t>(a.hq)) {
+                        off = (t * static_cast<Index>(a.hq) + static_cast<Index>(vh)) * static_cast<Index>(d);
+                        src = a.q_in;
+                        dst[k] = a.q_out;
+                    } else {
+                        off = (t * static_cast<Index>(a.hkv) + static_cast<Index>(vh - a.hq)) * static_cast<Index>(d);
+                        src = a.k_in;
+                        dst[k] = a.k_out;
+                    }
+                    off += static_cast<Index>(c * 8);
+                    src += off;
+                    dst[k] += off;
+                    lo[k] = load_stream(src);
+                    hi[k] = load_stream(src + h);
+                    live[k] = true;
+                    tok[k] = pos >= 0 ? static_cast<int>(i) : -1;
+                    chunk[k] = static_cast<int>(c);
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+            if (!live[k]) continue;
+            if (tok[k] >= 0) {
+                const float4 *cs = s_cs4 + (tok[k] * 4) * cph + chunk[k];
+                rotate2(lo[k].x, hi[k].x, cs[0]);
+                rotate2(lo[k].y, hi[k].y, cs[cph]);
+                rotate2(lo[k].z, hi[k].z, cs[2 * cph]);
+                rotate2(lo[k].w, hi[k].w, cs[3 * cph]);
+            }
+            store_stream(dst[k], lo[k]);
+            store_stream(dst[k] + h, hi[k]);
+        }
+    }
+}
+
+struct CacheArgs {
+    float w[kMaxHalf];
+};
+
+__global__ void cos_sin_cache_kernel(float2 *__restrict__ cache, int64_t rows, int h,
+                                     const __grid_constant__ CacheArgs a)
+{
+    const int64_t n = rows * h;
+    for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < n;
+         idx += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t p = idx / h;
+        const int j = static_cast<int>(idx - p * h);
+        cache[idx] = cos_sin_at(static_cast<int>(p), a.w[j]);
+    }
+}
+
+__global__ void positions_kernel(const int32_t *__restrict__ cu, int n, int n_tokens,
+                                 int32_t *__restrict__ pos_out)
+{
+    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < n_tokens; t += gridDim.x * blockDim.x)
+        pos_out[t] = token_position(cu, n, t);
+}
+
+__global__ void validate_kernel(const int32_t *__restrict__ cu, int n, int64_t n_tokens,
+                                int32_t *__restrict__ err)
+{
+    int32_t bits = 0;
+    const int64_t tid = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+    for (int64_t s = tid; s < n; s += int64_t(gridDim.x) * blockDim.x)
+        if (__ldg(cu + s + 1) < __ldg(cu + s)) bits |= ROPE_CU_DECREASING;
+    if (tid == 0) {
+        const int first = __ldg(cu);
+        if (first < 0) bits |= ROPE_CU_NEGATIVE_START;
+        if (first != 0) bits |= ROPE_CU_NONZERO_START;
+        if (static_cast<int64_t>(__ldg(cu + n)) > n_tokens) bits |= ROPE_CU_PAST_END;
+    }
+    if (bits) atomicOr(err, bits);
+}
+
+// ------------------------------------------------------------------ host side
+
+void host_inv_freq(double theta, int d, float *w)
+{
+    for (int j = 0; j < d / 2; ++j)
+        w[j] = static_cast<float>(std::pow(theta, -(2.0 * static_cast<double>(j)) / static_cast<double>(d)));
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool overlap(const void *a, int64_t na, const void *b, int64_t nb)
+{
+    if (na <= 0 || nb <= 0) return false;
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + static_cast<uintptr_t>(nb) && pb < pa + static_cast<uintptr_t>(na);
+}
+
+int check_head_dim(int32_t head_dim)
+{
+    if (head_dim < 16 || head_dim > 2 * kMaxHalf || head_dim % 16 != 0) return ROPE_ERR_HEAD_DIM;
+    return ROPE_OK;
+}
+
+int check_theta(double theta)
+{
+    if (!(theta > 0.0) || !std::isfinite(theta)) return ROPE_ERR_THETA;
+    return ROPE_OK;
+}
+
+// Tokens per tile: enough 16-byte pair units that every thread has about kUnroll * 2
+// of them, capped by the one-warp position search.
+int pick_tile_tokens(int h_tot, int head_dim)
+{
+    const int units_per_token = h_tot * (head_dim / 16);
+    const int target = 2 * kUnroll * kThreads;
+    int tt = (target + units_per_token - 1) / units_per_token;
+    if (tt < 1) tt = 1;
+    if (tt > kMaxTileTokens) tt = kMaxTileTokens;
+    return tt;
+}
+
+template <int D, bool LONG>
+cudaError_t launch_tile(const RopeArgs &a, int grid, size_t smem, cudaStream_t stream)
+{
+    rope_qk_tile_kernel<D, LONG><<<grid, kThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <bool LONG>
+cudaError_t dispatch_dim(const RopeArgs &a, int grid, size_t smem, cudaStream_t stream)
+{
+    switch (a.head_dim) {
+    case 64: return launch_tile<64, LONG>(a, grid, smem, stream);
+    case 128: return launch_tile<128, LONG>(a, grid, smem, stream);
+    case 256: return launch_tile<256, LONG>(a, grid, smem, stream);
+    default: return launch_tile<0, LONG>(a, grid, smem, stream);
+    }
+}
+
+int rope_qk_run(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_tokens,
+                int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, double theta,
+                int32_t in_place, void *q_out, void *k_out, const float *cache, int64_t cache_rows,
+                void *stream, int bwd)
+{
+    if (total_tokens < 0 || n_seqs < 0 || n_q_heads < 1 || n_kv_heads < 1 || cache_rows < 0)
+        return ROPE_ERR_SHAPE;
+    int rc = check_head_dim(head_dim);
+    if (rc != ROPE_OK) return rc;
+    if ((rc = check_theta(theta)) != ROPE_OK) return rc;
+    if (total_tokens >= kMaxTokens) return ROPE_ERR_UNSUPPORTED;
+    if (q == nullptr || k == nullptr || cu_seqlens == nullptr) return ROPE_ERR_NULL;
+    if (!in_place && (q_out == nullptr || k_out == nullptr)) return ROPE_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(k, 16)) return ROPE_ERR_ALIGN;
+    if (!in_place && (!aligned(q_out, 16) || !aligned(k_out, 16))) return ROPE_ERR_ALIGN;
+    if (cache != nullptr && !aligned(cache, 8)) return ROPE_ERR_ALIGN;
+    if (n_q_heads > (1 << 20) || n_kv_heads > (1 << 20)) return ROPE_ERR_SHAPE;
+
+    const int64_t q_elems = total_tokens * n_q_heads * head_dim;
+    const int64_t k_elems = total_tokens * n_kv_heads * head_dim;
+    const int64_t qb = q_elems * 2, kb = k_elems * 2;
+    if (overlap(q, qb, k, kb)) return ROPE_ERR_OVERLAP;
+    if (!in_place) {
+        if (overlap(q_out, qb, k_out, kb) || overlap(q_out, qb, q, qb) || overlap(q_out, qb, k, kb) ||
+            overlap(k_out, kb, q, qb) || overlap(k_out, kb, k, kb))
+            return ROPE_ERR_OVERLAP;
+    }
+    if (total_tokens == 0) return ROPE_OK;
+
+    RopeArgs a{};
+    a.q_in = static_cast<const __nv_bfloat16 *>(q);
+    a.k_in = static_cast<const __nv_bfloat16 *>(k);
+    a.q_out = static_cast<__nv_bfloat16 *>(in_place ? q : q_out);
+    a.k_out = static_cast<__nv_bfloat16 *>(in_place ? k : k_out);
+    a.cu = cu_seqlens;
+    a.cache = reinterpret_cast<const float2 *>(cache);
+    a.n_seqs = n_seqs;
+    a.n_tokens = static_cast<int32_t>(total_tokens);
+    a.hq = n_q_heads;
+    a.hkv = n_kv_heads;
+    a.h_tot = n_q_heads + n_kv_heads;
+    a.head_dim = head_dim;
+    a.cache_rows = static_cast<int32_t>(cache_rows < kMaxTokens ? cache_rows : kMaxTokens);
+    a.tile_tokens = pick_tile_tokens(a.h_tot, head_dim);
+    a.in_place = in_place ? 1 : 0;
+    a.bwd = bwd;
+    a.div_htot = make_fastdiv(static_cast<uint32_t>(a.h_tot));
+    a.div_cph = make_fastdiv(static_cast<uint32_t>(head_dim / 16));
+    host_inv_freq(theta, head_dim, a.w);
+
+    const int grid = static_cast<int>((total_tokens + a.tile_tokens - 1) / a.tile_tokens);
+    const size_t smem = static_cast<size_t>(a.tile_tokens) * (head_dim / 2) * sizeof(float2);
+    const bool long_index = (q_elems > INT32_MAX) || (k_elems > INT32_MAX);
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t err = long_index ? dispatch_dim<true>(a, grid, smem, s)
+                                       : dispatch_dim<false>(a, grid, smem, s);
+    return err == cudaSuccess ? ROPE_OK : ROPE_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+int rope_qk_fwd(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_tokens,
+                int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, double theta,
+                int32_t in_place, void *q_out, void *k_out, const float *cos_sin_cache,
+                int64_t cache_rows, void *stream)
+{
+    return rope_qk_run(q, k, cu_seqlens, n_seqs, total_tokens, n_q_heads, n_kv_heads, head_dim,
+                       theta, in_place, q_out, k_out, cos_sin_cache, cache_rows, stream, 0);
+}
+
+int rope_qk_bwd(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_tokens,
+                int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, double theta,
+                int32_t in_place, void *q_out, void *k_out, const float *cos_sin_cache,
+                int64_t cache_rows, void *stream)
+{
+    return rope_qk_run(q, k, cu_seqlens, n_seqs, total_tokens, n_q_heads, n_kv_heads, head_dim,
+                       theta, in_place, q_out, k_out, cos_sin_cache, cache_rows, stream, 1);
+}
+
+int64_t rope_cos_sin_cache_bytes(int64_t cache_rows, int32_t head_dim)
+{
+    if (cache_rows < 0 || check_head_dim(head_dim) != ROPE_OK) return -1;
+    return cache_rows * head_dim * static_cast<int64_t>(sizeof(float));
+}
+
+int rope_cos_sin_cache_build(float *cache, int64_t cache_rows, int32_t head_dim, double theta,
+                             void *stream)
+{
+    if (cache_rows < 0) return ROPE_ERR_SHAPE;
+    int rc = check_head_dim(head_dim);
+    if (rc != ROPE_OK) return rc;
+    if ((rc = check_theta(theta)) != ROPE_OK) return rc;
+    if (cache_rows > kMaxTokens) return ROPE_ERR_UNSUPPORTED;
+    if (cache_rows == 0) return ROPE_OK;
+    if (cache == nullptr) return ROPE_ERR_NULL;
+    if (!aligned(cache, 8)) return ROPE_ERR_ALIGN;
+    CacheArgs a{};
+    host_inv_freq(theta, head_dim, a.w);
+    const int h = head_dim / 2;
+    const int64_t n = cache_rows * h;
+    const int64_t blocks64 = (n + 255) / 256;
+    const int blocks = static_cast<int>(blocks64 < 152 * 64 ? blocks64 : 152 * 64);
+    cos_sin_cache_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<float2 *>(cache), cache_rows, h, a);
+    return cudaGetLastError() == cudaSuccess ? ROPE_OK : ROPE_ERR_LAUNCH;
+}
+
+int rope_qk_positions(const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_tokens,
+                      int32_t *pos_out, void *stream)
+{
+    if (total_tokens < 0 || n_seqs < 0) return ROPE_ERR_SHAPE;
+    if (total_tokens >= kMaxTokens) return ROPE_ERR_UNSUPPORTED;
+    if (total_tokens == 0) return ROPE_OK;
+    if (cu_seqlens == nullptr || pos_out == nullptr) return ROPE_ERR_NULL;
+    const int n = static_cast<int>(total_tokens);
+    const int blocks = (n + 255) / 256 < 152 * 16 ? (n + 255) / 256 : 152 * 16;
+    positions_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(cu_seqlens, n_seqs, n, pos_out);
+    return cudaGetLastError() == cudaSuccess ? ROPE_OK : ROPE_ERR_LAUNCH;
+}
+
+int rope_validate_cu_seqlens(const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_tokens,
+                             int32_t *err_word, void *stream)
+{
+    if (total_tokens < 0 || n_seqs < 0) return ROPE_ERR_SHAPE;
+    if (cu_seqlens == nullptr || err_word == nullptr) return ROPE_ERR_NULL;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(err_word, 0, sizeof(int32_t), s) != cudaSuccess) return ROPE_ERR_LAUNCH;
+    const int64_t blocks64 = (static_cast<int64_t>(n_seqs) + 255) / 256;
+    const int blocks = static_cast<int>(blocks64 < 1 ? 1 : (blocks64 < 152 * 16 ? blocks64 : 152 * 16));
+    validate_kernel<<<blocks, 256, 0, s>>>(cu_seqlens, n_seqs, total_tokens, err_word);
+    return cudaGetLastError() == cudaSuccess ? ROPE_OK : ROPE_ERR_LAUNCH;
+}
+
+int rope_qk_inv_freq(double theta, int32_t head_dim, float *w_out)
+{
+    int rc = check_head_dim(head_dim);
+    if (rc != ROPE_OK) return rc;
+    if ((rc = check_theta(theta)) != ROPE_OK) return rc;
+    if (w_out == nullptr) return ROPE_ERR_NULL;
+    host_inv_freq(theta, head_dim, w_out);
+    return ROPE_OK;
+}
+
+const char *rope_strerror(int status)
+{
+    switch (status) {
+    case ROPE_OK: return "ok";
+    case ROPE_ERR_NULL: return "a required pointer is NULL";
+    case ROPE_ERR_SHAPE: return "invalid size: negative token/sample/row count or head count < 1";
+    case ROPE_ERR_HEAD_DIM: return "head_dim must be a multiple of 16 in [16, 256]";
+    case ROPE_ERR_ALIGN: return "Q/K/outputs must be 16-byte aligned and the cos/sin cache 8-byte aligned";
+    case ROPE_ERR_OVERLAP: return "Q and K overlap, or an output overlaps an input";
+    case ROPE_ERR_UNSUPPORTED: return "total_tokens (or cache rows) must be below 2^24";
+    case ROPE_ERR_LAUNCH: return "the CUDA runtime rejected a launch";
+    case ROPE_ERR_THETA: return "theta must be finite and > 0";
+    default: return "unknown rope status";
+    }
+}
+
+int rope_qk_abi_version(void) { return ROPE_QK_ABI_VERSION; }
+
+}  // extern "C"

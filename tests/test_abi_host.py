@@ -1,0 +1,151 @@
+"""The C ABI without a GPU: exports, header validity, host-side argument checks.
+
+Every call here returns before the library touches the CUDA runtime (rejected
+arguments, or an empty pack), so it runs on a machine with no GPU.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rope_qk.h")
+
+OK, ERR_NULL, ERR_SHAPE, ERR_HEAD_DIM, ERR_ALIGN, ERR_OVERLAP, ERR_UNSUPPORTED, ERR_LAUNCH, ERR_THETA = \
+    0, -1, -2, -3, -4, -5, -6, -7, -8
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from packed_varlen_rope_gb300 import build, load_library
+
+    build.build()
+    return load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?(?:int|int64_t|char|void)\s*\*?\s*(rope_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_binding_exports():
+    from packed_varlen_rope_gb300 import EXPORTS
+
+    assert sorted(EXPORTS) == declared_functions()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True).stdout
+    for n in declared_functions():
+        assert re.search(r"\bT %s$" % n, out, flags=re.M), n
+
+
+def test_header_is_plain_c(tmp_path):
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "rope_qk.h"\nint main(void) { return ROPE_QK_ABI_VERSION == 1 ? 0 : 1; }\n')
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Werror", "-pedantic", "-I", os.path.dirname(HEADER),
+                           "-c", str(src), "-o", str(tmp_path / "use_header.o")])
+
+
+def test_abi_version_and_strerror(lib):
+    assert lib.rope_qk_abi_version() == 1
+    for code in (OK, ERR_NULL, ERR_SHAPE, ERR_HEAD_DIM, ERR_ALIGN, ERR_OVERLAP, ERR_UNSUPPORTED,
+                 ERR_LAUNCH, ERR_THETA):
+        assert lib.rope_strerror(code)
+    assert lib.rope_strerror(-99) == b"unknown rope status"
+
+
+def test_inv_freq_matches_oracle_bits(lib, oracle_mod):
+    from packed_varlen_rope_gb300 import rope_qk_inv_freq
+
+    for theta in (1.0e4, 5.0e5, 1.0e6, 2.0, 123456.789, 1.0e9):
+        for d in range(16, 257, 16):
+            assert np.array_equal(rope_qk_inv_freq(theta, d), oracle_mod.inv_freq(theta, d)), (theta, d)
+
+
+def test_cache_bytes(lib):
+    assert lib.rope_cos_sin_cache_bytes(4096, 128) == 4096 * 128 * 4
+    assert lib.rope_cos_sin_cache_bytes(-1, 128) == -1
+    assert lib.rope_cos_sin_cache_bytes(10, 72) == -1
+
+
+# fake, never-dereferenced device addresses
+Q, K, QO, KO, CU, CACHE = 0x10000000, 0x20000000, 0x30000000, 0x40000000, 0x50000000, 0x60000000
+
+
+def call(lib, fn="rope_qk_fwd", q=Q, k=K, cu=CU, n=4, T=0, hq=4, hkv=2, d=64, theta=1e4, in_place=1,
+         qo=None, ko=None, cache=None, rows=0):
+    return getattr(lib, fn)(q, k, cu, n, T, hq, hkv, d, theta, in_place, qo, ko, cache, rows, None)
+
+
+@pytest.mark.parametrize("fn", ["rope_qk_fwd", "rope_qk_bwd"])
+def test_argument_checks(lib, fn):
+    c = lambda **kw: call(lib, fn=fn, **kw)  # noqa: E731
+    assert c() == OK                                     # empty pack: nothing launched
+    assert c(T=-1) == ERR_SHAPE
+    assert c(n=-1) == ERR_SHAPE
+    assert c(hq=0) == ERR_SHAPE
+    assert c(hkv=0) == ERR_SHAPE
+    assert c(rows=-5) == ERR_SHAPE
+    for d in (0, 8, 24, 65, 72, 272, 512):
+        assert c(d=d) == ERR_HEAD_DIM, d
+    for th in (0.0, -1.0, float("nan"), float("inf")):
+        assert c(theta=th) == ERR_THETA
+    assert c(T=1 << 24) == ERR_UNSUPPORTED
+    assert c(q=None) == ERR_NULL
+    assert c(k=None) == ERR_NULL
+    assert c(cu=None) == ERR_NULL
+    assert c(in_place=0) == ERR_NULL
+    assert c(in_place=0, qo=QO) == ERR_NULL
+    assert c(q=Q + 8) == ERR_ALIGN
+    assert c(k=K + 2) == ERR_ALIGN
+    assert c(in_place=0, qo=QO + 4, ko=KO) == ERR_ALIGN
+    assert c(cache=CACHE + 4, rows=16) == ERR_ALIGN
+    assert c(in_place=0, qo=QO, ko=KO) == OK
+    # overlap checks need a non-empty pack but return before any launch
+    T = 16
+    qbytes = T * 4 * 64 * 2
+    assert c(T=T, k=Q + qbytes - 16) == ERR_OVERLAP
+    assert c(T=T, in_place=0, qo=Q, ko=KO) == ERR_OVERLAP
+    assert c(T=T, in_place=0, qo=QO, ko=QO + 16) == ERR_OVERLAP
+    assert c(T=T, in_place=0, qo=QO, ko=K + 32) == ERR_OVERLAP
+
+
+def test_other_entry_points_argument_checks(lib):
+    assert lib.rope_cos_sin_cache_build(CACHE, 0, 128, 1e6, None) == OK
+    assert lib.rope_cos_sin_cache_build(CACHE, -1, 128, 1e6, None) == ERR_SHAPE
+    assert lib.rope_cos_sin_cache_build(CACHE, 8, 100, 1e6, None) == ERR_HEAD_DIM
+    assert lib.rope_cos_sin_cache_build(CACHE, 8, 128, 0.0, None) == ERR_THETA
+    assert lib.rope_cos_sin_cache_build(CACHE, (1 << 24) + 1, 128, 1e6, None) == ERR_UNSUPPORTED
+    assert lib.rope_cos_sin_cache_build(None, 8, 128, 1e6, None) == ERR_NULL
+    assert lib.rope_cos_sin_cache_build(CACHE + 4, 8, 128, 1e6, None) == ERR_ALIGN
+    assert lib.rope_qk_positions(CU, 3, 0, Q, None) == OK
+    assert lib.rope_qk_positions(CU, -1, 8, Q, None) == ERR_SHAPE
+    assert lib.rope_qk_positions(None, 3, 8, Q, None) == ERR_NULL
+    assert lib.rope_qk_positions(CU, 3, 8, None, None) == ERR_NULL
+    assert lib.rope_qk_positions(CU, 3, 1 << 24, Q, None) == ERR_UNSUPPORTED
+    assert lib.rope_validate_cu_seqlens(None, 3, 8, Q, None) == ERR_NULL
+    assert lib.rope_validate_cu_seqlens(CU, 3, 8, None, None) == ERR_NULL
+    assert lib.rope_validate_cu_seqlens(CU, -2, 8, Q, None) == ERR_SHAPE
+    w = (ctypes.c_float * 64)()
+    assert lib.rope_qk_inv_freq(1e4, 100, w) == ERR_HEAD_DIM
+    assert lib.rope_qk_inv_freq(1e4, 128, None) == ERR_NULL
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+
+    import packed_varlen_rope_gb300 as pr
+
+    q = torch.zeros(4, 2, 64, dtype=torch.bfloat16)
+    k = torch.zeros(4, 1, 64, dtype=torch.bfloat16)
+    cu = torch.tensor([0, 4], dtype=torch.int32)
+    with pytest.raises(ValueError):
+        pr.rope_qk_fwd(q, k, cu, 1e4)

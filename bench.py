@@ -226,7 +226,7 @@ def run_reference(args, rank, world):
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 math, bf16 I/O",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "tokens_per_step": n, "n_q_heads": w.n_q_heads,
                    "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "theta": w.theta},
@@ -363,7 +363,7 @@ def run_ours(args, rank, world, local):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
         "config": {
             "workload": w.name, "total_tokens": T, "valid_tokens": pack.valid_tokens,
             "n_seqs": pack.n_seqs, "max_seq_len": max(pack.lengths), "n_q_heads": w.n_q_heads,

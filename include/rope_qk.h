@@ -58,9 +58,9 @@ typedef enum rope_status {
     ROPE_ERR_NULL = -1,         /* a required pointer is NULL */
     ROPE_ERR_SHAPE = -2,        /* total_tokens < 0, n_seqs < 0, a head count < 1, rows < 0 */
     ROPE_ERR_HEAD_DIM = -3,     /* head_dim not a multiple of 16 in [16, 256] */
-    ROPE_ERR_ALIGN = -4,        /* Q/K/output not 16-byte aligned, cache not 8-byte aligned */
+    ROPE_ERR_ALIGN = -4,        /* Q/K/output or cos/sin cache not 16-byte aligned */
     ROPE_ERR_OVERLAP = -5,      /* Q and K overlap, or an output overlaps an input */
-    ROPE_ERR_UNSUPPORTED = -6,  /* total_tokens >= 2^24 (positions no longer exact in fp32) */
+    ROPE_ERR_UNSUPPORTED = -6,  /* total_tokens >= 2^24 or cache_rows > 2^24 (fp32 positions) */
     ROPE_ERR_LAUNCH = -7,       /* the CUDA runtime refused a launch or copy */
     ROPE_ERR_THETA = -8         /* theta not finite and > 0 */
 } rope_status;
@@ -86,11 +86,10 @@ typedef enum rope_status {
  *   in_place        nonzero: write the result over q and k (q_out/k_out ignored);
  *                   zero: write to q_out/k_out (same shapes, 16-byte aligned, disjoint
  *                   from q and k); q and k are then only read.
- *   cos_sin_cache   optional device float [cache_rows][head_dim/2][2] holding (c, s)
- *                   per position as rope_cos_sin_cache_build writes them for the same
- *                   theta and head_dim; 8-byte aligned.  Positions >= cache_rows, and
- *                   every position when the cache is NULL, are evaluated on the fly
- *                   with identical results.
+ *   cos_sin_cache   optional device cache of (c, s) per position, as
+ *                   rope_cos_sin_cache_build writes it for the same theta and head_dim;
+ *                   16-byte aligned.  Positions >= cache_rows, and every position when
+ *                   the cache is NULL, are evaluated on the fly with identical results.
  *   cache_rows      rows of the cache (>= 0).
  *   stream          cudaStream_t or NULL.
  */
@@ -112,11 +111,14 @@ int rope_qk_bwd(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs,
                 void *stream);
 
 /*
- * Fill a cos/sin cache: cache[p][j] = (c, s) of position p and frequency j, for
- * p < cache_rows, j < head_dim/2, by the arithmetic above (binary64 cos/sin on the
- * device, rounded to binary32).  cache: device float, cache_rows*head_dim floats,
- * 8-byte aligned, owned by the caller.  Build it once per (theta, head_dim) with
- * cache_rows >= the longest sample; every layer and step can reuse it.
+ * Fill a cos/sin cache with (c, s) of every position p < cache_rows and frequency
+ * j < head_dim/2, by the arithmetic above (binary64 cos/sin on the device, rounded to
+ * binary32).  cache: device float[cache_rows][4][head_dim/16][4], 16-byte aligned,
+ * owned by the caller (cache_rows * head_dim floats).  Entry [p][q][c] holds
+ * (c_j, s_j, c_{j+1}, s_{j+1}) for j = 8c + 2q: chunk c covers frequencies
+ * 8c..8c+7, the order in which the rotation kernel consumes them.  Build it once per
+ * (theta, head_dim) with cache_rows >= the longest sample (at most 2^24); every layer
+ * and step can reuse it.
  */
 int rope_cos_sin_cache_build(float *cache, int64_t cache_rows, int32_t head_dim,
                              double theta, void *stream);

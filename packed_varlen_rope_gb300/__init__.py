@@ -53,7 +53,7 @@ def _autograd_function():
             dk = dk.contiguous()
             dq_out = torch.empty_like(dq)
             dk_out = torch.empty_like(dk)
-            rope_qk_bwd(dq, dk, cu_seqlens, ctx.theta, in_place=False, dq_out=dq_out, dk_out=dk_out,
+            rope_qk_bwd(dq, dk, cu_seqlens, ctx.theta, in_place=False, q_out=dq_out, k_out=dk_out,
                         cos_sin_cache=cache)
             return dq_out, dk_out, None, None, None
 

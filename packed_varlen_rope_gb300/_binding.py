@@ -121,9 +121,9 @@ def _rope(fn_name, q, k, cu_seqlens, theta, in_place, q_out, k_out, cos_sin_cach
             raise ValueError("q_out/k_out must have the shapes of q/k")
     rows = 0
     if cos_sin_cache is not None:
-        if cos_sin_cache.dim() != 3 or cos_sin_cache.shape[1:] != (d // 2, 2) or \
+        if cos_sin_cache.dim() != 4 or tuple(cos_sin_cache.shape[1:]) != (4, d // 16, 4) or \
                 not cos_sin_cache.is_contiguous() or cos_sin_cache.device != q.device:
-            raise ValueError("cos_sin_cache must be a contiguous float32 [rows, head_dim/2, 2] tensor")
+            raise ValueError("cos_sin_cache must be a contiguous float32 [rows, 4, head_dim/16, 4] tensor")
         rows = cos_sin_cache.shape[0]
     fn = getattr(load_library(), fn_name)
     st = fn(_ptr(q), _ptr(k), _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, hq, hkv, d,
@@ -141,20 +141,22 @@ def rope_qk_fwd(q, k, cu_seqlens, theta: float, in_place: bool = True, q_out=Non
     return _rope("rope_qk_fwd", q, k, cu_seqlens, theta, in_place, q_out, k_out, cos_sin_cache, stream)
 
 
-def rope_qk_bwd(dq, dk, cu_seqlens, theta: float, in_place: bool = True, dq_out=None, dk_out=None,
+def rope_qk_bwd(q, k, cu_seqlens, theta: float, in_place: bool = True, q_out=None, k_out=None,
                 cos_sin_cache=None, stream=None):
-    """Transpose rotation of the gradients dY_q, dY_k (sin negated)."""
-    return _rope("rope_qk_bwd", dq, dk, cu_seqlens, theta, in_place, dq_out, dk_out, cos_sin_cache, stream)
+    """Transpose rotation (sin negated): q and k hold the gradients dL/dY of Q and K and
+    receive dL/dX (or q_out/k_out do).  Same arguments as ``rope_qk_fwd``."""
+    return _rope("rope_qk_bwd", q, k, cu_seqlens, theta, in_place, q_out, k_out, cos_sin_cache, stream)
 
 
 def rope_cos_sin_cache_build(cache, theta: float, stream=None):
-    """Fill a float32 [rows, head_dim/2, 2] CUDA tensor with (cos, sin) per position."""
+    """Fill a float32 [rows, 4, head_dim/16, 4] CUDA tensor with (cos, sin) per position
+    (entry [p, q, c] = c_j, s_j, c_j+1, s_j+1 for j = 8c + 2q)."""
     import torch
 
     if cache.dtype != torch.float32 or not cache.is_cuda or not cache.is_contiguous() or \
-            cache.dim() != 3 or cache.shape[2] != 2:
-        raise ValueError("cache must be a contiguous CUDA float32 [rows, head_dim/2, 2] tensor")
-    st = load_library().rope_cos_sin_cache_build(_ptr(cache), cache.shape[0], 2 * cache.shape[1],
+            cache.dim() != 4 or cache.shape[1] != 4 or cache.shape[3] != 4:
+        raise ValueError("cache must be a contiguous CUDA float32 [rows, 4, head_dim/16, 4] tensor")
+    st = load_library().rope_cos_sin_cache_build(_ptr(cache), cache.shape[0], 16 * cache.shape[2],
                                                   float(theta), _stream(stream, cache.device))
     _check("rope_cos_sin_cache_build", st)
     return cache
@@ -164,8 +166,14 @@ def new_cos_sin_cache(rows: int, head_dim: int, theta: float, device="cuda", str
     """Allocate (through torch) and fill a cos/sin cache of ``rows`` positions."""
     import torch
 
-    cache = torch.empty((rows, head_dim // 2, 2), dtype=torch.float32, device=device)
+    cache = torch.empty((rows, 4, head_dim // 16, 4), dtype=torch.float32, device=device)
     return rope_cos_sin_cache_build(cache, theta, stream)
+
+
+def cache_as_cos_sin(cache_np):
+    """View a cache copied to the host (numpy [rows, 4, d/16, 4]) as [rows, d/2, 2] (c, s)."""
+    rows, _, cph, _ = cache_np.shape
+    return cache_np.transpose(0, 2, 1, 3).reshape(rows, 8 * cph, 2)
 
 
 def rope_qk_positions(cu_seqlens, total_tokens: int, pos_out=None, stream=None):

@@ -63,7 +63,7 @@ struct RopeArgs {
     __nv_bfloat16 *q_out;
     __nv_bfloat16 *k_out;
     const int32_t *cu;
-    const float2 *cache;
+    const float4 *cache;
     int32_t n_seqs;
     int32_t n_tokens;
     int32_t hq;
@@ -146,22 +146,17 @@ __device__ __forceinline__ void rotate2(uint32_t &lo, uint32_t &hi, float4 cs)
     hi = bf162_bits(__floats2bfloat162_rn(z0, z1));
 }
 
-// Shared-memory (cos, sin) layout for a tile: float4 chunks indexed
-// [token][quad][chunk], where chunk c covers frequencies 8c..8c+7 and quad q holds the
-// pairs of frequencies 8c+2q and 8c+2q+1.  The eight threads of a 16-byte load phase
-// read eight consecutive float4, so the reads are free of bank conflicts.
-__device__ __forceinline__ int cs_slot(int token, int j, int cph)
-{
-    const int c = j >> 3, quad = (j >> 1) & 3, e = j & 1;
-    return ((token * 4 + quad) * cph + c) * 2 + e;
-}
-
+// Shared-memory (cos, sin) rows of a tile use the cache's layout: per token, float4
+// entries [quad][chunk] where chunk c covers frequencies 8c..8c+7 and quad q holds
+// (cos, sin) of frequencies 8c+2q and 8c+2q+1.  The eight threads of a 16-byte load
+// phase (consecutive chunks of one head) read eight consecutive float4: no bank
+// conflicts.
 template <int D, bool LONG>
 __global__ void __launch_bounds__(kThreads)
 rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
 {
     using Index = typename std::conditional<LONG, int64_t, uint32_t>::type;
-    extern __shared__ __align__(16) float2 s_cs[];
+    extern __shared__ __align__(16) float4 s_cs[];
     __shared__ int s_pos[kMaxTileTokens];
 
     const int d = D > 0 ? D : a.head_dim;
@@ -179,25 +174,36 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
     }
     __syncthreads();
 
-    // 2. (cos, sin) rows of the tile, sin negated for the backward
-    for (int idx = threadIdx.x; idx < tt * h; idx += kThreads) {
-        const int i = idx / h;
-        const int j = idx - i * h;
+    // 2. (cos, sin) rows of the tile, sin negated for the backward.  A row is 4*cph
+    //    float4 in the cache's own [quad][chunk] order, so staging is a plain copy.
+    const int row4 = 4 * cph;
+    float4 *s_cs4w = reinterpret_cast<float4 *>(s_cs);
+    for (int idx = threadIdx.x; idx < tt * row4; idx += kThreads) {
+        const int i = idx / row4;
+        const int r = idx - i * row4;
         const int pos = s_pos[i];
-        float2 cs = make_float2(1.0f, 0.0f);
+        float4 cs = make_float4(1.0f, 0.0f, 1.0f, 0.0f);
         if (pos >= 0) {
-            if (a.cache != nullptr && pos < a.cache_rows)
-                cs = __ldg(a.cache + static_cast<int64_t>(pos) * h + j);
-            else
-                cs = cos_sin_at(pos, a.w[j]);
-            if (a.bwd) cs.y = -cs.y;
+            if (a.cache != nullptr && pos < a.cache_rows) {
+                cs = __ldg(a.cache + static_cast<int64_t>(pos) * row4 + r);
+            } else {
+                const int quad = r / cph;
+                const int j = 8 * (r - quad * cph) + 2 * quad;
+                const float2 c0 = cos_sin_at(pos, a.w[j]);
+                const float2 c1 = cos_sin_at(pos, a.w[j + 1]);
+                cs = make_float4(c0.x, c0.y, c1.x, c1.y);
+            }
+            if (a.bwd) {
+                cs.y = -cs.y;
+                cs.w = -cs.w;
+            }
         }
-        s_cs[cs_slot(i, j, cph)] = cs;
+        s_cs4w[idx] = cs;
     }
     __syncthreads();
 
     // 3. stream the Q and K rows of the tile
-    const float4 *s_cs4 = reinterpret_cast<const float4 *>(s_cs);
+    const float4 *s_cs4 = s_cs;
     const uint32_t units = static_cast<uint32_t>(tt) * static_cast<uint32_t>(a.h_tot * cph);
     for (uint32_t base = threadIdx.x; base < units; base += kUnroll * kThreads) {
         uint4 lo[kUnroll], hi[kUnroll];
@@ -261,15 +267,22 @@ struct CacheArgs {
     float w[kMaxHalf];
 };
 
-__global__ void cos_sin_cache_kernel(float2 *__restrict__ cache, int64_t rows, int h,
+// One float4 entry (cos, sin of frequencies j and j+1, j = 8*chunk + 2*quad) per
+// thread, in the [row][quad][chunk] order the rotation kernel stages.
+__global__ void cos_sin_cache_kernel(float4 *__restrict__ cache, int64_t rows, int cph,
                                      const __grid_constant__ CacheArgs a)
 {
-    const int64_t n = rows * h;
+    const int row4 = 4 * cph;
+    const int64_t n = rows * row4;
     for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < n;
          idx += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t p = idx / h;
-        const int j = static_cast<int>(idx - p * h);
-        cache[idx] = cos_sin_at(static_cast<int>(p), a.w[j]);
+        const int64_t p = idx / row4;
+        const int r = static_cast<int>(idx - p * row4);
+        const int quad = r / cph;
+        const int j = 8 * (r - quad * cph) + 2 * quad;
+        const float2 c0 = cos_sin_at(static_cast<int>(p), a.w[j]);
+        const float2 c1 = cos_sin_at(static_cast<int>(p), a.w[j + 1]);
+        cache[idx] = make_float4(c0.x, c0.y, c1.x, c1.y);
     }
 }
 
@@ -370,7 +383,7 @@ int rope_qk_run(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs, int
     if (!in_place && (q_out == nullptr || k_out == nullptr)) return ROPE_ERR_NULL;
     if (!aligned(q, 16) || !aligned(k, 16)) return ROPE_ERR_ALIGN;
     if (!in_place && (!aligned(q_out, 16) || !aligned(k_out, 16))) return ROPE_ERR_ALIGN;
-    if (cache != nullptr && !aligned(cache, 8)) return ROPE_ERR_ALIGN;
+    if (cache != nullptr && !aligned(cache, 16)) return ROPE_ERR_ALIGN;
     if (n_q_heads > (1 << 20) || n_kv_heads > (1 << 20)) return ROPE_ERR_SHAPE;
 
     const int64_t q_elems = total_tokens * n_q_heads * head_dim;
@@ -390,7 +403,7 @@ int rope_qk_run(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs, int
     a.q_out = static_cast<__nv_bfloat16 *>(in_place ? q : q_out);
     a.k_out = static_cast<__nv_bfloat16 *>(in_place ? k : k_out);
     a.cu = cu_seqlens;
-    a.cache = reinterpret_cast<const float2 *>(cache);
+    a.cache = reinterpret_cast<const float4 *>(cache);
     a.n_seqs = n_seqs;
     a.n_tokens = static_cast<int32_t>(total_tokens);
     a.hq = n_q_heads;
@@ -406,7 +419,7 @@ int rope_qk_run(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs, int
     host_inv_freq(theta, head_dim, a.w);
 
     const int grid = static_cast<int>((total_tokens + a.tile_tokens - 1) / a.tile_tokens);
-    const size_t smem = static_cast<size_t>(a.tile_tokens) * (head_dim / 2) * sizeof(float2);
+    const size_t smem = static_cast<size_t>(a.tile_tokens) * (head_dim / 2) * sizeof(float2);  // 4*cph float4 per token
     const bool long_index = (q_elems > INT32_MAX) || (k_elems > INT32_MAX);
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     const cudaError_t err = long_index ? dispatch_dim<true>(a, grid, smem, s)
@@ -452,15 +465,15 @@ int rope_cos_sin_cache_build(float *cache, int64_t cache_rows, int32_t head_dim,
     if (cache_rows > kMaxTokens) return ROPE_ERR_UNSUPPORTED;
     if (cache_rows == 0) return ROPE_OK;
     if (cache == nullptr) return ROPE_ERR_NULL;
-    if (!aligned(cache, 8)) return ROPE_ERR_ALIGN;
+    if (!aligned(cache, 16)) return ROPE_ERR_ALIGN;
     CacheArgs a{};
     host_inv_freq(theta, head_dim, a.w);
-    const int h = head_dim / 2;
-    const int64_t n = cache_rows * h;
+    const int cph = head_dim / 16;
+    const int64_t n = cache_rows * 4 * cph;
     const int64_t blocks64 = (n + 255) / 256;
     const int blocks = static_cast<int>(blocks64 < 152 * 64 ? blocks64 : 152 * 64);
     cos_sin_cache_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        reinterpret_cast<float2 *>(cache), cache_rows, h, a);
+        reinterpret_cast<float4 *>(cache), cache_rows, cph, a);
     return cudaGetLastError() == cudaSuccess ? ROPE_OK : ROPE_ERR_LAUNCH;
 }
 
@@ -507,7 +520,7 @@ const char *rope_strerror(int status)
     case ROPE_ERR_NULL: return "a required pointer is NULL";
     case ROPE_ERR_SHAPE: return "invalid size: negative token/sample/row count or head count < 1";
     case ROPE_ERR_HEAD_DIM: return "head_dim must be a multiple of 16 in [16, 256]";
-    case ROPE_ERR_ALIGN: return "Q/K/outputs must be 16-byte aligned and the cos/sin cache 8-byte aligned";
+    case ROPE_ERR_ALIGN: return "Q/K/outputs and the cos/sin cache must be 16-byte aligned";
     case ROPE_ERR_OVERLAP: return "Q and K overlap, or an output overlaps an input";
     case ROPE_ERR_UNSUPPORTED: return "total_tokens (or cache rows) must be below 2^24";
     case ROPE_ERR_LAUNCH: return "the CUDA runtime rejected a launch";

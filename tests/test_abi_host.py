@@ -108,6 +108,7 @@ def test_argument_checks(lib, fn):
     assert c(k=K + 2) == ERR_ALIGN
     assert c(in_place=0, qo=QO + 4, ko=KO) == ERR_ALIGN
     assert c(cache=CACHE + 4, rows=16) == ERR_ALIGN
+    assert c(cache=CACHE + 8, rows=16) == ERR_ALIGN
     assert c(in_place=0, qo=QO, ko=KO) == OK
     # overlap checks need a non-empty pack but return before any launch
     T = 16
@@ -125,7 +126,7 @@ def test_other_entry_points_argument_checks(lib):
     assert lib.rope_cos_sin_cache_build(CACHE, 8, 128, 0.0, None) == ERR_THETA
     assert lib.rope_cos_sin_cache_build(CACHE, (1 << 24) + 1, 128, 1e6, None) == ERR_UNSUPPORTED
     assert lib.rope_cos_sin_cache_build(None, 8, 128, 1e6, None) == ERR_NULL
-    assert lib.rope_cos_sin_cache_build(CACHE + 4, 8, 128, 1e6, None) == ERR_ALIGN
+    assert lib.rope_cos_sin_cache_build(CACHE + 8, 8, 128, 1e6, None) == ERR_ALIGN
     assert lib.rope_qk_positions(CU, 3, 0, Q, None) == OK
     assert lib.rope_qk_positions(CU, -1, 8, Q, None) == ERR_SHAPE
     assert lib.rope_qk_positions(None, 3, 8, Q, None) == ERR_NULL

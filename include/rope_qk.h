@@ -79,7 +79,8 @@ typedef enum rope_status {
  *                   [total_tokens, n_kv_heads, head_dim]; 16-byte aligned; disjoint.
  *   cu_seqlens      device int32 [n_seqs + 1] sample offsets in the token stream.
  *   n_seqs          number of samples (>= 0; 0 means nothing is inside the pack).
- *   total_tokens    T, rows of Q and K (0 <= T < 2^24; T == 0 launches nothing).
+ *   total_tokens    T, rows of Q and K (0 <= T < 2^24).  T == 0 launches nothing,
+ *                   reads no pointer and returns ROPE_OK (NULL pointers allowed).
  *   n_q_heads, n_kv_heads   >= 1 (grouped-query attention: any ratio).
  *   head_dim        d, a multiple of 16 in [16, 256].
  *   theta           rotary base (> 0, finite).

@@ -379,6 +379,7 @@ int rope_qk_run(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs, int
     if (rc != ROPE_OK) return rc;
     if ((rc = check_theta(theta)) != ROPE_OK) return rc;
     if (total_tokens >= kMaxTokens) return ROPE_ERR_UNSUPPORTED;
+    if (total_tokens == 0) return ROPE_OK;     // nothing is read or written; pointers may be NULL
     if (q == nullptr || k == nullptr || cu_seqlens == nullptr) return ROPE_ERR_NULL;
     if (!in_place && (q_out == nullptr || k_out == nullptr)) return ROPE_ERR_NULL;
     if (!aligned(q, 16) || !aligned(k, 16)) return ROPE_ERR_ALIGN;
@@ -395,7 +396,6 @@ int rope_qk_run(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs, int
             overlap(k_out, kb, q, qb) || overlap(k_out, kb, k, kb))
             return ROPE_ERR_OVERLAP;
     }
-    if (total_tokens == 0) return ROPE_OK;
 
     RopeArgs a{};
     a.q_in = static_cast<const __nv_bfloat16 *>(q);

@@ -87,8 +87,10 @@ def call(lib, fn="rope_qk_fwd", q=Q, k=K, cu=CU, n=4, T=0, hq=4, hkv=2, d=64, th
 
 @pytest.mark.parametrize("fn", ["rope_qk_fwd", "rope_qk_bwd"])
 def test_argument_checks(lib, fn):
-    c = lambda **kw: call(lib, fn=fn, **kw)  # noqa: E731
-    assert c() == OK                                     # empty pack: nothing launched
+    # every call below is rejected on the host, before anything could be launched
+    c = lambda **kw: call(lib, fn=fn, **{"T": 16, **kw})  # noqa: E731
+    assert c(T=0) == OK                                  # empty pack: nothing launched
+    assert c(T=0, q=None, k=None, cu=None) == OK         # ... and no pointer is read
     assert c(T=-1) == ERR_SHAPE
     assert c(n=-1) == ERR_SHAPE
     assert c(hq=0) == ERR_SHAPE
@@ -109,8 +111,7 @@ def test_argument_checks(lib, fn):
     assert c(in_place=0, qo=QO + 4, ko=KO) == ERR_ALIGN
     assert c(cache=CACHE + 4, rows=16) == ERR_ALIGN
     assert c(cache=CACHE + 8, rows=16) == ERR_ALIGN
-    assert c(in_place=0, qo=QO, ko=KO) == OK
-    # overlap checks need a non-empty pack but return before any launch
+    assert c(T=0, in_place=0, qo=QO, ko=KO) == OK
     T = 16
     qbytes = T * 4 * 64 * 2
     assert c(T=T, k=Q + qbytes - 16) == ERR_OVERLAP

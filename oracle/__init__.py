@@ -12,7 +12,8 @@ What each function follows (restated, not copied):
   "Packing non contaminé": position ids restart at each packed-sample boundary.
 * ``inv_freq`` / ``cos_sin`` -- rotary base ``rope_theta`` as named in the TRL
   "training beyond 1M tokens" page, YaRN section; the RoFormer frequency form is a
-  reading (the pages print no formula).
+  reading (the pages print no formula).  ``scale`` is that section's linear position
+  rescale ("position 100 000 becomes 25 000" with factor 4).
 * ``rope_rows`` / ``rope_packed`` -- unsloth.ai page, section "Kernel Triton QK
   RoPE fusionné avec packing": ``x*cos + rotate_half(x)*sin``; backward is the same
   with sin negated (``R^T``).
@@ -71,6 +72,15 @@ class Oracle:
                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
                                            ctypes.c_int32, i32p]
         lib.oracle_rope_packed.restype = ctypes.c_int
+        lib.oracle_inv_freq_scaled.argtypes = [ctypes.c_double, ctypes.c_int32, ctypes.c_double, f32p]
+        lib.oracle_inv_freq_scaled.restype = None
+        lib.oracle_cos_sin_scaled.argtypes = [ctypes.c_int32, ctypes.c_double, ctypes.c_int32, ctypes.c_double,
+                                              f32p, f32p]
+        lib.oracle_cos_sin_scaled.restype = None
+        lib.oracle_rope_rows_scaled.argtypes = [u16p, u16p, ctypes.c_int64, i32p, ctypes.c_int32,
+                                                ctypes.c_int32, ctypes.c_double, ctypes.c_double,
+                                                ctypes.c_int32]
+        lib.oracle_rope_rows_scaled.restype = None
         lib.oracle_float_to_bf16.argtypes = [ctypes.c_float]
         lib.oracle_float_to_bf16.restype = ctypes.c_uint16
         self.lib = lib
@@ -86,29 +96,32 @@ class Oracle:
             raise ValueError("cu_seqlens is not non-decreasing within [0, total_tokens]")
         return out
 
-    def inv_freq(self, theta: float, head_dim: int) -> np.ndarray:
+    def inv_freq(self, theta: float, head_dim: int, scale: float = 1.0) -> np.ndarray:
         w = np.empty(head_dim // 2, dtype=np.float32)
-        self.lib.oracle_inv_freq(float(theta), int(head_dim), _ptr(w, ctypes.c_float))
+        self.lib.oracle_inv_freq_scaled(float(theta), int(head_dim), float(scale), _ptr(w, ctypes.c_float))
         return w
 
-    def cos_sin(self, pos: int, theta: float, head_dim: int):
+    def cos_sin(self, pos: int, theta: float, head_dim: int, scale: float = 1.0):
         """(c, s) float32 arrays of length head_dim/2 for one position."""
         c = np.empty(head_dim // 2, dtype=np.float32)
         s = np.empty(head_dim // 2, dtype=np.float32)
-        self.lib.oracle_cos_sin(int(pos), float(theta), int(head_dim), _ptr(c, ctypes.c_float),
-                                _ptr(s, ctypes.c_float))
+        self.lib.oracle_cos_sin_scaled(int(pos), float(theta), int(head_dim), float(scale),
+                                       _ptr(c, ctypes.c_float), _ptr(s, ctypes.c_float))
         return c, s
 
-    def rope_rows(self, x_bits: np.ndarray, pos, theta: float, bwd: bool = False) -> np.ndarray:
+    def rope_rows(self, x_bits: np.ndarray, pos, theta: float, bwd: bool = False,
+                  scale: float = 1.0) -> np.ndarray:
         """Rotate token rows.  x_bits: uint16 bf16 bit patterns [rows, H, d]; pos: int32
-        [rows] (-1 leaves a row unchanged).  Returns a new uint16 array."""
+        [rows] (-1 leaves a row unchanged); scale: linear position rescale (1 = none).
+        Returns a new uint16 array."""
         x = np.ascontiguousarray(x_bits, dtype=np.uint16)
         rows, H, d = x.shape
         p = np.ascontiguousarray(pos, dtype=np.int32)
         assert p.shape == (rows,) and d % 2 == 0 and d <= 1024
         y = np.empty_like(x)
-        self.lib.oracle_rope_rows(_ptr(x, ctypes.c_uint16), _ptr(y, ctypes.c_uint16), rows,
-                                  _ptr(p, ctypes.c_int32), H, d, float(theta), 1 if bwd else 0)
+        self.lib.oracle_rope_rows_scaled(_ptr(x, ctypes.c_uint16), _ptr(y, ctypes.c_uint16), rows,
+                                         _ptr(p, ctypes.c_int32), H, d, float(theta), float(scale),
+                                         1 if bwd else 0)
         return y
 
     def rope_packed(self, x_bits: np.ndarray, cu_seqlens, theta: float, bwd: bool = False) -> np.ndarray:
@@ -145,16 +158,16 @@ def positions(cu_seqlens, total_tokens):
     return get().positions(cu_seqlens, total_tokens)
 
 
-def inv_freq(theta, head_dim):
-    return get().inv_freq(theta, head_dim)
+def inv_freq(theta, head_dim, scale=1.0):
+    return get().inv_freq(theta, head_dim, scale)
 
 
-def cos_sin(pos, theta, head_dim):
-    return get().cos_sin(pos, theta, head_dim)
+def cos_sin(pos, theta, head_dim, scale=1.0):
+    return get().cos_sin(pos, theta, head_dim, scale)
 
 
-def rope_rows(x_bits, pos, theta, bwd=False):
-    return get().rope_rows(x_bits, pos, theta, bwd)
+def rope_rows(x_bits, pos, theta, bwd=False, scale=1.0):
+    return get().rope_rows(x_bits, pos, theta, bwd, scale)
 
 
 def rope_packed(x_bits, cu_seqlens, theta, bwd=False):

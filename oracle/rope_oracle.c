@@ -14,17 +14,22 @@
  *        i.e. the same rotation with sin negated.
  *   [U2] same page, section "Packing non contaminé": position ids restart at
  *        every packed-sample boundary; the sequence-length metadata is kept.
- *   [U3] TRL docs, "training beyond 1M tokens" (fr), section on YaRN rescaling:
- *        names the rotary base `rope_theta`.  The frequency formula itself is not
- *        printed on the pages; the standard RoFormer form is used (reading R3).
+ *   [U3] / [T] TRL docs, "training beyond 1M tokens" (fr), section on YaRN rescaling:
+ *        names the rotary base `rope_theta` and describes the rescale as a linear map
+ *        of positions (factor 4: 40,960 trained, 163,840 wanted).  The frequency
+ *        formula itself is not printed on the pages; the standard RoFormer form is
+ *        used (reading R3).
  *
  * Readings (the pages leave these steps open; each is stated once here):
  *   R1  pos(t) = t - cu[s] for the s with cu[s] <= t < cu[s+1]; tokens with no such
  *       s (t >= cu[n], or t < cu[0]) are outside every sequence and are not rotated.
  *       For a non-decreasing cu each token has at most one such s; an empty sequence
  *       (cu[s] == cu[s+1]) owns no token.
- *   R3  inverse frequencies w_j = RN32( pow(theta, -(2j)/d) ), the power taken in
- *       binary64 with the exponent formed as -(2.0*j)/d in binary64, j in [0, d/2).
+ *   R3  inverse frequencies w_j = RN32( pow(theta, -(2j)/d) / scale ), the power and
+ *       the quotient taken in binary64 with the exponent formed as -(2.0*j)/d in
+ *       binary64, j in [0, d/2).  scale is 1 for the plain rotation.
+ *   R13 linear position rescaling ([T]: "position 100 000 becomes 25 000", factor 4):
+ *       position p is read as p / scale, done by dividing every frequency by scale.
  *   R4  angle phi = RN32( (float)pos * w_j ): one binary32 multiply.
  *   R5  c = RN32(cos((double)phi)), s = RN32(sin((double)phi)) using the host
  *       libm in binary64 (the correctly rounded binary32 value except in cases
@@ -88,25 +93,35 @@ int oracle_positions(const int32_t *cu, int32_t n_seqs, int64_t T, int32_t *pos_
 
 /* ---- frequencies and cos/sin (R3-R5, [U1], [U3]) ---------------------- */
 
-void oracle_inv_freq(double theta, int32_t d, float *w_out)
+void oracle_inv_freq_scaled(double theta, int32_t d, double scale, float *w_out)
 {
     int32_t h = d / 2;
     for (int32_t j = 0; j < h; ++j) {
         double e = -(2.0 * (double)j) / (double)d;
-        w_out[j] = (float)pow(theta, e);
+        w_out[j] = (float)(pow(theta, e) / scale);
     }
 }
 
-void oracle_cos_sin(int32_t pos, double theta, int32_t d, float *c_out, float *s_out)
+void oracle_inv_freq(double theta, int32_t d, float *w_out)
+{
+    oracle_inv_freq_scaled(theta, d, 1.0, w_out);
+}
+
+void oracle_cos_sin_scaled(int32_t pos, double theta, int32_t d, double scale, float *c_out, float *s_out)
 {
     int32_t h = d / 2;
     float w[512];
-    oracle_inv_freq(theta, d, w);
+    oracle_inv_freq_scaled(theta, d, scale, w);
     for (int32_t j = 0; j < h; ++j) {
         float phi = (float)pos * w[j];
         c_out[j] = (float)cos((double)phi);
         s_out[j] = (float)sin((double)phi);
     }
+}
+
+void oracle_cos_sin(int32_t pos, double theta, int32_t d, float *c_out, float *s_out)
+{
+    oracle_cos_sin_scaled(pos, theta, d, 1.0, c_out, s_out);
 }
 
 /* ---- rotation (R6, [U1]) ----------------------------------------------- */
@@ -115,8 +130,8 @@ void oracle_cos_sin(int32_t pos, double theta, int32_t d, float *c_out, float *s
  * pos[r] is the position of row r, or -1 to copy the row through unchanged.
  * bwd != 0 applies the transpose rotation (sin negated).  x and y may alias.
  * d must be even and at most 1024. */
-void oracle_rope_rows(const uint16_t *x, uint16_t *y, int64_t n_rows, const int32_t *pos,
-                      int32_t H, int32_t d, double theta, int32_t bwd)
+void oracle_rope_rows_scaled(const uint16_t *x, uint16_t *y, int64_t n_rows, const int32_t *pos,
+                             int32_t H, int32_t d, double theta, double scale, int32_t bwd)
 {
     int32_t h = d / 2;
     float c[512], s[512];
@@ -128,7 +143,7 @@ void oracle_rope_rows(const uint16_t *x, uint16_t *y, int64_t n_rows, const int3
                 memmove(yr, xr, sizeof(uint16_t) * (size_t)H * (size_t)d);
             continue;
         }
-        oracle_cos_sin(pos[r], theta, d, c, s);
+        oracle_cos_sin_scaled(pos[r], theta, d, scale, c, s);
         for (int32_t hd = 0; hd < H; ++hd) {
             const uint16_t *xh = xr + (int64_t)hd * d;
             uint16_t *yh = yr + (int64_t)hd * d;
@@ -147,6 +162,12 @@ void oracle_rope_rows(const uint16_t *x, uint16_t *y, int64_t n_rows, const int3
             }
         }
     }
+}
+
+void oracle_rope_rows(const uint16_t *x, uint16_t *y, int64_t n_rows, const int32_t *pos,
+                      int32_t H, int32_t d, double theta, int32_t bwd)
+{
+    oracle_rope_rows_scaled(x, y, n_rows, pos, H, d, theta, 1.0, bwd);
 }
 
 /* Whole packed tensor: positions from cu (R1), then the rotation of every token

@@ -18,7 +18,10 @@ What pins what:
   <R(m)q, R(n)k> depends on m - n only -> invariants of any rotation embedding;
 * numpy ``searchsorted`` positions, packed == each sample alone, padded == packed
   -> the position reset of the "Packing non contaminé" section;
-* torch's CPU bf16 conversion -> round to nearest even.
+* torch's CPU bf16 conversion -> round to nearest even;
+* the TRL page's worked rescale (factor 4: position 100,000 reads as 25,000, and the
+  163,840 wanted positions map onto the 40,960 trained ones) -> the linear position
+  scale (``pin_position_scale``).
 """
 from __future__ import annotations
 
@@ -278,6 +281,34 @@ def pin_bf16_rounding(o) -> None:
     assert np.array_equal(got, want)
 
 
+def pin_position_scale(o) -> None:
+    import mpmath
+
+    rng = np.random.Generator(np.random.PCG64(20))
+    x = random_bf16_bits(rng, (4, 3, 128))
+    # TRL "training beyond 1M tokens", YaRN section: factor 4, 100,000 -> 25,000 and
+    # 163,840 -> 40,960 (power-of-two factor: identical bits)
+    for theta in (1.0e6, 1.0e4):
+        for bwd in (False, True):
+            scaled = o.rope_rows(x, np.array([100000, 163840, 4, 0], np.int32), theta, bwd=bwd, scale=4.0)
+            plain = o.rope_rows(x, np.array([25000, 40960, 1, 0], np.int32), theta, bwd=bwd)
+            assert np.array_equal(scaled, plain)
+    # frequencies divided by the scale: exact for powers of two ...
+    for d in (8, 64, 128):
+        assert np.array_equal(o.inv_freq(1.0e6, d, 4.0), o.inv_freq(1.0e6, d) / np.float32(4.0))
+        assert np.array_equal(o.inv_freq(1.0e6, d, 1.0), o.inv_freq(1.0e6, d))
+    # ... and rounded once otherwise (mpmath, within one binary32 step)
+    mpmath.mp.prec = 256
+    w = o.inv_freq(5.0e5, 64, 2.5)
+    for j in range(32):
+        exact = mpmath.power(mpmath.mpf(5.0e5), mpmath.mpf(-2 * j) / 64) / mpmath.mpf(2.5)
+        want = nearest_f32(exact)
+        assert abs(int(np.float32(w[j]).view(np.int32)) - int(want.view(np.int32))) <= 1, (j, w[j], want)
+    # a scaled position is not the plain one
+    assert not np.array_equal(o.rope_rows(x, np.array([100000] * 4, np.int32), 1.0e6, scale=4.0),
+                              o.rope_rows(x, np.array([100000] * 4, np.int32), 1.0e6))
+
+
 ALL_PINS = [pin_positions, pin_inv_freq, pin_cos_sin_mpmath, pin_identity_pos0, pin_matrix,
             pin_pair_norm, pin_roundtrip, pin_packed_equals_alone, pin_padded_equals_packed,
-            pin_relative_position, pin_bf16_rounding]
+            pin_relative_position, pin_bf16_rounding, pin_position_scale]

@@ -28,7 +28,9 @@ MUTATIONS = {
     "no-position-reset": ("pos_out[t] = (int32_t)(t - start);", "pos_out[t] = (int32_t)t;"),
     "position-off-by-one": ("pos_out[t] = (int32_t)(t - start);", "pos_out[t] = (int32_t)(t - start + 1);"),
     "bwd-sign-ignored": ("float sn = bwd ? -s[i] : s[i];", "float sn = s[i];"),
-    "theta-ignored": ("w_out[j] = (float)pow(theta, e);", "w_out[j] = (float)pow(10000.0, e);"),
+    "theta-ignored": ("w_out[j] = (float)(pow(theta, e) / scale);", "w_out[j] = (float)(pow(10000.0, e) / scale);"),
+    "scale-multiplies": ("w_out[j] = (float)(pow(theta, e) / scale);", "w_out[j] = (float)(pow(theta, e) * scale);"),
+    "scale-ignored": ("w_out[j] = (float)(pow(theta, e) / scale);", "w_out[j] = (float)pow(theta, e);"),
 }
 
 

@@ -6,6 +6,6 @@ import oracle_pins
 
 @pytest.mark.parametrize("pin", oracle_pins.ALL_PINS, ids=lambda p: p.__name__)
 def test_oracle_pin(oracle_mod, pin):
-    if pin is oracle_pins.pin_cos_sin_mpmath:
+    if pin in (oracle_pins.pin_cos_sin_mpmath, oracle_pins.pin_position_scale):
         pytest.importorskip("mpmath")
     pin(oracle_mod)

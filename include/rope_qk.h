@@ -51,18 +51,20 @@
 extern "C" {
 #endif
 
-#define ROPE_QK_ABI_VERSION 1
+#define ROPE_QK_ABI_VERSION 2
 
 typedef enum rope_status {
     ROPE_OK = 0,
     ROPE_ERR_NULL = -1,         /* a required pointer is NULL */
-    ROPE_ERR_SHAPE = -2,        /* total_tokens < 0, n_seqs < 0, a head count < 1, rows < 0 */
+    ROPE_ERR_SHAPE = -2,        /* negative count, stride or offset; a head count < 1 */
     ROPE_ERR_HEAD_DIM = -3,     /* head_dim not a multiple of 16 in [16, 256] */
-    ROPE_ERR_ALIGN = -4,        /* Q/K/output or cos/sin cache not 16-byte aligned */
-    ROPE_ERR_OVERLAP = -5,      /* Q and K overlap, or an output overlaps an input */
-    ROPE_ERR_UNSUPPORTED = -6,  /* total_tokens >= 2^24 or cache_rows > 2^24 (fp32 positions) */
+    ROPE_ERR_ALIGN = -4,        /* a pointer not 16-byte aligned, a stride not a multiple of 8 */
+    ROPE_ERR_OVERLAP = -5,      /* Q and K share elements, a view overlaps itself, or an
+                                   output overlaps an input */
+    ROPE_ERR_UNSUPPORTED = -6,  /* a global token index or cache row beyond 2^24 (positions
+                                   are exact in binary32 only up to there) */
     ROPE_ERR_LAUNCH = -7,       /* the CUDA runtime refused a launch or copy */
-    ROPE_ERR_THETA = -8         /* theta not finite and > 0 */
+    ROPE_ERR_THETA = -8         /* theta or position_scale not finite and > 0 */
 } rope_status;
 
 /* Bits of the word rope_validate_cu_seqlens writes. */
@@ -79,8 +81,9 @@ typedef enum rope_status {
  *                   [total_tokens, n_kv_heads, head_dim]; 16-byte aligned; disjoint.
  *   cu_seqlens      device int32 [n_seqs + 1] sample offsets in the token stream.
  *   n_seqs          number of samples (>= 0; 0 means nothing is inside the pack).
- *   total_tokens    T, rows of Q and K (0 <= T < 2^24).  T == 0 launches nothing,
- *                   reads no pointer and returns ROPE_OK (NULL pointers allowed).
+ *   total_tokens    T, rows of Q and K (0 <= T <= 2^24, so that every position is an
+ *                   exact binary32 integer).  T == 0 launches nothing, reads no
+ *                   pointer and returns ROPE_OK (NULL pointers allowed).
  *   n_q_heads, n_kv_heads   >= 1 (grouped-query attention: any ratio).
  *   head_dim        d, a multiple of 16 in [16, 256].
  *   theta           rotary base (> 0, finite).
@@ -112,6 +115,68 @@ int rope_qk_bwd(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs,
                 void *stream);
 
 /*
+ * General form: any strided Q/K views, explicit positions or a global token offset, a
+ * linear position rescale, forward or backward, in place or out of place.
+ *
+ * Views.  Each of q, k, q_out, k_out is a bf16 [total_tokens, heads, head_dim] view with
+ * head_dim contiguous and element strides for tokens and heads (multiples of 8, >= 0;
+ * pointers 16-byte aligned).  No two (token, head) rows of one view may share an
+ * element (else ROPE_ERR_OVERLAP).  Q and K must share no element: either their address
+ * ranges are disjoint, or they step tokens by the same stride and each token's Q block
+ * and K block are disjoint -- the Q and K slices of one fused QKV projection output,
+ * e.g. qkv[T, Hq + 2*Hkv, d] with q = qkv[:, :Hq], k = qkv[:, Hq:Hq+Hkv], are accepted
+ * and rotated in place without a copy (unsloth.ai page, "Kernel Triton QK RoPE
+ * fusionné avec packing": no clones, no contiguous transposes).  q_out and k_out both
+ * NULL = in place; else both set, disjoint from each other (same rule) and with address
+ * ranges disjoint from q and k.
+ *
+ * Positions.  If position_ids is non-NULL (device int32 [total_tokens], the per-example
+ * position ids a 1-D pack carries in databricks.com "Reducing Qwen training time 6x",
+ * section on 1-D packing), row r has position position_ids[r]; a value outside
+ * [0, 2^24) leaves the row out (in place: untouched; out of place: copied).  Otherwise
+ * row r is token token_offset + r of the stream cu_seqlens describes and its position
+ * is derived as for rope_qk_fwd; token_offset lets a context-parallel shard holding
+ * tokens [a, b) of a pack pass the whole pack's cu_seqlens with token_offset = a
+ * (token_offset + total_tokens <= 2^24).
+ *
+ * position_scale.  Linear position rescale (> 0; 1.0 = none): every frequency is
+ * divided by it in binary64 before the rounding to binary32, i.e. position p acts as
+ * p / position_scale.  A cos/sin cache must come from rope_cos_sin_cache_build_scaled
+ * with the same theta, head_dim and position_scale.
+ */
+typedef struct rope_qk_desc {
+    void *q;                       /* bf16 view [total_tokens, n_q_heads, head_dim]  */
+    int64_t q_stride_token;        /* elements between consecutive tokens             */
+    int64_t q_stride_head;         /* elements between consecutive heads              */
+    void *k;                       /* bf16 view [total_tokens, n_kv_heads, head_dim] */
+    int64_t k_stride_token;
+    int64_t k_stride_head;
+    void *q_out;                   /* NULL (with k_out NULL): in place                */
+    int64_t q_out_stride_token;
+    int64_t q_out_stride_head;
+    void *k_out;
+    int64_t k_out_stride_token;
+    int64_t k_out_stride_head;
+    const int32_t *cu_seqlens;     /* device int32 [n_seqs + 1]; unused with position_ids */
+    int32_t n_seqs;
+    int32_t n_q_heads;
+    int32_t n_kv_heads;
+    int32_t head_dim;              /* multiple of 16 in [16, 256]                     */
+    const int32_t *position_ids;   /* optional device int32 [total_tokens]            */
+    int64_t total_tokens;
+    int64_t token_offset;          /* >= 0; global index of row 0 in cu_seqlens' stream */
+    double theta;
+    double position_scale;         /* 1.0 = plain rotation                            */
+    const float *cos_sin_cache;    /* optional, as for rope_qk_fwd                    */
+    int64_t cache_rows;
+    int32_t backward;              /* 0: rotation; nonzero: transpose (sin negated)   */
+    int32_t reserved;              /* set to 0                                        */
+} rope_qk_desc;
+
+/* Apply the rotation a descriptor describes (asynchronous on `stream`). */
+int rope_qk_apply(const rope_qk_desc *desc, void *stream);
+
+/*
  * Fill a cos/sin cache with (c, s) of every position p < cache_rows and frequency
  * j < head_dim/2, by the arithmetic above (binary64 cos/sin on the device, rounded to
  * binary32).  cache: device float[cache_rows][4][head_dim/16][4], 16-byte aligned,
@@ -123,6 +188,16 @@ int rope_qk_bwd(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs,
  */
 int rope_cos_sin_cache_build(float *cache, int64_t cache_rows, int32_t head_dim,
                              double theta, void *stream);
+
+/*
+ * rope_cos_sin_cache_build for a linearly rescaled position (TRL "training beyond 1M
+ * tokens", YaRN section: with factor 4, position 100,000 is read as 25,000).  Every
+ * frequency is divided by position_scale (> 0, finite) before the one rounding to
+ * binary32, as the `position_scale` field of rope_qk_desc does.  A cache serves only
+ * calls with the same theta, head_dim and position_scale.
+ */
+int rope_cos_sin_cache_build_scaled(float *cache, int64_t cache_rows, int32_t head_dim,
+                                    double theta, double position_scale, void *stream);
 
 /* Bytes a cache of `cache_rows` rows takes (cache_rows * head_dim * 4), or -1. */
 int64_t rope_cos_sin_cache_bytes(int64_t cache_rows, int32_t head_dim);
@@ -144,9 +219,10 @@ int rope_qk_positions(const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_t
 int rope_validate_cu_seqlens(const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_tokens,
                              int32_t *err_word, void *stream);
 
-/* Host-side inverse frequencies w_j (head_dim/2 floats) exactly as the kernels use
- * them.  w_out: HOST float[head_dim/2].  No CUDA call. */
-int rope_qk_inv_freq(double theta, int32_t head_dim, float *w_out);
+/* Host-side inverse frequencies w_j = (float)(pow(theta, -(2.0*j)/d) / position_scale)
+ * (head_dim/2 floats) exactly as the kernels use them; position_scale is 1.0 for the
+ * plain rotation.  w_out: HOST float[head_dim/2].  No CUDA call. */
+int rope_qk_inv_freq(double theta, int32_t head_dim, double position_scale, float *w_out);
 
 /* Static text for a status code. */
 const char *rope_strerror(int status);

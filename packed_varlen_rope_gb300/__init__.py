@@ -18,10 +18,12 @@ from ._binding import (  # noqa: F401
     ROPE_CU_NONZERO_START,
     ROPE_CU_PAST_END,
     RopeError,
+    RopeQKDesc,
     load_library,
     new_cos_sin_cache,
     rope_cos_sin_cache_build,
     rope_qk_abi_version,
+    rope_qk_apply,
     rope_qk_bwd,
     rope_qk_fwd,
     rope_qk_inv_freq,

@@ -15,9 +15,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "librope_qk.so")
 
 EXPORTS = (
-    "rope_qk_fwd", "rope_qk_bwd", "rope_cos_sin_cache_build", "rope_cos_sin_cache_bytes",
-    "rope_qk_positions", "rope_validate_cu_seqlens", "rope_qk_inv_freq", "rope_strerror",
-    "rope_qk_abi_version",
+    "rope_qk_fwd", "rope_qk_bwd", "rope_qk_apply", "rope_cos_sin_cache_build",
+    "rope_cos_sin_cache_build_scaled", "rope_cos_sin_cache_bytes", "rope_qk_positions",
+    "rope_validate_cu_seqlens", "rope_qk_inv_freq", "rope_strerror", "rope_qk_abi_version",
 )
 
 ROPE_CU_NEGATIVE_START = 0x1
@@ -26,6 +26,23 @@ ROPE_CU_PAST_END = 0x4
 ROPE_CU_NONZERO_START = 0x8
 
 _lib = None
+
+
+class RopeQKDesc(ctypes.Structure):
+    """Mirror of ``rope_qk_desc`` in include/rope_qk.h (same field order and types)."""
+
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("q_stride_token", ctypes.c_int64), ("q_stride_head", ctypes.c_int64),
+        ("k", ctypes.c_void_p), ("k_stride_token", ctypes.c_int64), ("k_stride_head", ctypes.c_int64),
+        ("q_out", ctypes.c_void_p), ("q_out_stride_token", ctypes.c_int64), ("q_out_stride_head", ctypes.c_int64),
+        ("k_out", ctypes.c_void_p), ("k_out_stride_token", ctypes.c_int64), ("k_out_stride_head", ctypes.c_int64),
+        ("cu_seqlens", ctypes.c_void_p), ("n_seqs", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
+        ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+        ("position_ids", ctypes.c_void_p), ("total_tokens", ctypes.c_int64), ("token_offset", ctypes.c_int64),
+        ("theta", ctypes.c_double), ("position_scale", ctypes.c_double),
+        ("cos_sin_cache", ctypes.c_void_p), ("cache_rows", ctypes.c_int64),
+        ("backward", ctypes.c_int32), ("reserved", ctypes.c_int32),
+    ]
 
 
 class RopeError(RuntimeError):
@@ -49,15 +66,19 @@ def load_library(path: Optional[str] = None):
     for name in ("rope_qk_fwd", "rope_qk_bwd"):
         getattr(lib, name).argtypes = rope_args
         getattr(lib, name).restype = ctypes.c_int
+    lib.rope_qk_apply.argtypes = [ctypes.POINTER(RopeQKDesc), vp]
+    lib.rope_qk_apply.restype = ctypes.c_int
     lib.rope_cos_sin_cache_build.argtypes = [vp, i64, i32, dbl, vp]
     lib.rope_cos_sin_cache_build.restype = ctypes.c_int
+    lib.rope_cos_sin_cache_build_scaled.argtypes = [vp, i64, i32, dbl, dbl, vp]
+    lib.rope_cos_sin_cache_build_scaled.restype = ctypes.c_int
     lib.rope_cos_sin_cache_bytes.argtypes = [i64, i32]
     lib.rope_cos_sin_cache_bytes.restype = ctypes.c_int64
     lib.rope_qk_positions.argtypes = [vp, i32, i64, vp, vp]
     lib.rope_qk_positions.restype = ctypes.c_int
     lib.rope_validate_cu_seqlens.argtypes = [vp, i32, i64, vp, vp]
     lib.rope_validate_cu_seqlens.restype = ctypes.c_int
-    lib.rope_qk_inv_freq.argtypes = [dbl, i32, ctypes.POINTER(ctypes.c_float)]
+    lib.rope_qk_inv_freq.argtypes = [dbl, i32, dbl, ctypes.POINTER(ctypes.c_float)]
     lib.rope_qk_inv_freq.restype = ctypes.c_int
     lib.rope_strerror.argtypes = [ctypes.c_int]
     lib.rope_strerror.restype = ctypes.c_char_p
@@ -148,26 +169,34 @@ def rope_qk_bwd(q, k, cu_seqlens, theta: float, in_place: bool = True, q_out=Non
     return _rope("rope_qk_bwd", q, k, cu_seqlens, theta, in_place, q_out, k_out, cos_sin_cache, stream)
 
 
-def rope_cos_sin_cache_build(cache, theta: float, stream=None):
+def rope_cos_sin_cache_build(cache, theta: float, stream=None, position_scale: float = 1.0):
     """Fill a float32 [rows, 4, head_dim/16, 4] CUDA tensor with (cos, sin) per position
-    (entry [p, q, c] = c_j, s_j, c_j+1, s_j+1 for j = 8c + 2q)."""
+    (entry [p, q, c] = c_j, s_j, c_j+1, s_j+1 for j = 8c + 2q).  A position_scale other
+    than 1 builds the cache of the linearly rescaled rotation."""
     import torch
 
     if cache.dtype != torch.float32 or not cache.is_cuda or not cache.is_contiguous() or \
             cache.dim() != 4 or cache.shape[1] != 4 or cache.shape[3] != 4:
         raise ValueError("cache must be a contiguous CUDA float32 [rows, 4, head_dim/16, 4] tensor")
-    st = load_library().rope_cos_sin_cache_build(_ptr(cache), cache.shape[0], 16 * cache.shape[2],
-                                                  float(theta), _stream(stream, cache.device))
-    _check("rope_cos_sin_cache_build", st)
+    lib = load_library()
+    st_ = _stream(stream, cache.device)
+    if position_scale == 1.0:
+        st = lib.rope_cos_sin_cache_build(_ptr(cache), cache.shape[0], 16 * cache.shape[2], float(theta), st_)
+        _check("rope_cos_sin_cache_build", st)
+    else:
+        st = lib.rope_cos_sin_cache_build_scaled(_ptr(cache), cache.shape[0], 16 * cache.shape[2], float(theta),
+                                                 float(position_scale), st_)
+        _check("rope_cos_sin_cache_build_scaled", st)
     return cache
 
 
-def new_cos_sin_cache(rows: int, head_dim: int, theta: float, device="cuda", stream=None):
+def new_cos_sin_cache(rows: int, head_dim: int, theta: float, device="cuda", stream=None,
+                      position_scale: float = 1.0):
     """Allocate (through torch) and fill a cos/sin cache of ``rows`` positions."""
     import torch
 
     cache = torch.empty((rows, 4, head_dim // 16, 4), dtype=torch.float32, device=device)
-    return rope_cos_sin_cache_build(cache, theta, stream)
+    return rope_cos_sin_cache_build(cache, theta, stream, position_scale)
 
 
 def cache_as_cos_sin(cache_np):
@@ -202,15 +231,79 @@ def rope_validate_cu_seqlens(cu_seqlens, total_tokens: int, err_word=None, strea
     return err_word
 
 
-def rope_qk_inv_freq(theta: float, head_dim: int):
+def rope_qk_inv_freq(theta: float, head_dim: int, position_scale: float = 1.0):
     """Host-side inverse frequencies (numpy float32 [head_dim/2]) as the kernels use them."""
     import numpy as np
 
     w = np.empty(int(head_dim) // 2, dtype=np.float32)
-    st = load_library().rope_qk_inv_freq(float(theta), int(head_dim),
+    st = load_library().rope_qk_inv_freq(float(theta), int(head_dim), float(position_scale),
                                          w.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
     _check("rope_qk_inv_freq", st)
     return w
+
+
+def _view_args(t, name):
+    import torch
+
+    if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 3 or t.stride(2) != 1:
+        raise ValueError("%s must be a CUDA bf16 [tokens, heads, head_dim] view with head_dim contiguous" % name)
+    return _ptr(t), t.stride(0), t.stride(1)
+
+
+def rope_qk_apply(q, k, theta: float, cu_seqlens=None, position_ids=None, backward: bool = False,
+                  q_out=None, k_out=None, token_offset: int = 0, position_scale: float = 1.0,
+                  cos_sin_cache=None, stream=None):
+    """General form of the rotation (C entry point ``rope_qk_apply``).
+
+    q, k: bf16 CUDA views [T, Hq, d] and [T, Hkv, d] with any token/head strides
+    (head_dim contiguous) -- e.g. the Q and K slices of one fused QKV output, rotated in
+    place.  Positions come from ``position_ids`` (int32 [T]) if given, else from
+    ``cu_seqlens`` with row r read as token ``token_offset + r``.  ``position_scale``
+    is the linear position rescale (1 = none).  Returns (q, k) in place, else (q_out,
+    k_out)."""
+    qp, q_ts, q_hs = _view_args(q, "q")
+    kp, k_ts, k_hs = _view_args(k, "k")
+    if q.shape[0] != k.shape[0] or q.shape[2] != k.shape[2] or q.device != k.device:
+        raise ValueError("q and k must share tokens, head_dim and device")
+    T, hq, d = q.shape
+    desc = RopeQKDesc()
+    desc.q, desc.q_stride_token, desc.q_stride_head = qp, q_ts, q_hs
+    desc.k, desc.k_stride_token, desc.k_stride_head = kp, k_ts, k_hs
+    if (q_out is None) != (k_out is None):
+        raise ValueError("give both q_out and k_out, or neither (in place)")
+    if q_out is not None:
+        if q_out.shape != q.shape or k_out.shape != k.shape:
+            raise ValueError("q_out/k_out must have the shapes of q/k")
+        desc.q_out, desc.q_out_stride_token, desc.q_out_stride_head = _view_args(q_out, "q_out")
+        desc.k_out, desc.k_out_stride_token, desc.k_out_stride_head = _view_args(k_out, "k_out")
+    if position_ids is not None:
+        import torch
+
+        if position_ids.dtype != torch.int32 or position_ids.device != q.device or \
+                not position_ids.is_contiguous() or position_ids.numel() != T:
+            raise ValueError("position_ids must be a contiguous int32 [tokens] tensor on the device of q")
+        desc.position_ids = _ptr(position_ids)
+    elif cu_seqlens is not None:
+        _check_cu(cu_seqlens, q.device)
+        desc.cu_seqlens = _ptr(cu_seqlens)
+        desc.n_seqs = cu_seqlens.numel() - 1
+    else:
+        raise ValueError("give cu_seqlens or position_ids")
+    desc.n_q_heads, desc.n_kv_heads, desc.head_dim = hq, k.shape[1], d
+    desc.total_tokens = T
+    desc.token_offset = int(token_offset)
+    desc.theta = float(theta)
+    desc.position_scale = float(position_scale)
+    if cos_sin_cache is not None:
+        if cos_sin_cache.dim() != 4 or tuple(cos_sin_cache.shape[1:]) != (4, d // 16, 4) or \
+                not cos_sin_cache.is_contiguous() or cos_sin_cache.device != q.device:
+            raise ValueError("cos_sin_cache must be a contiguous float32 [rows, 4, head_dim/16, 4] tensor")
+        desc.cos_sin_cache = _ptr(cos_sin_cache)
+        desc.cache_rows = cos_sin_cache.shape[0]
+    desc.backward = 1 if backward else 0
+    st = load_library().rope_qk_apply(ctypes.byref(desc), _stream(stream, q.device))
+    _check("rope_qk_apply", st)
+    return (q, k) if q_out is None else (q_out, k_out)
 
 
 def rope_qk_abi_version() -> int:

@@ -2,6 +2,7 @@
 //
 // One CTA owns a tile of consecutive tokens and rotates every Q head and every K head
 // of those tokens (grouped-query attention: any n_q_heads / n_kv_heads).  Per tile:
+//   0. every thread issues its first 16-byte loads at once, before anything else;
 //   1. the first warp finds each token's sample by binary search over cu_seqlens, so
 //      positions restart at every packed-sample boundary (unsloth.ai "3x faster
 //      training with packing", section "Packing non contaminé");
@@ -27,6 +28,7 @@
 #include <cmath>
 #include <cstdint>
 #include <type_traits>
+#include <utility>
 
 #include "rope_qk.h"
 
@@ -36,7 +38,7 @@ constexpr int kThreads = 256;           // threads per CTA
 constexpr int kUnroll = 4;              // pair units in flight per thread (8 x 16 B loads)
 constexpr int kMaxHalf = 128;           // head_dim <= 256
 constexpr int kMaxTileTokens = 32;      // one warp resolves the tile's positions
-constexpr int64_t kMaxTokens = int64_t(1) << 24;   // fp32 positions are exact below 2^24
+constexpr int64_t kMaxTokens = int64_t(1) << 24;   // positions < 2^24 are exact in fp32
 
 // Division by a runtime constant for 0 <= n < 2^31 (Granlund & Montgomery, "Division
 // by invariant integers using multiplication", PLDI 1994): q = (mulhi(n, m) + n) >> l.
@@ -62,10 +64,14 @@ struct RopeArgs {
     const __nv_bfloat16 *k_in;
     __nv_bfloat16 *q_out;
     __nv_bfloat16 *k_out;
+    int64_t q_ts, q_hs, k_ts, k_hs;          // input strides in elements (token, head)
+    int64_t qo_ts, qo_hs, ko_ts, ko_hs;      // output strides
     const int32_t *cu;
+    const int32_t *pos_ids;                  // optional per-row positions (replaces cu)
     const float4 *cache;
     int32_t n_seqs;
     int32_t n_tokens;
+    int32_t token_offset;                    // row r is token token_offset + r of cu's stream
     int32_t hq;
     int32_t hkv;
     int32_t h_tot;
@@ -162,22 +168,76 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
     const int d = D > 0 ? D : a.head_dim;
     const int h = d >> 1;
     const int cph = d >> 4;
+    const int row4 = 4 * cph;
     const int t0 = blockIdx.x * a.tile_tokens;
     const int tt = min(a.tile_tokens, a.n_tokens - t0);
+    const uint32_t units = static_cast<uint32_t>(tt) * static_cast<uint32_t>(a.h_tot * cph);
 
-    // 1. positions of the tile's tokens (one lane per token)
+    // A unit is 8 elements from each half of one head of one token: (token i, virtual
+    // head vh in [0, hq + hkv), chunk c).  Its input and output addresses:
+    auto locate = [&](uint32_t u, uint32_t &i, uint32_t &c, const __nv_bfloat16 *&src, __nv_bfloat16 *&dst) {
+        const uint32_t hr = D > 0 ? u / static_cast<uint32_t>(D >> 4) : fast_div(u, a.div_cph);
+        c = u - hr * static_cast<uint32_t>(cph);
+        i = fast_div(hr, a.div_htot);
+        const uint32_t vh = hr - i * static_cast<uint32_t>(a.h_tot);
+        const Index t = static_cast<Index>(t0) + static_cast<Index>(i);
+        const Index e = static_cast<Index>(c * 8);
+        if (vh < static_cast<uint32_t>(a.hq)) {
+            const Index hd = static_cast<Index>(vh);
+            src = a.q_in + (t * static_cast<Index>(a.q_ts) + hd * static_cast<Index>(a.q_hs) + e);
+            dst = a.q_out + (t * static_cast<Index>(a.qo_ts) + hd * static_cast<Index>(a.qo_hs) + e);
+        } else {
+            const Index hd = static_cast<Index>(vh - a.hq);
+            src = a.k_in + (t * static_cast<Index>(a.k_ts) + hd * static_cast<Index>(a.k_hs) + e);
+            dst = a.k_out + (t * static_cast<Index>(a.ko_ts) + hd * static_cast<Index>(a.ko_hs) + e);
+        }
+    };
+
+    uint4 lo[kUnroll], hi[kUnroll];
+    __nv_bfloat16 *dst[kUnroll];
+    int tok[kUnroll], chunk[kUnroll];
+    bool live[kUnroll];
+
+    // 0. the first batch of loads goes out before the positions are known, so HBM is
+    //    busy while the tile's positions and cos/sin rows are being resolved
+    uint32_t base = threadIdx.x;
+#pragma unroll
+    for (int k = 0; k < kUnroll; ++k) {
+        const uint32_t u = base + k * kThreads;
+        live[k] = u < units;
+        tok[k] = 0;
+        chunk[k] = 0;
+        dst[k] = nullptr;
+        if (live[k]) {
+            uint32_t i, c;
+            const __nv_bfloat16 *src;
+            locate(u, i, c, src, dst[k]);
+            lo[k] = load_stream(src);
+            hi[k] = load_stream(src + h);
+            tok[k] = static_cast<int>(i);
+            chunk[k] = static_cast<int>(c);
+        }
+    }
+
+    // 1. positions of the tile's tokens (one lane per token): from the caller's
+    //    position ids, else by binary search of cu_seqlens in the global token stream
     if (threadIdx.x < kMaxTileTokens) {
         int pos = -1;
-        if (static_cast<int>(threadIdx.x) < tt)
-            pos = token_position(a.cu, a.n_seqs, t0 + static_cast<int>(threadIdx.x));
+        if (static_cast<int>(threadIdx.x) < tt) {
+            const int r = t0 + static_cast<int>(threadIdx.x);
+            if (a.pos_ids != nullptr) {
+                const int p = __ldg(a.pos_ids + r);
+                pos = (p >= 0 && p < static_cast<int>(kMaxTokens)) ? p : -1;
+            } else {
+                pos = token_position(a.cu, a.n_seqs, a.token_offset + r);
+            }
+        }
         s_pos[threadIdx.x] = pos;
     }
     __syncthreads();
 
     // 2. (cos, sin) rows of the tile, sin negated for the backward.  A row is 4*cph
     //    float4 in the cache's own [quad][chunk] order, so staging is a plain copy.
-    const int row4 = 4 * cph;
-    float4 *s_cs4w = reinterpret_cast<float4 *>(s_cs);
     for (int idx = threadIdx.x; idx < tt * row4; idx += kThreads) {
         const int i = idx / row4;
         const int r = idx - i * row4;
@@ -198,67 +258,48 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
                 cs.w = -cs.w;
             }
         }
-        s_cs4w[idx] = cs;
+        s_cs[idx] = cs;
     }
     __syncthreads();
 
-    // 3. stream the Q and K rows of the tile
-    const float4 *s_cs4 = s_cs;
-    const uint32_t units = static_cast<uint32_t>(tt) * static_cast<uint32_t>(a.h_tot * cph);
-    for (uint32_t base = threadIdx.x; base < units; base += kUnroll * kThreads) {
-        uint4 lo[kUnroll], hi[kUnroll];
-        __nv_bfloat16 *dst[kUnroll];
-        int tok[kUnroll], chunk[kUnroll];
-        bool live[kUnroll];
-#pragma unroll
-        for (int k = 0; k < kUnroll; ++k) {
-            const uint32_t u = base + k * kThreads;
-            live[k] = false;
-            tok[k] = -1;
-            chunk[k] = 0;
-            dst[k] = nullptr;
-            if (u < units) {
-                const uint32_t hr = D > 0 ? u / static_cast<uint32_t>(D >> 4) : fast_div(u, a.div_cph);
-                const uint32_t c = u - hr * static_cast<uint32_t>(cph);
-                const uint32_t i = fast_div(hr, a.div_htot);
-                const uint32_t vh = hr - i * static_cast<uint32_t>(a.h_tot);
-                const int pos = s_pos[i];
-                if (pos >= 0 || !a.in_place) {
-                    const Index t = static_cast<Index>(t0) + static_cast<Index>(i);
-                    const __nv_bfloat16 *src;
-                    Index off;
-                    if (vh < static_cast<uint32_t>(a.hq)) {
-                        off = (t * static_cast<Index>(a.hq) + static_cast<Index>(vh)) * static_cast<Index>(d);
-                        src = a.q_in;
-                        dst[k] = a.q_out;
-                    } else {
-                        off = (t * static_cast<Index>(a.hkv) + static_cast<Index>(vh - a.hq)) * static_cast<Index>(d);
-                        src = a.k_in;
-                        dst[k] = a.k_out;
-                    }
-                    off += static_cast<Index>(c * 8);
-                    src += off;
-                    dst[k] += off;
-                    lo[k] = load_stream(src);
-                    hi[k] = load_stream(src + h);
-                    live[k] = true;
-                    tok[k] = pos >= 0 ? static_cast<int>(i) : -1;
-                    chunk[k] = static_cast<int>(c);
-                }
-            }
-        }
+    // 3. rotate and store the batch in registers, load the next one, until the tile is
+    //    done.  Rows of tokens outside the pack are stored unchanged out of place and
+    //    not touched in place.
+    for (;;) {
 #pragma unroll
         for (int k = 0; k < kUnroll; ++k) {
             if (!live[k]) continue;
-            if (tok[k] >= 0) {
-                const float4 *cs = s_cs4 + (tok[k] * 4) * cph + chunk[k];
+            const bool inside = s_pos[tok[k]] >= 0;
+            if (inside) {
+                const float4 *cs = s_cs + (tok[k] * 4) * cph + chunk[k];
                 rotate2(lo[k].x, hi[k].x, cs[0]);
                 rotate2(lo[k].y, hi[k].y, cs[cph]);
                 rotate2(lo[k].z, hi[k].z, cs[2 * cph]);
                 rotate2(lo[k].w, hi[k].w, cs[3 * cph]);
             }
-            store_stream(dst[k], lo[k]);
-            store_stream(dst[k] + h, hi[k]);
+            if (inside || !a.in_place) {
+                store_stream(dst[k], lo[k]);
+                store_stream(dst[k] + h, hi[k]);
+            }
+        }
+        base += kUnroll * kThreads;
+        if (base >= units) break;
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+            const uint32_t u = base + k * kThreads;
+            live[k] = false;
+            if (u < units) {
+                uint32_t i, c;
+                const __nv_bfloat16 *src;
+                locate(u, i, c, src, dst[k]);
+                if (s_pos[i] >= 0 || !a.in_place) {
+                    lo[k] = load_stream(src);
+                    hi[k] = load_stream(src + h);
+                    live[k] = true;
+                    tok[k] = static_cast<int>(i);
+                    chunk[k] = static_cast<int>(c);
+                }
+            }
         }
     }
 }
@@ -311,10 +352,12 @@ __global__ void validate_kernel(const int32_t *__restrict__ cu, int n, int64_t n
 
 // ------------------------------------------------------------------ host side
 
-void host_inv_freq(double theta, int d, float *w)
+// w_j = RN32( pow(theta, -(2j)/d) / scale ), binary64 until the one rounding; a linear
+// position rescale by `scale` (position p acts as p / scale) divides every frequency.
+void host_inv_freq(double theta, int d, double scale, float *w)
 {
     for (int j = 0; j < d / 2; ++j)
-        w[j] = static_cast<float>(std::pow(theta, -(2.0 * static_cast<double>(j)) / static_cast<double>(d)));
+        w[j] = static_cast<float>(std::pow(theta, -(2.0 * static_cast<double>(j)) / static_cast<double>(d)) / scale);
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -335,6 +378,12 @@ int check_head_dim(int32_t head_dim)
 int check_theta(double theta)
 {
     if (!(theta > 0.0) || !std::isfinite(theta)) return ROPE_ERR_THETA;
+    return ROPE_OK;
+}
+
+int check_scale(double scale)
+{
+    if (!(scale > 0.0) || !std::isfinite(scale)) return ROPE_ERR_THETA;
     return ROPE_OK;
 }
 
@@ -368,6 +417,132 @@ cudaError_t dispatch_dim(const RopeArgs &a, int grid, size_t smem, cudaStream_t 
     }
 }
 
+// A strided bf16 view of `rows` x `heads` blocks of head_dim contiguous elements.
+struct View {
+    const void *base;
+    int64_t rows, heads, ts, hs, d;
+
+    int64_t span_elems() const { return (rows - 1) * ts + (heads - 1) * hs + d; }
+    int64_t bytes() const { return span_elems() * 2; }
+};
+
+// Distinct (row, head) pairs address disjoint blocks: with the two dimensions sorted by
+// stride, the smaller stride covers a block and the larger one covers every block of
+// the smaller dimension.  A dimension of extent 1 is ignored.
+bool view_injective(const View &v)
+{
+    int64_t s1 = v.ts, n1 = v.rows, s2 = v.hs, n2 = v.heads;
+    if (n1 <= 1) { s1 = s2; n1 = n2; s2 = 0; n2 = 1; }
+    if (n2 > 1 && s2 < s1) { std::swap(s1, s2); std::swap(n1, n2); }
+    if (n1 > 1 && s1 < v.d) return false;
+    if (n2 > 1 && s2 < n1 * s1) return false;
+    return true;
+}
+
+// Two views share no element.  True when their address ranges are disjoint, or when
+// both step tokens by the same stride S, each token's block fits in S, and the second
+// view's block sits after the first's inside every period of S (the Q and K slices of
+// a fused QKV projection output).
+bool views_disjoint(const View &a, const View &b)
+{
+    if (!overlap(a.base, a.bytes(), b.base, b.bytes())) return true;
+    if (a.rows != b.rows || a.ts != b.ts || a.ts <= 0 || a.rows < 1) return false;
+    const int64_t S = a.ts;
+    const int64_t ea = (a.heads - 1) * a.hs + a.d;
+    const int64_t eb = (b.heads - 1) * b.hs + b.d;
+    if (ea > S || eb > S) return false;
+    const int64_t delta_bytes = static_cast<int64_t>(reinterpret_cast<uintptr_t>(b.base)) -
+                                static_cast<int64_t>(reinterpret_cast<uintptr_t>(a.base));
+    if (delta_bytes % 2 != 0) return false;
+    const int64_t r = ((delta_bytes / 2) % S + S) % S;
+    return r >= ea && r + eb <= S;
+}
+
+int check_view(const View &v)
+{
+    if (v.base == nullptr) return ROPE_ERR_NULL;
+    if (!aligned(v.base, 16) || v.ts % 8 != 0 || v.hs % 8 != 0) return ROPE_ERR_ALIGN;
+    if (v.ts < 0 || v.hs < 0) return ROPE_ERR_SHAPE;
+    if (!view_injective(v)) return ROPE_ERR_OVERLAP;
+    return ROPE_OK;
+}
+
+int rope_qk_apply_impl(const rope_qk_desc *dp, void *stream)
+{
+    if (dp == nullptr) return ROPE_ERR_NULL;
+    const rope_qk_desc &p = *dp;
+    const int64_t T = p.total_tokens;
+    if (T < 0 || p.n_seqs < 0 || p.n_q_heads < 1 || p.n_kv_heads < 1 || p.cache_rows < 0 ||
+        p.token_offset < 0)
+        return ROPE_ERR_SHAPE;
+    if (p.n_q_heads > (1 << 20) || p.n_kv_heads > (1 << 20)) return ROPE_ERR_SHAPE;
+    int rc = check_head_dim(p.head_dim);
+    if (rc != ROPE_OK) return rc;
+    if ((rc = check_theta(p.theta)) != ROPE_OK) return rc;
+    if ((rc = check_scale(p.position_scale)) != ROPE_OK) return rc;
+    // positions must stay exact in binary32: global token indices (cu_seqlens) below
+    // 2^24; explicit position ids outside [0, 2^24) are skipped by the kernel
+    if (p.position_ids == nullptr && p.token_offset + T > kMaxTokens) return ROPE_ERR_UNSUPPORTED;
+    if (T > INT32_MAX / 2) return ROPE_ERR_UNSUPPORTED;
+    if (T == 0) return ROPE_OK;     // nothing is read or written; pointers may be NULL
+    if (p.position_ids == nullptr && p.cu_seqlens == nullptr) return ROPE_ERR_NULL;
+    if (p.cos_sin_cache != nullptr && !aligned(p.cos_sin_cache, 16)) return ROPE_ERR_ALIGN;
+
+    const int64_t d = p.head_dim;
+    const View q{p.q, T, p.n_q_heads, p.q_stride_token, p.q_stride_head, d};
+    const View k{p.k, T, p.n_kv_heads, p.k_stride_token, p.k_stride_head, d};
+    const bool in_place = p.q_out == nullptr && p.k_out == nullptr;
+    if (!in_place && (p.q_out == nullptr || p.k_out == nullptr)) return ROPE_ERR_NULL;
+    const View qo = in_place ? q : View{p.q_out, T, p.n_q_heads, p.q_out_stride_token, p.q_out_stride_head, d};
+    const View ko = in_place ? k : View{p.k_out, T, p.n_kv_heads, p.k_out_stride_token, p.k_out_stride_head, d};
+    for (const View *v : {&q, &k, &qo, &ko})
+        if ((rc = check_view(*v)) != ROPE_OK) return rc;
+    if (!views_disjoint(q, k)) return ROPE_ERR_OVERLAP;
+    if (!in_place) {
+        if (!views_disjoint(qo, ko)) return ROPE_ERR_OVERLAP;
+        for (const View *o : {&qo, &ko})
+            for (const View *i : {&q, &k})
+                if (overlap(o->base, o->bytes(), i->base, i->bytes())) return ROPE_ERR_OVERLAP;
+    }
+
+    RopeArgs a{};
+    a.q_in = static_cast<const __nv_bfloat16 *>(p.q);
+    a.k_in = static_cast<const __nv_bfloat16 *>(p.k);
+    a.q_out = static_cast<__nv_bfloat16 *>(const_cast<void *>(qo.base));
+    a.k_out = static_cast<__nv_bfloat16 *>(const_cast<void *>(ko.base));
+    a.q_ts = q.ts;  a.q_hs = q.hs;  a.k_ts = k.ts;  a.k_hs = k.hs;
+    a.qo_ts = qo.ts; a.qo_hs = qo.hs; a.ko_ts = ko.ts; a.ko_hs = ko.hs;
+    a.cu = p.cu_seqlens;
+    a.pos_ids = p.position_ids;
+    a.cache = reinterpret_cast<const float4 *>(p.cos_sin_cache);
+    a.n_seqs = p.position_ids != nullptr ? 0 : p.n_seqs;
+    a.n_tokens = static_cast<int32_t>(T);
+    a.token_offset = static_cast<int32_t>(p.position_ids != nullptr ? 0 : p.token_offset);
+    a.hq = p.n_q_heads;
+    a.hkv = p.n_kv_heads;
+    a.h_tot = p.n_q_heads + p.n_kv_heads;
+    a.head_dim = p.head_dim;
+    a.cache_rows = static_cast<int32_t>(p.cache_rows < kMaxTokens ? p.cache_rows : kMaxTokens);
+    a.tile_tokens = pick_tile_tokens(a.h_tot, p.head_dim);
+    a.in_place = in_place ? 1 : 0;
+    a.bwd = p.backward ? 1 : 0;
+    a.div_htot = make_fastdiv(static_cast<uint32_t>(a.h_tot));
+    a.div_cph = make_fastdiv(static_cast<uint32_t>(p.head_dim / 16));
+    host_inv_freq(p.theta, p.head_dim, p.position_scale, a.w);
+
+    const int grid = static_cast<int>((T + a.tile_tokens - 1) / a.tile_tokens);
+    const size_t smem = static_cast<size_t>(a.tile_tokens) * (p.head_dim / 2) * sizeof(float2);  // 4*cph float4 per token
+    // 64-bit offsets only when some element offset of a view reaches 2^31
+    bool long_index = false;
+    for (const View *v : {&q, &k, &qo, &ko})
+        long_index = long_index || v->span_elems() > INT32_MAX;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t err = long_index ? dispatch_dim<true>(a, grid, smem, s)
+                                       : dispatch_dim<false>(a, grid, smem, s);
+    return err == cudaSuccess ? ROPE_OK : ROPE_ERR_LAUNCH;
+}
+
+// The contiguous [T, H, d] form of the two simple entry points.
 int rope_qk_run(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_tokens,
                 int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, double theta,
                 int32_t in_place, void *q_out, void *k_out, const float *cache, int64_t cache_rows,
@@ -375,56 +550,29 @@ int rope_qk_run(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs, int
 {
     if (total_tokens < 0 || n_seqs < 0 || n_q_heads < 1 || n_kv_heads < 1 || cache_rows < 0)
         return ROPE_ERR_SHAPE;
-    int rc = check_head_dim(head_dim);
-    if (rc != ROPE_OK) return rc;
-    if ((rc = check_theta(theta)) != ROPE_OK) return rc;
-    if (total_tokens >= kMaxTokens) return ROPE_ERR_UNSUPPORTED;
-    if (total_tokens == 0) return ROPE_OK;     // nothing is read or written; pointers may be NULL
-    if (q == nullptr || k == nullptr || cu_seqlens == nullptr) return ROPE_ERR_NULL;
-    if (!in_place && (q_out == nullptr || k_out == nullptr)) return ROPE_ERR_NULL;
-    if (!aligned(q, 16) || !aligned(k, 16)) return ROPE_ERR_ALIGN;
-    if (!in_place && (!aligned(q_out, 16) || !aligned(k_out, 16))) return ROPE_ERR_ALIGN;
-    if (cache != nullptr && !aligned(cache, 16)) return ROPE_ERR_ALIGN;
-    if (n_q_heads > (1 << 20) || n_kv_heads > (1 << 20)) return ROPE_ERR_SHAPE;
-
-    const int64_t q_elems = total_tokens * n_q_heads * head_dim;
-    const int64_t k_elems = total_tokens * n_kv_heads * head_dim;
-    const int64_t qb = q_elems * 2, kb = k_elems * 2;
-    if (overlap(q, qb, k, kb)) return ROPE_ERR_OVERLAP;
+    // out of place needs both outputs (a desc with no outputs would mean in place)
+    if (total_tokens > 0 && !in_place && (q_out == nullptr || k_out == nullptr)) return ROPE_ERR_NULL;
+    rope_qk_desc p{};
+    const int64_t hqd = static_cast<int64_t>(n_q_heads) * head_dim;
+    const int64_t hkd = static_cast<int64_t>(n_kv_heads) * head_dim;
+    p.q = q;  p.q_stride_token = hqd; p.q_stride_head = head_dim;
+    p.k = k;  p.k_stride_token = hkd; p.k_stride_head = head_dim;
     if (!in_place) {
-        if (overlap(q_out, qb, k_out, kb) || overlap(q_out, qb, q, qb) || overlap(q_out, qb, k, kb) ||
-            overlap(k_out, kb, q, qb) || overlap(k_out, kb, k, kb))
-            return ROPE_ERR_OVERLAP;
+        p.q_out = q_out; p.q_out_stride_token = hqd; p.q_out_stride_head = head_dim;
+        p.k_out = k_out; p.k_out_stride_token = hkd; p.k_out_stride_head = head_dim;
     }
-
-    RopeArgs a{};
-    a.q_in = static_cast<const __nv_bfloat16 *>(q);
-    a.k_in = static_cast<const __nv_bfloat16 *>(k);
-    a.q_out = static_cast<__nv_bfloat16 *>(in_place ? q : q_out);
-    a.k_out = static_cast<__nv_bfloat16 *>(in_place ? k : k_out);
-    a.cu = cu_seqlens;
-    a.cache = reinterpret_cast<const float4 *>(cache);
-    a.n_seqs = n_seqs;
-    a.n_tokens = static_cast<int32_t>(total_tokens);
-    a.hq = n_q_heads;
-    a.hkv = n_kv_heads;
-    a.h_tot = n_q_heads + n_kv_heads;
-    a.head_dim = head_dim;
-    a.cache_rows = static_cast<int32_t>(cache_rows < kMaxTokens ? cache_rows : kMaxTokens);
-    a.tile_tokens = pick_tile_tokens(a.h_tot, head_dim);
-    a.in_place = in_place ? 1 : 0;
-    a.bwd = bwd;
-    a.div_htot = make_fastdiv(static_cast<uint32_t>(a.h_tot));
-    a.div_cph = make_fastdiv(static_cast<uint32_t>(head_dim / 16));
-    host_inv_freq(theta, head_dim, a.w);
-
-    const int grid = static_cast<int>((total_tokens + a.tile_tokens - 1) / a.tile_tokens);
-    const size_t smem = static_cast<size_t>(a.tile_tokens) * (head_dim / 2) * sizeof(float2);  // 4*cph float4 per token
-    const bool long_index = (q_elems > INT32_MAX) || (k_elems > INT32_MAX);
-    const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const cudaError_t err = long_index ? dispatch_dim<true>(a, grid, smem, s)
-                                       : dispatch_dim<false>(a, grid, smem, s);
-    return err == cudaSuccess ? ROPE_OK : ROPE_ERR_LAUNCH;
+    p.cu_seqlens = cu_seqlens;
+    p.n_seqs = n_seqs;
+    p.total_tokens = total_tokens;
+    p.n_q_heads = n_q_heads;
+    p.n_kv_heads = n_kv_heads;
+    p.head_dim = head_dim;
+    p.backward = bwd;
+    p.theta = theta;
+    p.position_scale = 1.0;
+    p.cos_sin_cache = cache;
+    p.cache_rows = cache_rows;
+    return rope_qk_apply_impl(&p, stream);
 }
 
 }  // namespace
@@ -455,19 +603,20 @@ int64_t rope_cos_sin_cache_bytes(int64_t cache_rows, int32_t head_dim)
     return cache_rows * head_dim * static_cast<int64_t>(sizeof(float));
 }
 
-int rope_cos_sin_cache_build(float *cache, int64_t cache_rows, int32_t head_dim, double theta,
-                             void *stream)
+int rope_cos_sin_cache_build_scaled(float *cache, int64_t cache_rows, int32_t head_dim, double theta,
+                                    double position_scale, void *stream)
 {
     if (cache_rows < 0) return ROPE_ERR_SHAPE;
     int rc = check_head_dim(head_dim);
     if (rc != ROPE_OK) return rc;
     if ((rc = check_theta(theta)) != ROPE_OK) return rc;
+    if ((rc = check_scale(position_scale)) != ROPE_OK) return rc;
     if (cache_rows > kMaxTokens) return ROPE_ERR_UNSUPPORTED;
     if (cache_rows == 0) return ROPE_OK;
     if (cache == nullptr) return ROPE_ERR_NULL;
     if (!aligned(cache, 16)) return ROPE_ERR_ALIGN;
     CacheArgs a{};
-    host_inv_freq(theta, head_dim, a.w);
+    host_inv_freq(theta, head_dim, position_scale, a.w);
     const int cph = head_dim / 16;
     const int64_t n = cache_rows * 4 * cph;
     const int64_t blocks64 = (n + 255) / 256;
@@ -477,11 +626,22 @@ int rope_cos_sin_cache_build(float *cache, int64_t cache_rows, int32_t head_dim,
     return cudaGetLastError() == cudaSuccess ? ROPE_OK : ROPE_ERR_LAUNCH;
 }
 
+int rope_cos_sin_cache_build(float *cache, int64_t cache_rows, int32_t head_dim, double theta,
+                             void *stream)
+{
+    return rope_cos_sin_cache_build_scaled(cache, cache_rows, head_dim, theta, 1.0, stream);
+}
+
+int rope_qk_apply(const rope_qk_desc *desc, void *stream)
+{
+    return rope_qk_apply_impl(desc, stream);
+}
+
 int rope_qk_positions(const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_tokens,
                       int32_t *pos_out, void *stream)
 {
     if (total_tokens < 0 || n_seqs < 0) return ROPE_ERR_SHAPE;
-    if (total_tokens >= kMaxTokens) return ROPE_ERR_UNSUPPORTED;
+    if (total_tokens > kMaxTokens) return ROPE_ERR_UNSUPPORTED;
     if (total_tokens == 0) return ROPE_OK;
     if (cu_seqlens == nullptr || pos_out == nullptr) return ROPE_ERR_NULL;
     const int n = static_cast<int>(total_tokens);
@@ -503,13 +663,14 @@ int rope_validate_cu_seqlens(const int32_t *cu_seqlens, int32_t n_seqs, int64_t 
     return cudaGetLastError() == cudaSuccess ? ROPE_OK : ROPE_ERR_LAUNCH;
 }
 
-int rope_qk_inv_freq(double theta, int32_t head_dim, float *w_out)
+int rope_qk_inv_freq(double theta, int32_t head_dim, double position_scale, float *w_out)
 {
     int rc = check_head_dim(head_dim);
     if (rc != ROPE_OK) return rc;
     if ((rc = check_theta(theta)) != ROPE_OK) return rc;
+    if ((rc = check_scale(position_scale)) != ROPE_OK) return rc;
     if (w_out == nullptr) return ROPE_ERR_NULL;
-    host_inv_freq(theta, head_dim, w_out);
+    host_inv_freq(theta, head_dim, position_scale, w_out);
     return ROPE_OK;
 }
 
@@ -518,13 +679,13 @@ const char *rope_strerror(int status)
     switch (status) {
     case ROPE_OK: return "ok";
     case ROPE_ERR_NULL: return "a required pointer is NULL";
-    case ROPE_ERR_SHAPE: return "invalid size: negative token/sample/row count or head count < 1";
+    case ROPE_ERR_SHAPE: return "invalid size or stride: negative count/stride/offset or head count < 1";
     case ROPE_ERR_HEAD_DIM: return "head_dim must be a multiple of 16 in [16, 256]";
-    case ROPE_ERR_ALIGN: return "Q/K/outputs and the cos/sin cache must be 16-byte aligned";
-    case ROPE_ERR_OVERLAP: return "Q and K overlap, or an output overlaps an input";
-    case ROPE_ERR_UNSUPPORTED: return "total_tokens (or cache rows) must be below 2^24";
+    case ROPE_ERR_ALIGN: return "Q/K/outputs and the cos/sin cache must be 16-byte aligned, strides multiples of 8 elements";
+    case ROPE_ERR_OVERLAP: return "Q and K overlap, a view overlaps itself, or an output overlaps an input";
+    case ROPE_ERR_UNSUPPORTED: return "global token indices and cache rows must stay within 2^24 (exact fp32 positions)";
     case ROPE_ERR_LAUNCH: return "the CUDA runtime rejected a launch";
-    case ROPE_ERR_THETA: return "theta must be finite and > 0";
+    case ROPE_ERR_THETA: return "theta and position_scale must be finite and > 0";
     default: return "unknown rope status";
     }
 }

@@ -49,13 +49,13 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_header_is_plain_c(tmp_path):
     src = tmp_path / "use_header.c"
-    src.write_text('#include "rope_qk.h"\nint main(void) { return ROPE_QK_ABI_VERSION == 1 ? 0 : 1; }\n')
+    src.write_text('#include "rope_qk.h"\nint main(void) { return ROPE_QK_ABI_VERSION == 2 ? 0 : 1; }\n')
     subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Werror", "-pedantic", "-I", os.path.dirname(HEADER),
                            "-c", str(src), "-o", str(tmp_path / "use_header.o")])
 
 
 def test_abi_version_and_strerror(lib):
-    assert lib.rope_qk_abi_version() == 1
+    assert lib.rope_qk_abi_version() == 2
     for code in (OK, ERR_NULL, ERR_SHAPE, ERR_HEAD_DIM, ERR_ALIGN, ERR_OVERLAP, ERR_UNSUPPORTED,
                  ERR_LAUNCH, ERR_THETA):
         assert lib.rope_strerror(code)
@@ -67,7 +67,25 @@ def test_inv_freq_matches_oracle_bits(lib, oracle_mod):
 
     for theta in (1.0e4, 5.0e5, 1.0e6, 2.0, 123456.789, 1.0e9):
         for d in range(16, 257, 16):
-            assert np.array_equal(rope_qk_inv_freq(theta, d), oracle_mod.inv_freq(theta, d)), (theta, d)
+            for scale in (1.0, 4.0, 2.5, 0.5, 7.0):
+                assert np.array_equal(rope_qk_inv_freq(theta, d, scale),
+                                      oracle_mod.inv_freq(theta, d, scale)), (theta, d, scale)
+
+
+def test_desc_layout_matches_header(tmp_path):
+    """The ctypes mirror of rope_qk_desc has the C struct's offsets and size."""
+    from packed_varlen_rope_gb300 import RopeQKDesc
+
+    names = [f[0] for f in RopeQKDesc._fields_]
+    body = "".join('printf("%%zu\\n", offsetof(rope_qk_desc, %s));' % n for n in names)
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "rope_qk.h"\n'
+                   'int main(void) { %s printf("%%zu\\n", sizeof(rope_qk_desc)); return 0; }\n' % body)
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-std=c99", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)])
+    got = [int(v) for v in subprocess.check_output([str(exe)]).split()]
+    want = [getattr(RopeQKDesc, n).offset for n in names] + [ctypes.sizeof(RopeQKDesc)]
+    assert got == want
 
 
 def test_cache_bytes(lib):
@@ -100,7 +118,7 @@ def test_argument_checks(lib, fn):
         assert c(d=d) == ERR_HEAD_DIM, d
     for th in (0.0, -1.0, float("nan"), float("inf")):
         assert c(theta=th) == ERR_THETA
-    assert c(T=1 << 24) == ERR_UNSUPPORTED
+    assert c(T=(1 << 24) + 1) == ERR_UNSUPPORTED
     assert c(q=None) == ERR_NULL
     assert c(k=None) == ERR_NULL
     assert c(cu=None) == ERR_NULL
@@ -132,13 +150,56 @@ def test_other_entry_points_argument_checks(lib):
     assert lib.rope_qk_positions(CU, -1, 8, Q, None) == ERR_SHAPE
     assert lib.rope_qk_positions(None, 3, 8, Q, None) == ERR_NULL
     assert lib.rope_qk_positions(CU, 3, 8, None, None) == ERR_NULL
-    assert lib.rope_qk_positions(CU, 3, 1 << 24, Q, None) == ERR_UNSUPPORTED
+    assert lib.rope_qk_positions(CU, 3, (1 << 24) + 1, Q, None) == ERR_UNSUPPORTED
     assert lib.rope_validate_cu_seqlens(None, 3, 8, Q, None) == ERR_NULL
     assert lib.rope_validate_cu_seqlens(CU, 3, 8, None, None) == ERR_NULL
     assert lib.rope_validate_cu_seqlens(CU, -2, 8, Q, None) == ERR_SHAPE
     w = (ctypes.c_float * 64)()
-    assert lib.rope_qk_inv_freq(1e4, 100, w) == ERR_HEAD_DIM
-    assert lib.rope_qk_inv_freq(1e4, 128, None) == ERR_NULL
+    assert lib.rope_qk_inv_freq(1e4, 100, 1.0, w) == ERR_HEAD_DIM
+    assert lib.rope_qk_inv_freq(1e4, 128, 1.0, None) == ERR_NULL
+    assert lib.rope_qk_inv_freq(1e4, 128, 0.0, w) == ERR_THETA
+    assert lib.rope_cos_sin_cache_build_scaled(CACHE, 8, 128, 1e6, -2.0, None) == ERR_THETA
+    assert lib.rope_cos_sin_cache_build_scaled(CACHE, 0, 128, 1e6, 4.0, None) == OK
+
+
+def _desc(T=16, hq=4, hkv=2, d=64, **kw):
+    from packed_varlen_rope_gb300 import RopeQKDesc
+
+    p = RopeQKDesc()
+    p.q, p.q_stride_token, p.q_stride_head = Q, hq * d, d
+    p.k, p.k_stride_token, p.k_stride_head = K, hkv * d, d
+    p.cu_seqlens, p.n_seqs = CU, 3
+    p.n_q_heads, p.n_kv_heads, p.head_dim = hq, hkv, d
+    p.total_tokens, p.theta, p.position_scale = T, 1e4, 1.0
+    for key, v in kw.items():
+        setattr(p, key, v)
+    return p
+
+
+def test_apply_argument_checks(lib):
+    """rope_qk_apply rejections (every one happens on the host, before any launch)."""
+    a = lambda **kw: lib.rope_qk_apply(ctypes.byref(_desc(**kw)), None)  # noqa: E731
+    assert lib.rope_qk_apply(None, None) == ERR_NULL
+    assert a(T=0) == OK
+    assert a(T=0, q=None, k=None, cu_seqlens=None) == OK
+    assert a(position_scale=0.0) == ERR_THETA
+    assert a(position_scale=float("nan")) == ERR_THETA
+    assert a(token_offset=-1) == ERR_SHAPE
+    assert a(token_offset=(1 << 24) - 8) == ERR_UNSUPPORTED        # global tokens past 2^24
+    assert a(cu_seqlens=None) == ERR_NULL
+    assert a(q_stride_token=4 * 64 + 4) == ERR_ALIGN                # stride not a multiple of 8
+    assert a(k_stride_head=60) == ERR_ALIGN
+    assert a(q_stride_head=56) == ERR_OVERLAP                       # heads overlap (stride < d)
+    assert a(q_stride_token=128) == ERR_OVERLAP                     # tokens overlap the 4 heads
+    assert a(q_stride_token=-256) == ERR_SHAPE
+    # fused QKV buffer: Q and K slices may interleave, but not share elements
+    S = (4 + 2 * 2) * 64
+    assert a(q_stride_token=S, k=Q + 3 * 64 * 2, k_stride_token=S) == ERR_OVERLAP   # K starts inside Q
+    assert a(q_stride_token=S, k=Q + 4 * 64 * 2, k_stride_token=S + 8) == ERR_OVERLAP  # strides differ
+    # out of place: both outputs or none, and outputs away from inputs
+    assert a(q_out=QO) == ERR_NULL
+    assert a(q_out=QO, q_out_stride_token=256, q_out_stride_head=64, k_out=Q, k_out_stride_token=128,
+             k_out_stride_head=64) == ERR_OVERLAP
 
 
 def test_binding_rejects_cpu_tensors():

@@ -1,0 +1,270 @@
+"""The general entry point rope_qk_apply against the CPU oracle (needs a GB300).
+
+Covers strided views (the Q and K slices of a fused QKV projection output rotated in
+place, head-major layouts, strided outputs), explicit position ids, context-parallel
+shards through a global token offset, and the linear position rescale.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from parity_util import assert_parity, compare, from_bits, to_bits
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from packed_varlen_rope_gb300 import build
+
+    build.build()
+    oracle.build()
+    return torch.device("cuda:0")
+
+
+def pr():
+    import packed_varlen_rope_gb300 as m
+
+    return m
+
+
+def _bits(rng, shape):
+    f = torch.from_numpy(rng.standard_normal(size=shape).astype(np.float32))
+    return f.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _pack(rng, n, max_len, extra=0):
+    lengths = rng.integers(0, max_len + 1, size=n)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    return cu, int(cu[-1]) + extra
+
+
+def _expect(x_bits, pos, theta, bwd=False, scale=1.0):
+    return oracle.rope_rows(x_bits, pos, theta, bwd=bwd, scale=scale)
+
+
+def _check(got_bits, ref_bits, x_bits, what):
+    s = compare(got_bits, ref_bits, x_bits)
+    assert_parity(s, what)
+    assert s["bit_mismatch"] == 0, (what, s)
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (4, 2, 64), (6, 1, 96), (8, 8, 256)])
+@pytest.mark.parametrize("bwd", [False, True])
+def test_fused_qkv_in_place(dev, hq, hkv, d, bwd):
+    rng = np.random.Generator(np.random.PCG64(hq * 1000 + d))
+    cu, T = _pack(rng, 9, 300, extra=5)
+    qkv_bits = _bits(rng, (T, hq + 2 * hkv, d))
+    qkv = from_bits(qkv_bits, dev)
+    q, k = qkv[:, :hq], qkv[:, hq:hq + hkv]
+    pr().rope_qk_apply(q, k, 1.0e6, cu_seqlens=torch.from_numpy(cu).to(dev), backward=bwd)
+    torch.cuda.synchronize()
+    out = to_bits(qkv)
+    pos = oracle.positions(cu, T)
+    _check(out[:, :hq], _expect(qkv_bits[:, :hq], pos, 1.0e6, bwd), qkv_bits[:, :hq], "fused q")
+    _check(out[:, hq:hq + hkv], _expect(qkv_bits[:, hq:hq + hkv], pos, 1.0e6, bwd),
+           qkv_bits[:, hq:hq + hkv], "fused k")
+    assert np.array_equal(out[:, hq + hkv:], qkv_bits[:, hq + hkv:])          # V untouched
+
+
+def test_fused_qkv_workload2_with_cache(dev):
+    """Qwen3-4B shape, 16,384 packed tokens, rotated inside its fused QKV buffer."""
+    from packed_varlen_rope_gb300 import workloads as wl
+
+    w = wl.WORKLOADS[2]
+    pack = wl.make_pack(w)
+    T, hq, hkv, d = pack.total_tokens, w.n_q_heads, w.n_kv_heads, w.head_dim
+    qkv = wl.normal_bf16((T, hq + 2 * hkv, d), 91, device="cuda")
+    before = to_bits(qkv)
+    cache = pr().new_cos_sin_cache(max(pack.lengths), d, w.theta, device=dev)
+    pr().rope_qk_apply(qkv[:, :hq], qkv[:, hq:hq + hkv], w.theta,
+                       cu_seqlens=torch.from_numpy(pack.cu_seqlens).to(dev), cos_sin_cache=cache)
+    torch.cuda.synchronize()
+    out = to_bits(qkv)
+    pos = oracle.positions(pack.cu_seqlens, T)
+    for sl in (slice(0, hq), slice(hq, hq + hkv)):
+        _check(out[:, sl], _expect(before[:, sl], pos, w.theta), before[:, sl], "w2 fused")
+    assert np.array_equal(out[:, hq + hkv:], before[:, hq + hkv:])
+
+
+def test_head_major_views(dev):
+    """Q stored [H, T, d] (a transposed view): token stride d, head stride T*d."""
+    rng = np.random.Generator(np.random.PCG64(5))
+    cu, T = _pack(rng, 6, 200)
+    hq, hkv, d = 5, 3, 64
+    qb = _bits(rng, (hq, T, d))
+    kb = _bits(rng, (hkv, T, d))
+    qh, kh = from_bits(qb, dev), from_bits(kb, dev)
+    pr().rope_qk_apply(qh.permute(1, 0, 2), kh.permute(1, 0, 2), 1.0e4,
+                       cu_seqlens=torch.from_numpy(cu).to(dev))
+    torch.cuda.synchronize()
+    pos = oracle.positions(cu, T)
+    q_tok = np.ascontiguousarray(qb.transpose(1, 0, 2))
+    k_tok = np.ascontiguousarray(kb.transpose(1, 0, 2))
+    _check(np.ascontiguousarray(to_bits(qh).transpose(1, 0, 2)), _expect(q_tok, pos, 1.0e4), q_tok, "hm q")
+    _check(np.ascontiguousarray(to_bits(kh).transpose(1, 0, 2)), _expect(k_tok, pos, 1.0e4), k_tok, "hm k")
+
+
+def test_out_of_place_into_fused_buffer(dev):
+    rng = np.random.Generator(np.random.PCG64(6))
+    cu, T = _pack(rng, 5, 150, extra=3)
+    hq, hkv, d = 4, 2, 128
+    qb, kb = _bits(rng, (T, hq, d)), _bits(rng, (T, hkv, d))
+    q, k = from_bits(qb, dev), from_bits(kb, dev)
+    out = torch.full((T, hq + 2 * hkv, d), 9.0, dtype=torch.bfloat16, device=dev)
+    pr().rope_qk_apply(q, k, 5.0e5, cu_seqlens=torch.from_numpy(cu).to(dev),
+                       q_out=out[:, :hq], k_out=out[:, hq:hq + hkv])
+    torch.cuda.synchronize()
+    pos = oracle.positions(cu, T)
+    ob = to_bits(out)
+    _check(ob[:, :hq], _expect(qb, pos, 5.0e5), qb, "ooq")
+    _check(ob[:, hq:hq + hkv], _expect(kb, pos, 5.0e5), kb, "ook")
+    assert torch.all(out[:, hq + hkv:] == 9.0)
+    assert np.array_equal(to_bits(q), qb) and np.array_equal(to_bits(k), kb)
+
+
+def test_position_ids_equal_cu_path(dev):
+    from packed_varlen_rope_gb300 import workloads as wl
+
+    w = wl.WORKLOADS[3]
+    pack = wl.make_pack(w, "padded")
+    T = pack.total_tokens
+    q = wl.normal_bf16((T, w.n_q_heads, w.head_dim), 3, device="cuda")
+    k = wl.normal_bf16((T, w.n_kv_heads, w.head_dim), 4, device="cuda")
+    q2, k2 = q.clone(), k.clone()
+    cu = torch.from_numpy(pack.cu_seqlens).to(dev)
+    pr().rope_qk_fwd(q, k, cu, w.theta)
+    pos = pr().rope_qk_positions(cu, T)
+    pr().rope_qk_apply(q2, k2, w.theta, position_ids=pos)
+    torch.cuda.synchronize()
+    assert torch.equal(q.view(torch.int16), q2.view(torch.int16))
+    assert torch.equal(k.view(torch.int16), k2.view(torch.int16))
+
+
+def test_position_ids_arbitrary(dev):
+    """Explicit ids in any order, including ids outside [0, 2^24) which leave the row out."""
+    rng = np.random.Generator(np.random.PCG64(7))
+    T, hq, hkv, d = 300, 3, 2, 64
+    ids = rng.integers(0, 1 << 24, size=T).astype(np.int64)
+    ids[:10] = [0, 1, (1 << 24) - 1, -1, -7, 1 << 24, (1 << 31) - 1, 5, 100000, 25000]
+    qb, kb = _bits(rng, (T, hq, d)), _bits(rng, (T, hkv, d))
+    for bwd in (False, True):
+        q, k = from_bits(qb, dev), from_bits(kb, dev)
+        pid = torch.from_numpy(ids.astype(np.int32)).to(dev)
+        pr().rope_qk_apply(q, k, 1.0e6, position_ids=pid, backward=bwd)
+        torch.cuda.synchronize()
+        pos = np.where((ids >= 0) & (ids < (1 << 24)), ids, -1).astype(np.int32)
+        _check(to_bits(q), _expect(qb, pos, 1.0e6, bwd), qb, "ids q")
+        _check(to_bits(k), _expect(kb, pos, 1.0e6, bwd), kb, "ids k")
+
+
+@pytest.mark.parametrize("cp", [2, 4])
+def test_context_parallel_shards(dev, cp):
+    """Shards of one pack, each holding its tokens and the pack's cu_seqlens with its
+    token offset, give the unsharded result.  Both the contiguous split and the
+    load-balanced split into 2*cp chunks (rank r holds chunks r and 2*cp-1-r) of the
+    TRL context-parallel section are covered."""
+    from packed_varlen_rope_gb300 import workloads as wl
+
+    w = wl.WORKLOADS[2]
+    pack = wl.make_pack(w)
+    T = pack.total_tokens
+    cu = torch.from_numpy(pack.cu_seqlens).to(dev)
+    q = wl.normal_bf16((T, w.n_q_heads, w.head_dim), 8, device="cuda")
+    k = wl.normal_bf16((T, w.n_kv_heads, w.head_dim), 9, device="cuda")
+    q0, k0 = to_bits(q), to_bits(k)
+    ref_q, ref_k = q.clone(), k.clone()
+    pr().rope_qk_fwd(ref_q, ref_k, cu, w.theta)
+    n_chunks = 2 * cp
+    bounds = np.linspace(0, T, n_chunks + 1).astype(np.int64)
+    layouts = {
+        "contiguous": [[(int(bounds[2 * r]), int(bounds[2 * r + 2]))] for r in range(cp)],
+        "balanced": [[(int(bounds[r]), int(bounds[r + 1])), (int(bounds[n_chunks - 1 - r]), int(bounds[n_chunks - r]))]
+                     for r in range(cp)],
+    }
+    for name, ranks in layouts.items():
+        out_q, out_k = torch.empty_like(q), torch.empty_like(k)
+        for chunks in ranks:
+            for a, b in chunks:
+                sq, sk = q[a:b].clone(), k[a:b].clone()            # the shard's own buffers
+                pr().rope_qk_apply(sq, sk, w.theta, cu_seqlens=cu, token_offset=a)
+                out_q[a:b], out_k[a:b] = sq, sk
+        torch.cuda.synchronize()
+        assert torch.equal(out_q.view(torch.int16), ref_q.view(torch.int16)), name
+        assert torch.equal(out_k.view(torch.int16), ref_k.view(torch.int16)), name
+    pos = oracle.positions(pack.cu_seqlens, T)
+    _check(to_bits(ref_k), _expect(k0, pos, w.theta), k0, "cp ref k")
+
+
+def test_position_scale_page_example(dev):
+    """TRL YaRN section: with factor 4, position 100,000 reads as 25,000 (and 163,840
+    as 40,960) -- bit-identical rows, with and without a cos/sin cache."""
+    rng = np.random.Generator(np.random.PCG64(10))
+    hq, hkv, d = 4, 2, 128
+    xb, kb = _bits(rng, (2, hq, d)), _bits(rng, (2, hkv, d))
+    for use_cache in (False, True):
+        outs = []
+        for ids, scale in (([100000, 163840], 4.0), ([25000, 40960], 1.0)):
+            q, k = from_bits(xb, dev), from_bits(kb, dev)
+            cache = None
+            if use_cache:
+                cache = pr().new_cos_sin_cache(163841, d, 1.0e6, device=dev, position_scale=scale)
+            pr().rope_qk_apply(q, k, 1.0e6, position_ids=torch.tensor(ids, dtype=torch.int32, device=dev),
+                               position_scale=scale, cos_sin_cache=cache)
+            torch.cuda.synchronize()
+            outs.append((to_bits(q), to_bits(k)))
+        assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+
+
+@pytest.mark.parametrize("scale", [4.0, 2.5])
+def test_position_scale_parity(dev, scale):
+    from packed_varlen_rope_gb300 import workloads as wl
+
+    w = wl.WORKLOADS[2]
+    pack = wl.make_pack(w)
+    T = pack.total_tokens
+    q = wl.normal_bf16((T, w.n_q_heads, w.head_dim), 11, device="cuda")
+    k = wl.normal_bf16((T, w.n_kv_heads, w.head_dim), 12, device="cuda")
+    q0, k0 = to_bits(q), to_bits(k)
+    cache = pr().new_cos_sin_cache(max(pack.lengths), w.head_dim, w.theta, device=dev, position_scale=scale)
+    cu = torch.from_numpy(pack.cu_seqlens).to(dev)
+    pr().rope_qk_apply(q, k, w.theta, cu_seqlens=cu, position_scale=scale, cos_sin_cache=cache)
+    torch.cuda.synchronize()
+    pos = oracle.positions(pack.cu_seqlens, T)
+    _check(to_bits(q), _expect(q0, pos, w.theta, scale=scale), q0, "scaled q")
+    _check(to_bits(k), _expect(k0, pos, w.theta, scale=scale), k0, "scaled k")
+    # the scaled cache holds the oracle's scaled cos/sin
+    host = pr()._binding.cache_as_cos_sin(cache[:64].cpu().numpy())
+    for p in range(64):
+        c, s = oracle.cos_sin(p, w.theta, w.head_dim, scale)
+        assert np.array_equal(host[p, :, 0], c) and np.array_equal(host[p, :, 1], s)
+
+
+def test_long_strided_fused_qkv(dev):
+    """A fused QKV buffer of 2^20 tokens x (32 + 2*8) heads x 128 (6.4e9 elements): the
+    Q/K views span more than 2^31 elements, so the 64-bit-offset kernel runs on strided
+    views.  Sampled rows around the 2^31 element offset against the oracle."""
+    T, hq, hkv, d = 1 << 20, 32, 8, 128
+    from packed_varlen_rope_gb300 import workloads as wl
+
+    qkv = wl.normal_bf16((T, hq + 2 * hkv, d), 13, device="cuda")
+    per_token = (hq + 2 * hkv) * d
+    cross = (1 << 31) // per_token
+    rng = np.random.Generator(np.random.PCG64(14))
+    rows = np.unique(np.concatenate([rng.integers(0, T, 512), [0, cross - 1, cross, cross + 1, T - 1]]))
+    rows_dev = torch.from_numpy(rows).to(dev)
+    before = to_bits(qkv[rows_dev])
+    cu = torch.tensor([0, 300000, T], dtype=torch.int32, device=dev)
+    pr().rope_qk_apply(qkv[:, :hq], qkv[:, hq:hq + hkv], 1.0e6, cu_seqlens=cu)
+    torch.cuda.synchronize()
+    after = to_bits(qkv[rows_dev])
+    pos = oracle.positions(np.array([0, 300000, T], dtype=np.int32), T)[rows]
+    for sl in (slice(0, hq), slice(hq, hq + hkv)):
+        _check(after[:, sl], _expect(before[:, sl], pos, 1.0e6), before[:, sl], "long fused")
+    assert np.array_equal(after[:, hq + hkv:], before[:, hq + hkv:])

@@ -17,6 +17,10 @@ What each function follows (restated, not copied):
 * ``rope_rows`` / ``rope_packed`` -- unsloth.ai page, section "Kernel Triton QK
   RoPE fusionné avec packing": ``x*cos + rotate_half(x)*sin``; backward is the same
   with sin negated (``R^T``).
+* ``glu_fwd`` / ``glu_bwd`` (``glu_oracle.c``) -- the SwiGLU / GeGLU kernels of the
+  same page (updated for int64 indexing) and the MLP line
+  ``down_proj(act_fn(gate_proj(x)) * up_proj(x))`` of the TRL page, in binary64,
+  rounded once to bf16.
 """
 from __future__ import annotations
 
@@ -28,22 +32,26 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 SOURCE = os.path.join(_HERE, "rope_oracle.c")
+SOURCES = [SOURCE, os.path.join(_HERE, "glu_oracle.c")]
 LIB_PATH = os.path.join(_HERE, "librope_oracle.so")
 CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-shared", "-fPIC"]
 
 
-def compile_source(src: str, out: str) -> str:
-    """Compile one oracle C source into a shared library (no FMA contraction)."""
+def compile_source(src, out: str) -> str:
+    """Compile oracle C sources (one path or a list) into a shared library, no FMA
+    contraction."""
+    srcs = [src] if isinstance(src, str) else list(src)
     tmp = out + ".tmp%d" % os.getpid()
-    subprocess.check_call(["gcc", *CFLAGS, src, "-o", tmp, "-lm"])
+    subprocess.check_call(["gcc", *CFLAGS, *srcs, "-o", tmp, "-lm"])
     os.replace(tmp, out)
     return out
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle if its library is missing or older than its source."""
-    if force or not os.path.exists(LIB_PATH) or os.path.getmtime(LIB_PATH) < os.path.getmtime(SOURCE):
-        compile_source(SOURCE, LIB_PATH)
+    """Compile the oracle if its library is missing or older than a source."""
+    if force or not os.path.exists(LIB_PATH) or \
+            any(os.path.getmtime(LIB_PATH) < os.path.getmtime(p) for p in SOURCES):
+        compile_source(SOURCES, LIB_PATH)
     return LIB_PATH
 
 
@@ -81,6 +89,15 @@ class Oracle:
                                                 ctypes.c_int32, ctypes.c_double, ctypes.c_double,
                                                 ctypes.c_int32]
         lib.oracle_rope_rows_scaled.restype = None
+        lib.oracle_glu_activation.argtypes = [ctypes.c_int32, ctypes.c_double,
+                                              ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
+        lib.oracle_glu_activation.restype = None
+        lib.oracle_glu_fwd.argtypes = [ctypes.c_int32, u16p, u16p, u16p, ctypes.c_int64]
+        lib.oracle_glu_fwd.restype = None
+        lib.oracle_glu_bwd.argtypes = [ctypes.c_int32, u16p, u16p, u16p, u16p, u16p, ctypes.c_int64]
+        lib.oracle_glu_bwd.restype = None
+        lib.oracle_double_to_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_double_to_bf16.restype = ctypes.c_uint16
         lib.oracle_float_to_bf16.argtypes = [ctypes.c_float]
         lib.oracle_float_to_bf16.restype = ctypes.c_uint16
         self.lib = lib
@@ -142,6 +159,41 @@ class Oracle:
     def float_to_bf16_bits(self, v: float) -> int:
         return int(self.lib.oracle_float_to_bf16(float(v)))
 
+    # ---- gated MLP activations (glu_oracle.c)
+    GLU_KINDS = {"swiglu": 0, "geglu": 1, "geglu_tanh": 2}
+
+    def glu_activation(self, kind: str, x: float):
+        """(act(x), act'(x)) in binary64."""
+        a, da = ctypes.c_double(), ctypes.c_double()
+        self.lib.oracle_glu_activation(self.GLU_KINDS[kind], float(x), ctypes.byref(a), ctypes.byref(da))
+        return a.value, da.value
+
+    def glu_fwd(self, kind: str, e_bits, g_bits):
+        """h = bf16(act(e) * g), elementwise on uint16 bf16 bit arrays of one shape."""
+        e = np.ascontiguousarray(e_bits, dtype=np.uint16)
+        g = np.ascontiguousarray(g_bits, dtype=np.uint16)
+        assert e.shape == g.shape
+        h = np.empty_like(e)
+        self.lib.oracle_glu_fwd(self.GLU_KINDS[kind], _ptr(e, ctypes.c_uint16), _ptr(g, ctypes.c_uint16),
+                                _ptr(h, ctypes.c_uint16), e.size)
+        return h
+
+    def glu_bwd(self, kind: str, dh_bits, e_bits, g_bits):
+        """(de, dg) = (bf16(dh * g * act'(e)), bf16(dh * act(e)))."""
+        dh = np.ascontiguousarray(dh_bits, dtype=np.uint16)
+        e = np.ascontiguousarray(e_bits, dtype=np.uint16)
+        g = np.ascontiguousarray(g_bits, dtype=np.uint16)
+        assert dh.shape == e.shape == g.shape
+        de = np.empty_like(e)
+        dg = np.empty_like(e)
+        self.lib.oracle_glu_bwd(self.GLU_KINDS[kind], _ptr(dh, ctypes.c_uint16), _ptr(e, ctypes.c_uint16),
+                                _ptr(g, ctypes.c_uint16), _ptr(de, ctypes.c_uint16), _ptr(dg, ctypes.c_uint16),
+                                e.size)
+        return de, dg
+
+    def double_to_bf16_bits(self, v: float) -> int:
+        return int(self.lib.oracle_double_to_bf16(float(v)))
+
 
 _default = None
 
@@ -176,3 +228,11 @@ def rope_packed(x_bits, cu_seqlens, theta, bwd=False):
 
 def float_to_bf16_bits(v):
     return get().float_to_bf16_bits(v)
+
+
+def glu_fwd(kind, e_bits, g_bits):
+    return get().glu_fwd(kind, e_bits, g_bits)
+
+
+def glu_bwd(kind, dh_bits, e_bits, g_bits):
+    return get().glu_bwd(kind, dh_bits, e_bits, g_bits)

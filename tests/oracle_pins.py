@@ -19,6 +19,8 @@ What pins what:
 * numpy ``searchsorted`` positions, packed == each sample alone, padded == packed
   -> the position reset of the "Packing non contaminé" section;
 * torch's CPU bf16 conversion -> round to nearest even;
+* mpmath (256 bits) values and derivatives, torch's float64 silu/gelu, and a gradient
+  check of the backward -> the SwiGLU/GeGLU oracle (``pin_glu_*``);
 * the TRL page's worked rescale (factor 4: position 100,000 reads as 25,000, and the
   163,840 wanted positions map onto the 40,960 trained ones) -> the linear position
   scale (``pin_position_scale``).
@@ -309,6 +311,107 @@ def pin_position_scale(o) -> None:
                               o.rope_rows(x, np.array([100000] * 4, np.int32), 1.0e6))
 
 
+# ---------------------------------------------------------------- gated MLP activations
+
+GLU_KINDS = ("swiglu", "geglu", "geglu_tanh")
+
+
+def _mp_act(kind, x):
+    import mpmath
+
+    x = mpmath.mpf(x)
+    if kind == "swiglu":
+        return x / (1 + mpmath.exp(-x))
+    if kind == "geglu":
+        return x * (1 + mpmath.erf(x / mpmath.sqrt(2))) / 2
+    u = mpmath.sqrt(2 / mpmath.pi) * (x + mpmath.mpf("0.044715") * x ** 3)
+    return x * (1 + mpmath.tanh(u)) / 2
+
+
+def nearest_bf16_bits(v) -> int:
+    """Nearest bf16 (ties to even) of an mpmath/float value, by exact comparison of
+    neighbouring bf16 values."""
+    import mpmath
+
+    f = np.float32(float(v))
+    b = int(f.view(np.uint32)) >> 16
+    best, best_err = None, None
+    for c in (b - 1, b, b + 1, b + 2):
+        c &= 0xFFFF
+        cv = bits_to_f64(np.array([c], np.uint16))[0]
+        if not np.isfinite(cv):
+            continue
+        err = abs(mpmath.mpf(cv) - mpmath.mpf(v))
+        if best is None or err < best_err or (err == best_err and c % 2 == 0):
+            best, best_err = c, err
+    return best
+
+
+def pin_glu_activation(o) -> None:
+    """act and act' against mpmath at 256 bits, mpmath numerical derivatives, and torch's
+    float64 silu / gelu / gelu(tanh) as independent library routines."""
+    import mpmath
+    import torch
+
+    mpmath.mp.prec = 256
+    xs = [0.0, 1.0, -1.0, 0.5, -2.75, 3.25, 8.0, -8.0, 20.0, -20.0, 1e-3, -1e-3, 0.044715, -1.2784645]
+    for kind in GLU_KINDS:
+        assert o.glu_activation(kind, 0.0) == (0.0, 0.5)
+        for x in xs:
+            a, da = o.glu_activation(kind, x)
+            ea = _mp_act(kind, x)
+            eda = mpmath.diff(lambda t: _mp_act(kind, t), mpmath.mpf(x))
+            assert abs(a - ea) <= 1e-14 * max(1.0, abs(float(ea))), (kind, x, a, ea)
+            assert abs(da - eda) <= 1e-13 * max(1.0, abs(float(eda))), (kind, x, da, eda)
+        t = torch.tensor(xs, dtype=torch.float64)
+        ref = {"swiglu": torch.nn.functional.silu(t), "geglu": torch.nn.functional.gelu(t),
+               "geglu_tanh": torch.nn.functional.gelu(t, approximate="tanh")}[kind]
+        got = np.array([o.glu_activation(kind, x)[0] for x in xs])
+        assert np.allclose(got, ref.numpy(), rtol=1e-14, atol=1e-300)
+    # SiLU at ln 3: sigmoid is exactly 3/4
+    a, _ = o.glu_activation("swiglu", float(np.log(3.0)))
+    assert abs(a - 0.75 * np.log(3.0)) <= 4 * np.spacing(a)
+
+
+def pin_double_to_bf16(o) -> None:
+    import mpmath
+
+    rng = np.random.Generator(np.random.PCG64(21))
+    vals = list(rng.standard_normal(3000) * np.exp2(rng.integers(-140, 120, 3000)))
+    vals += [1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8), 1.0 + 2.0 ** -8 + 2.0 ** -40,
+             2.0 ** -134, 3 * 2.0 ** -135, 2.0 ** -126 * (1 - 2.0 ** -9), 0.0, -0.0,
+             float(np.float32(1.0 + 2.0 ** -8)) + 2.0 ** -30]
+    for v in vals:
+        got = o.double_to_bf16_bits(v)
+        if v == 0.0:
+            assert got == (0x8000 if np.signbit(v) else 0)
+            continue
+        assert got == nearest_bf16_bits(mpmath.mpf(v)), (v, hex(got))
+
+
+def pin_glu_gradient(o) -> None:
+    """The backward is the gradient of L = sum(dh * act(e) * g): de and dg against
+    mpmath derivatives of L, rounded once to bf16."""
+    import mpmath
+
+    mpmath.mp.prec = 128
+    rng = np.random.Generator(np.random.PCG64(22))
+    n = 48
+    e, g, dh = (random_bf16_bits(rng, (n,), 2.0) for _ in range(3))
+    ef, gf, dhf = bits_to_f64(e), bits_to_f64(g), bits_to_f64(dh)
+    for kind in GLU_KINDS:
+        de, dg = o.glu_bwd(kind, dh, e, g)
+        h = o.glu_fwd(kind, e, g)
+        for i in range(n):
+            L = lambda ee, gg: mpmath.mpf(dhf[i]) * _mp_act(kind, ee) * gg  # noqa: E731
+            want_de = mpmath.diff(lambda t: L(t, mpmath.mpf(gf[i])), mpmath.mpf(ef[i]))
+            want_dg = mpmath.diff(lambda t: L(mpmath.mpf(ef[i]), t), mpmath.mpf(gf[i]))
+            assert int(de[i]) == nearest_bf16_bits(want_de), (kind, i)
+            assert int(dg[i]) == nearest_bf16_bits(want_dg), (kind, i)
+            assert int(h[i]) == nearest_bf16_bits(_mp_act(kind, ef[i]) * mpmath.mpf(gf[i])), (kind, i)
+
+
 ALL_PINS = [pin_positions, pin_inv_freq, pin_cos_sin_mpmath, pin_identity_pos0, pin_matrix,
             pin_pair_norm, pin_roundtrip, pin_packed_equals_alone, pin_padded_equals_packed,
-            pin_relative_position, pin_bf16_rounding, pin_position_scale]
+            pin_relative_position, pin_bf16_rounding, pin_position_scale,
+            pin_glu_activation, pin_double_to_bf16, pin_glu_gradient]

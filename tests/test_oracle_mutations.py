@@ -11,6 +11,8 @@ import pytest
 import oracle
 import oracle_pins
 
+GLU = "glu_oracle.c"
+
 MUTATIONS = {
     "lo-sign": ("float lo = ac - bs;", "float lo = ac + bs;"),
     "hi-sign": ("float hi = bc + as;", "float hi = bc - as;"),
@@ -31,18 +33,34 @@ MUTATIONS = {
     "theta-ignored": ("w_out[j] = (float)(pow(theta, e) / scale);", "w_out[j] = (float)(pow(10000.0, e) / scale);"),
     "scale-multiplies": ("w_out[j] = (float)(pow(theta, e) / scale);", "w_out[j] = (float)(pow(theta, e) * scale);"),
     "scale-ignored": ("w_out[j] = (float)(pow(theta, e) / scale);", "w_out[j] = (float)pow(theta, e);"),
+    # SwiGLU / GeGLU oracle
+    "glu-sigmoid-sign": ("return 1.0 / (1.0 + exp(-x));", "return 1.0 / (1.0 + exp(x));", GLU),
+    "glu-silu-derivative": ("*dact = s * (1.0 + x * (1.0 - s));", "*dact = s * (1.0 + x * (1.0 + s));", GLU),
+    "glu-erf-argument": ("0.5 * (1.0 + erf(x * kInvSqrt2));", "0.5 * (1.0 + erf(x * kSqrt2OverPi));", GLU),
+    "glu-gelu-derivative-term": ("*dact = Phi + x * phi;", "*dact = Phi;", GLU),
+    "glu-tanh-cubic": ("(x + kGeluTanhC * x * x * x)", "(x + kGeluTanhC * x * x)", GLU),
+    "glu-dg-uses-derivative": ("dg[i] = double_to_bf16(dhi * a);", "dg[i] = double_to_bf16(dhi * da);", GLU),
+    "glu-de-drops-g": ("de[i] = double_to_bf16(dhi * gi * da);", "de[i] = double_to_bf16(dhi * da);", GLU),
+    "glu-round-truncates": ("double r = ldexp(nearbyint(ldexp(v, -q)), q);", "double r = ldexp(trunc(ldexp(v, -q)), q);", GLU),
+    "glu-fwd-uses-derivative": ("h[i] = double_to_bf16(a * bf16_to_double(g[i]));", "h[i] = double_to_bf16(da * bf16_to_double(g[i]));", GLU),
 }
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_mutant_is_caught(tmp_path, name):
     pytest.importorskip("mpmath")
-    old, new = MUTATIONS[name]
-    src = open(oracle.SOURCE).read()
-    assert src.count(old) == 1, "mutation anchor not found: " + old
-    mutant_src = tmp_path / "rope_oracle_mutant.c"
-    mutant_src.write_text(src.replace(old, new))
-    lib = oracle.compile_source(str(mutant_src), str(tmp_path / ("librope_oracle_%s.so" % name.replace("-", "_"))))
+    old, new, *where = MUTATIONS[name]
+    target = where[0] if where else "rope_oracle.c"
+    sources = []
+    for path in oracle.SOURCES:
+        text = open(path).read()
+        if os.path.basename(path) == target:
+            assert text.count(old) == 1, "mutation anchor not found: " + old
+            text = text.replace(old, new)
+        out = tmp_path / os.path.basename(path)
+        out.write_text(text)
+        sources.append(str(out))
+    lib = oracle.compile_source(sources, str(tmp_path / ("liboracle_%s.so" % name.replace("-", "_"))))
     mutant = oracle.Oracle(lib)
     caught = []
     for pin in oracle_pins.ALL_PINS:

@@ -23,7 +23,8 @@
  *         gelu_t'(x) = (1 + t)/2 + x/2 (1 - t^2) sqrt(2/pi) (1 + 3 * 0.044715 x^2),
  *                      t = tanh(sqrt(2/pi) (x + 0.044715 x^3)).
  *   G5  every result is evaluated in binary64 from the exact bf16 inputs and rounded
- *       once to bf16 (round to nearest even).
+ *       once to bf16 (round to nearest even), with each formula written so that no
+ *       subtraction cancels in the tails (see activation()).
  */
 #include <math.h>
 #include <stdint.h>
@@ -65,23 +66,26 @@ static const double kGeluTanhC = 0.044715;
 
 static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
 
-/* act(x) and act'(x) for kind 0 = SwiGLU, 1 = GeGLU (erf), 2 = GeGLU (tanh). */
+/* act(x) and act'(x) for kind 0 = SwiGLU, 1 = GeGLU (erf), 2 = GeGLU (tanh), written in
+ * forms without cancellation in the tails (identical in exact arithmetic):
+ *   1 - sigmoid(x) = sigmoid(-x);  Phi(x) = erfc(-x/sqrt 2) / 2;
+ *   (1 + tanh u)/2 = sigmoid(2u);  (1 - tanh^2 u)/2 = 2 sigmoid(2u) sigmoid(-2u). */
 static void activation(int32_t kind, double x, double *act, double *dact)
 {
     if (kind == 0) {
         double s = sigmoid(x);
         *act = x * s;
-        *dact = s * (1.0 + x * (1.0 - s));
+        *dact = s * (1.0 + x * sigmoid(-x));
     } else if (kind == 1) {
-        double Phi = 0.5 * (1.0 + erf(x * kInvSqrt2));
+        double Phi = 0.5 * erfc(-x * kInvSqrt2);
         double phi = exp(-0.5 * x * x) * kInvSqrt2Pi;
         *act = x * Phi;
         *dact = Phi + x * phi;
     } else {
         double u = kSqrt2OverPi * (x + kGeluTanhC * x * x * x);
-        double t = tanh(u);
-        *act = 0.5 * x * (1.0 + t);
-        *dact = 0.5 * (1.0 + t) + 0.5 * x * (1.0 - t * t) * kSqrt2OverPi * (1.0 + 3.0 * kGeluTanhC * x * x);
+        double sp = sigmoid(2.0 * u), sm = sigmoid(-2.0 * u);
+        *act = x * sp;
+        *dact = sp + 2.0 * x * sp * sm * kSqrt2OverPi * (1.0 + 3.0 * kGeluTanhC * x * x);
     }
 }
 

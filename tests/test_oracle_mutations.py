@@ -35,8 +35,10 @@ MUTATIONS = {
     "scale-ignored": ("w_out[j] = (float)(pow(theta, e) / scale);", "w_out[j] = (float)pow(theta, e);"),
     # SwiGLU / GeGLU oracle
     "glu-sigmoid-sign": ("return 1.0 / (1.0 + exp(-x));", "return 1.0 / (1.0 + exp(x));", GLU),
-    "glu-silu-derivative": ("*dact = s * (1.0 + x * (1.0 - s));", "*dact = s * (1.0 + x * (1.0 + s));", GLU),
-    "glu-erf-argument": ("0.5 * (1.0 + erf(x * kInvSqrt2));", "0.5 * (1.0 + erf(x * kSqrt2OverPi));", GLU),
+    "glu-silu-derivative": ("*dact = s * (1.0 + x * sigmoid(-x));", "*dact = s * (1.0 + x * sigmoid(x));", GLU),
+    "glu-erf-argument": ("0.5 * erfc(-x * kInvSqrt2);", "0.5 * erfc(-x * kSqrt2OverPi);", GLU),
+    "glu-erfc-sign": ("0.5 * erfc(-x * kInvSqrt2);", "0.5 * erfc(x * kInvSqrt2);", GLU),
+    "glu-tanh-form-factor": ("double sp = sigmoid(2.0 * u), sm = sigmoid(-2.0 * u);", "double sp = sigmoid(u), sm = sigmoid(-u);", GLU),
     "glu-gelu-derivative-term": ("*dact = Phi + x * phi;", "*dact = Phi;", GLU),
     "glu-tanh-cubic": ("(x + kGeluTanhC * x * x * x)", "(x + kGeluTanhC * x * x)", GLU),
     "glu-dg-uses-derivative": ("dg[i] = double_to_bf16(dhi * a);", "dg[i] = double_to_bf16(dhi * da);", GLU),

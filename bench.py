@@ -54,6 +54,9 @@ def parse_args():
                     help="target seconds of oracle work for the CPU baseline sample")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=["rope", "glu"], default="rope",
+                    help="rope: the QK-RoPE step (default); glu: SwiGLU/GeGLU forward+backward")
+    ap.add_argument("--glu-workload", default="qwen3-4b-mlp-1m")
     return ap.parse_args()
 
 
@@ -430,6 +433,87 @@ def end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev):
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": E}
 
 
+def run_glu(args, rank, world, local):
+    """SwiGLU / GeGLU forward + backward on one matrix shape (second workload of the
+    source page: the MLP activation kernels with int64 indexing).  One step = glu_fwd
+    (h = act(e) * g) then glu_bwd (de, dg into their own buffers)."""
+    import torch
+
+    from packed_varlen_rope_gb300 import build as _build
+
+    _build.build()
+    import packed_varlen_rope_gb300 as pr
+    from packed_varlen_rope_gb300 import workloads as wl
+
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = wl.GLU_WORKLOADS[args.glu_workload]
+    shape = (w.rows, w.cols)
+    e = wl.normal_bf16(shape, 7001 + rank * wl.RANK_SEED_STRIDE, device=dev)
+    g = wl.normal_bf16(shape, 7002 + rank * wl.RANK_SEED_STRIDE, device=dev)
+    dh = wl.normal_bf16(shape, 7003 + rank * wl.RANK_SEED_STRIDE, device=dev)
+    h, de, dg = (torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(3))
+    stream = torch.cuda.current_stream(dev)
+    n = w.rows * w.cols
+    fwd_bytes, bwd_bytes = 6 * n, 10 * n
+    for _ in range(max(3, args.warmup)):
+        pr.glu_fwd(w.kind, e, g, h)
+        pr.glu_bwd(w.kind, dh, e, g, de, dg)
+    sampler = ClockSampler(physical_gpu_index(local))
+    sampler.start()
+    K = args.steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4 * K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        ev[4 * i].record(stream)
+        pr.glu_fwd(w.kind, e, g, h)
+        ev[4 * i + 1].record(stream)
+        ev[4 * i + 2].record(stream)
+        pr.glu_bwd(w.kind, dh, e, g, de, dg)
+        ev[4 * i + 3].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t1 = time.time()
+    sampler.stop()
+    ms = max_over_ranks(start.elapsed_time(end), world, dev) / K
+    fwd_s = statistics.mean(ev[4 * i].elapsed_time(ev[4 * i + 1]) for i in range(K)) / 1e3
+    bwd_s = statistics.mean(ev[4 * i + 2].elapsed_time(ev[4 * i + 3]) for i in range(K)) / 1e3
+    peak, peak_kind = measured_peak()
+    if rank == 0:
+        line = {
+            "metric": "SwiGLU/GeGLU fwd+bwd tokens/s and HBM GB/s", "value": whole_job_tokens_per_s(world, w.rows, ms),
+            "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "rows": w.rows, "cols": w.cols, "kind": w.kind,
+                       "l2": "no flush: %.1f GB per step > 129 MB L2" % ((fwd_bytes + bwd_bytes) / 1e9)},
+            "hbm_gbs": (fwd_bytes + bwd_bytes) / (ms / 1e3) / 1e9,
+            "roofline": {"bound": "hbm", "unit": "GB/s", "peak": peak, "peak_kind": peak_kind + " (hbm_gbs)",
+                         "kernels": {
+                             "glu_fwd": {"achieved": fwd_bytes / fwd_s / 1e9, "frac": fwd_bytes / fwd_s / 1e9 / peak,
+                                         "algorithmic_bytes_per_launch": fwd_bytes, "avg_launch_us": fwd_s * 1e6},
+                             "glu_bwd": {"achieved": bwd_bytes / bwd_s / 1e9, "frac": bwd_bytes / bwd_s / 1e9 / peak,
+                                         "algorithmic_bytes_per_launch": bwd_bytes, "avg_launch_us": bwd_s * 1e6}}},
+            "clocks": sampler.summary(t0, t1),
+            "gpu_launches": 2 * K,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_env()
@@ -438,6 +522,8 @@ def main():
         return 2
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.path == "glu":
+        return run_glu(args, rank, world, local)
     return run_ours(args, rank, world, local)
 
 

@@ -64,7 +64,8 @@ typedef enum rope_status {
     ROPE_ERR_UNSUPPORTED = -6,  /* a global token index or cache row beyond 2^24 (positions
                                    are exact in binary32 only up to there) */
     ROPE_ERR_LAUNCH = -7,       /* the CUDA runtime refused a launch or copy */
-    ROPE_ERR_THETA = -8         /* theta or position_scale not finite and > 0 */
+    ROPE_ERR_THETA = -8,        /* theta or position_scale not finite and > 0 */
+    ROPE_ERR_KIND = -9          /* unknown activation kind (glu.h) */
 } rope_status;
 
 /* Bits of the word rope_validate_cu_seqlens writes. */

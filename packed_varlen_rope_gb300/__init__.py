@@ -12,6 +12,7 @@ from __future__ import annotations
 
 from ._binding import (  # noqa: F401
     EXPORTS,
+    GLU_KINDS,
     LIB_PATH,
     ROPE_CU_DECREASING,
     ROPE_CU_NEGATIVE_START,
@@ -19,6 +20,8 @@ from ._binding import (  # noqa: F401
     ROPE_CU_PAST_END,
     RopeError,
     RopeQKDesc,
+    glu_bwd,
+    glu_fwd,
     load_library,
     new_cos_sin_cache,
     rope_cos_sin_cache_build,

@@ -18,7 +18,10 @@ EXPORTS = (
     "rope_qk_fwd", "rope_qk_bwd", "rope_qk_apply", "rope_cos_sin_cache_build",
     "rope_cos_sin_cache_build_scaled", "rope_cos_sin_cache_bytes", "rope_qk_positions",
     "rope_validate_cu_seqlens", "rope_qk_inv_freq", "rope_strerror", "rope_qk_abi_version",
+    "glu_fwd", "glu_bwd",
 )
+
+GLU_KINDS = {"swiglu": 0, "geglu": 1, "geglu_tanh": 2}
 
 ROPE_CU_NEGATIVE_START = 0x1
 ROPE_CU_DECREASING = 0x2
@@ -82,6 +85,10 @@ def load_library(path: Optional[str] = None):
     lib.rope_qk_inv_freq.restype = ctypes.c_int
     lib.rope_strerror.argtypes = [ctypes.c_int]
     lib.rope_strerror.restype = ctypes.c_char_p
+    lib.glu_fwd.argtypes = [i32, vp, i64, vp, i64, vp, i64, i64, i64, vp]
+    lib.glu_fwd.restype = ctypes.c_int
+    lib.glu_bwd.argtypes = [i32, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i64, i64, vp]
+    lib.glu_bwd.restype = ctypes.c_int
     lib.rope_qk_abi_version.argtypes = []
     lib.rope_qk_abi_version.restype = ctypes.c_int
     if path is None:
@@ -308,3 +315,49 @@ def rope_qk_apply(q, k, theta: float, cu_seqlens=None, position_ids=None, backwa
 
 def rope_qk_abi_version() -> int:
     return int(load_library().rope_qk_abi_version())
+
+
+def _mat_args(t, name, shape):
+    import torch
+
+    if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 2 or (t.numel() and t.stride(1) != 1):
+        raise ValueError("%s must be a CUDA bf16 [rows, cols] view with contiguous rows" % name)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s" % (name, tuple(shape)))
+    return _ptr(t), t.stride(0)
+
+
+def glu_fwd(kind: str, e, g, h=None, stream=None):
+    """h = act(e) * g for SwiGLU ("swiglu") or GeGLU ("geglu", "geglu_tanh").  e, g, h:
+    bf16 [rows, cols] CUDA views (cols a multiple of 8); h may be e or g (in place).
+    Returns h (a new tensor when not given)."""
+    import torch
+
+    shape = tuple(e.shape)
+    if h is None:
+        h = torch.empty(shape, dtype=torch.bfloat16, device=e.device)
+    ep, es = _mat_args(e, "e", shape)
+    gp, gs = _mat_args(g, "g", shape)
+    hp, hs = _mat_args(h, "h", shape)
+    st = load_library().glu_fwd(GLU_KINDS[kind], ep, es, gp, gs, hp, hs, shape[0], shape[1],
+                                _stream(stream, e.device))
+    _check("glu_fwd", st)
+    return h
+
+
+def glu_bwd(kind: str, dh, e, g, de=None, dg=None, stream=None):
+    """de = dh * g * act'(e), dg = dh * act(e).  de/dg may be e/g (or dh) for an
+    in-place backward.  Returns (de, dg)."""
+    import torch
+
+    shape = tuple(e.shape)
+    if de is None:
+        de = torch.empty(shape, dtype=torch.bfloat16, device=e.device)
+    if dg is None:
+        dg = torch.empty(shape, dtype=torch.bfloat16, device=e.device)
+    args = []
+    for name, t in (("dh", dh), ("e", e), ("g", g), ("de", de), ("dg", dg)):
+        args += list(_mat_args(t, name, shape))
+    st = load_library().glu_bwd(GLU_KINDS[kind], *args, shape[0], shape[1], _stream(stream, e.device))
+    _check("glu_bwd", st)
+    return de, dg

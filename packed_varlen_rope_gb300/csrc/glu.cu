@@ -1,0 +1,291 @@
+// Gated MLP activations, SwiGLU and GeGLU, forward and backward, for GB300 (sm_103a).
+//
+// Elementwise and HBM-bound (forward 6 bytes per element, backward 10): each thread owns
+// units of 8 consecutive elements of a row (16-byte loads and stores) and keeps 4 units
+// in flight.  64-bit offsets are a compile-time specialisation used only when an
+// element offset of a matrix reaches 2^31 (unsloth.ai "3x faster training with
+// packing", section "Indexage int64 pour les kernels Triton"); the intermediate matrix
+// of 1,048,576 tokens x 9,728 (TRL "training beyond 1M tokens") needs it.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <type_traits>
+
+#include "fastdiv.cuh"
+#include "glu.h"
+
+namespace {
+
+using pvr::FastDiv;
+using pvr::fast_div;
+using pvr::make_fastdiv;
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;
+constexpr float kSqrt2OverPi = 0.797884560802865355879892f;  // sqrt(2/pi)
+constexpr float kInvSqrt2Pi = 0.398942280401432677939946f;   // 1/sqrt(2 pi)
+constexpr float kInvSqrt2 = 0.707106781186547524400844f;     // 1/sqrt(2)
+constexpr float kGeluTanhC = 0.044715f;
+
+struct GluArgs {
+    const __nv_bfloat16 *dh;
+    const __nv_bfloat16 *e;
+    const __nv_bfloat16 *g;
+    __nv_bfloat16 *out0;      // h (forward) or de (backward)
+    __nv_bfloat16 *out1;      // dg (backward)
+    int64_t s_dh, s_e, s_g, s_out0, s_out1;
+    uint32_t units;           // rows * cols / 8
+    uint32_t cols8;
+    FastDiv div_cols8;
+};
+
+// sigmoid(y) and sigmoid(-y) from one exponential: with t = exp(-y),
+// sigmoid(y) = 1 / (1 + t) and sigmoid(-y) = t / (1 + t) (= 1 once t overflows).
+__device__ __forceinline__ void sigmoid_pair(float y, float &sp, float &sm)
+{
+    const float t = expf(-y);
+    sp = __frcp_rn(1.0f + t);
+    sm = isinf(t) ? 1.0f : t * sp;
+}
+
+// act(x) and act'(x), in forms without cancellation in the tails.
+template <int KIND>
+__device__ __forceinline__ void activation(float x, float &a, float &da)
+{
+    if (KIND == GLU_SWIGLU) {
+        float sp, sm;
+        sigmoid_pair(x, sp, sm);
+        a = x * sp;
+        da = sp * (1.0f + x * sm);
+    } else if (KIND == GLU_GEGLU) {
+        const float Phi = 0.5f * erfcf(-x * kInvSqrt2);
+        const float phi = expf(-0.5f * x * x) * kInvSqrt2Pi;
+        a = x * Phi;
+        da = Phi + x * phi;
+    } else {
+        const float u = kSqrt2OverPi * (x + kGeluTanhC * x * x * x);
+        float sp, sm;
+        sigmoid_pair(2.0f * u, sp, sm);
+        a = x * sp;
+        // the second term vanishes with sp * sm; test it first so that a huge |x|
+        // (where 1 + 3c x^2 overflows) gives 0, not 0 * inf
+        const float w = sp * sm;
+        da = w == 0.0f ? sp : sp + 2.0f * x * w * kSqrt2OverPi * (1.0f + 3.0f * kGeluTanhC * x * x);
+    }
+}
+
+__device__ __forceinline__ uint4 load_stream(const __nv_bfloat16 *p)
+{
+    return __ldcs(reinterpret_cast<const uint4 *>(p));
+}
+
+__device__ __forceinline__ void store_stream(__nv_bfloat16 *p, uint4 v)
+{
+    __stcs(reinterpret_cast<uint4 *>(p), v);
+}
+
+__device__ __forceinline__ float2 unpack(uint32_t w)
+{
+    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&w);
+    return __bfloat1622float2(v);
+}
+
+__device__ __forceinline__ uint32_t pack(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+template <int KIND, bool LONG, bool BWD>
+__global__ void __launch_bounds__(kThreads)
+glu_kernel(const __grid_constant__ GluArgs a)
+{
+    using Index = typename std::conditional<LONG, int64_t, uint32_t>::type;
+    const uint32_t base = blockIdx.x * static_cast<uint32_t>(kUnroll * kThreads) + threadIdx.x;
+    uint4 ve[kUnroll], vg[kUnroll], vd[kUnroll];
+    Index row[kUnroll], col[kUnroll];
+    bool live[kUnroll];
+#pragma unroll
+    for (int k = 0; k < kUnroll; ++k) {
+        const uint32_t u = base + k * kThreads;
+        live[k] = u < a.units;
+        row[k] = 0;
+        col[k] = 0;
+        if (live[k]) {
+            const uint32_t r = fast_div(u, a.div_cols8);
+            row[k] = static_cast<Index>(r);
+            col[k] = static_cast<Index>((u - r * a.cols8) * 8u);
+            ve[k] = load_stream(a.e + (row[k] * static_cast<Index>(a.s_e) + col[k]));
+            vg[k] = load_stream(a.g + (row[k] * static_cast<Index>(a.s_g) + col[k]));
+            if (BWD) vd[k] = load_stream(a.dh + (row[k] * static_cast<Index>(a.s_dh) + col[k]));
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kUnroll; ++k) {
+        if (!live[k]) continue;
+        const uint32_t *we = &ve[k].x, *wg = &vg[k].x, *wd = &vd[k].x;
+        uint4 o0, o1;
+        uint32_t *p0 = &o0.x, *p1 = &o1.x;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float2 x = unpack(we[w]);
+            const float2 gg = unpack(wg[w]);
+            float a0, d0, a1, d1;
+            activation<KIND>(x.x, a0, d0);
+            activation<KIND>(x.y, a1, d1);
+            if (!BWD) {
+                p0[w] = pack(a0 * gg.x, a1 * gg.y);
+            } else {
+                const float2 dh = unpack(wd[w]);
+                p0[w] = pack(dh.x * gg.x * d0, dh.y * gg.y * d1);   // de
+                p1[w] = pack(dh.x * a0, dh.y * a1);                 // dg
+            }
+        }
+        store_stream(a.out0 + (row[k] * static_cast<Index>(a.s_out0) + col[k]), o0);
+        if (BWD) store_stream(a.out1 + (row[k] * static_cast<Index>(a.s_out1) + col[k]), o1);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+struct Mat {
+    const void *p;
+    int64_t stride;
+};
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t span_bytes(const Mat &m, int64_t rows, int64_t cols) { return ((rows - 1) * m.stride + cols) * 2; }
+
+bool ranges_overlap(const Mat &a, const Mat &b, int64_t rows, int64_t cols)
+{
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a.p), pb = reinterpret_cast<uintptr_t>(b.p);
+    return pa < pb + static_cast<uintptr_t>(span_bytes(b, rows, cols)) &&
+           pb < pa + static_cast<uintptr_t>(span_bytes(a, rows, cols));
+}
+
+// An output is fine if it is exactly an input, else it must not touch any input.
+int check_output(const Mat &o, const Mat *in, int n_in, int64_t rows, int64_t cols)
+{
+    for (int i = 0; i < n_in; ++i) {
+        if (o.p == in[i].p && o.stride == in[i].stride) continue;
+        if (ranges_overlap(o, in[i], rows, cols)) return ROPE_ERR_OVERLAP;
+    }
+    return ROPE_OK;
+}
+
+int check_mats(const Mat *m, int n, int64_t rows, int64_t cols)
+{
+    for (int i = 0; i < n; ++i) {
+        if (m[i].p == nullptr) return ROPE_ERR_NULL;
+        if (!aligned16(m[i].p) || m[i].stride % 8 != 0) return ROPE_ERR_ALIGN;
+        if (rows > 1 && m[i].stride < cols) return ROPE_ERR_SHAPE;
+    }
+    return ROPE_OK;
+}
+
+template <int KIND, bool LONG, bool BWD>
+cudaError_t launch(const GluArgs &a, cudaStream_t s)
+{
+    const uint32_t per_block = kUnroll * kThreads;
+    const uint32_t grid = (a.units + per_block - 1) / per_block;
+    glu_kernel<KIND, LONG, BWD><<<grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <bool BWD>
+int run(int32_t kind, const GluArgs &a, bool long_index, cudaStream_t s)
+{
+    cudaError_t err;
+    switch (kind) {
+    case GLU_SWIGLU:
+        err = long_index ? launch<GLU_SWIGLU, true, BWD>(a, s) : launch<GLU_SWIGLU, false, BWD>(a, s);
+        break;
+    case GLU_GEGLU:
+        err = long_index ? launch<GLU_GEGLU, true, BWD>(a, s) : launch<GLU_GEGLU, false, BWD>(a, s);
+        break;
+    default:
+        err = long_index ? launch<GLU_GEGLU_TANH, true, BWD>(a, s) : launch<GLU_GEGLU_TANH, false, BWD>(a, s);
+        break;
+    }
+    return err == cudaSuccess ? ROPE_OK : ROPE_ERR_LAUNCH;
+}
+
+int prepare(int32_t kind, int64_t rows, int64_t cols, GluArgs &a)
+{
+    if (kind < GLU_SWIGLU || kind > GLU_GEGLU_TANH) return ROPE_ERR_KIND;
+    if (rows < 0 || cols < 0 || cols % 8 != 0) return ROPE_ERR_SHAPE;
+    const int64_t units = rows * (cols / 8);
+    if (units >= (int64_t(1) << 31)) return ROPE_ERR_SHAPE;
+    a.units = static_cast<uint32_t>(units);
+    a.cols8 = static_cast<uint32_t>(cols / 8);
+    a.div_cols8 = make_fastdiv(a.cols8 > 0 ? a.cols8 : 1);
+    return ROPE_OK;
+}
+
+bool needs_long(const Mat *m, int n, int64_t rows, int64_t cols)
+{
+    for (int i = 0; i < n; ++i)
+        if ((rows - 1) * m[i].stride + cols > INT32_MAX) return true;
+    return false;
+}
+
+}  // namespace
+
+extern "C" {
+
+int glu_fwd(int32_t kind, const void *e, int64_t e_stride, const void *g, int64_t g_stride,
+            void *h, int64_t h_stride, int64_t rows, int64_t cols, void *stream)
+{
+    GluArgs a{};
+    int rc = prepare(kind, rows, cols, a);
+    if (rc != ROPE_OK) return rc;
+    if (a.units == 0) return ROPE_OK;
+    const Mat in[2] = {{e, e_stride}, {g, g_stride}};
+    const Mat out{h, h_stride};
+    if ((rc = check_mats(in, 2, rows, cols)) != ROPE_OK) return rc;
+    if ((rc = check_mats(&out, 1, rows, cols)) != ROPE_OK) return rc;
+    if ((rc = check_output(out, in, 2, rows, cols)) != ROPE_OK) return rc;
+    a.e = static_cast<const __nv_bfloat16 *>(e);
+    a.g = static_cast<const __nv_bfloat16 *>(g);
+    a.out0 = static_cast<__nv_bfloat16 *>(h);
+    a.s_e = e_stride;
+    a.s_g = g_stride;
+    a.s_out0 = h_stride;
+    const Mat all[3] = {in[0], in[1], out};
+    return run<false>(kind, a, needs_long(all, 3, rows, cols), static_cast<cudaStream_t>(stream));
+}
+
+int glu_bwd(int32_t kind, const void *dh, int64_t dh_stride, const void *e, int64_t e_stride,
+            const void *g, int64_t g_stride, void *de, int64_t de_stride, void *dg,
+            int64_t dg_stride, int64_t rows, int64_t cols, void *stream)
+{
+    GluArgs a{};
+    int rc = prepare(kind, rows, cols, a);
+    if (rc != ROPE_OK) return rc;
+    if (a.units == 0) return ROPE_OK;
+    const Mat in[3] = {{dh, dh_stride}, {e, e_stride}, {g, g_stride}};
+    const Mat out[2] = {{de, de_stride}, {dg, dg_stride}};
+    if ((rc = check_mats(in, 3, rows, cols)) != ROPE_OK) return rc;
+    if ((rc = check_mats(out, 2, rows, cols)) != ROPE_OK) return rc;
+    if (ranges_overlap(out[0], out[1], rows, cols)) return ROPE_ERR_OVERLAP;
+    for (const Mat &o : out)
+        if ((rc = check_output(o, in, 3, rows, cols)) != ROPE_OK) return rc;
+    a.dh = static_cast<const __nv_bfloat16 *>(dh);
+    a.e = static_cast<const __nv_bfloat16 *>(e);
+    a.g = static_cast<const __nv_bfloat16 *>(g);
+    a.out0 = static_cast<__nv_bfloat16 *>(de);
+    a.out1 = static_cast<__nv_bfloat16 *>(dg);
+    a.s_dh = dh_stride;
+    a.s_e = e_stride;
+    a.s_g = g_stride;
+    a.s_out0 = de_stride;
+    a.s_out1 = dg_stride;
+    const Mat all[5] = {in[0], in[1], in[2], out[0], out[1]};
+    return run<true>(kind, a, needs_long(all, 5, rows, cols), static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

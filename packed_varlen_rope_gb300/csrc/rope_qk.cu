@@ -2,7 +2,6 @@
 //
 // One CTA owns a tile of consecutive tokens and rotates every Q head and every K head
 // of those tokens (grouped-query attention: any n_q_heads / n_kv_heads).  Per tile:
-//   0. every thread issues its first 16-byte loads at once, before anything else;
 //   1. the first warp finds each token's sample by binary search over cu_seqlens, so
 //      positions restart at every packed-sample boundary (unsloth.ai "3x faster
 //      training with packing", section "Packing non contaminé");
@@ -30,6 +29,7 @@
 #include <type_traits>
 #include <utility>
 
+#include "fastdiv.cuh"
 #include "rope_qk.h"
 
 namespace {
@@ -40,24 +40,9 @@ constexpr int kMaxHalf = 128;           // head_dim <= 256
 constexpr int kMaxTileTokens = 32;      // one warp resolves the tile's positions
 constexpr int64_t kMaxTokens = int64_t(1) << 24;   // positions < 2^24 are exact in fp32
 
-// Division by a runtime constant for 0 <= n < 2^31 (Granlund & Montgomery, "Division
-// by invariant integers using multiplication", PLDI 1994): q = (mulhi(n, m) + n) >> l.
-struct FastDiv {
-    uint32_t d, m, l;
-};
-
-FastDiv make_fastdiv(uint32_t d)
-{
-    uint32_t l = 0;
-    while ((uint64_t(1) << l) < d) ++l;
-    uint64_t m = ((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1;
-    return FastDiv{d, uint32_t(m), l};
-}
-
-__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv &f)
-{
-    return (__umulhi(n, f.m) + n) >> f.l;
-}
+using pvr::FastDiv;
+using pvr::fast_div;
+using pvr::make_fastdiv;
 
 struct RopeArgs {
     const __nv_bfloat16 *q_in;
@@ -193,32 +178,6 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
         }
     };
 
-    uint4 lo[kUnroll], hi[kUnroll];
-    __nv_bfloat16 *dst[kUnroll];
-    int tok[kUnroll], chunk[kUnroll];
-    bool live[kUnroll];
-
-    // 0. the first batch of loads goes out before the positions are known, so HBM is
-    //    busy while the tile's positions and cos/sin rows are being resolved
-    uint32_t base = threadIdx.x;
-#pragma unroll
-    for (int k = 0; k < kUnroll; ++k) {
-        const uint32_t u = base + k * kThreads;
-        live[k] = u < units;
-        tok[k] = 0;
-        chunk[k] = 0;
-        dst[k] = nullptr;
-        if (live[k]) {
-            uint32_t i, c;
-            const __nv_bfloat16 *src;
-            locate(u, i, c, src, dst[k]);
-            lo[k] = load_stream(src);
-            hi[k] = load_stream(src + h);
-            tok[k] = static_cast<int>(i);
-            chunk[k] = static_cast<int>(c);
-        }
-    }
-
     // 1. positions of the tile's tokens (one lane per token): from the caller's
     //    position ids, else by binary search of cu_seqlens in the global token stream
     if (threadIdx.x < kMaxTileTokens) {
@@ -262,44 +221,49 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
     }
     __syncthreads();
 
-    // 3. rotate and store the batch in registers, load the next one, until the tile is
-    //    done.  Rows of tokens outside the pack are stored unchanged out of place and
-    //    not touched in place.
-    for (;;) {
+    // 3. stream the tile: load a batch of units (kUnroll per thread, 8 loads of 16 B in
+    //    flight), rotate, store.  Rows of tokens outside the pack are not touched in
+    //    place and are copied unchanged out of place.
+    for (uint32_t base = threadIdx.x; base < units; base += kUnroll * kThreads) {
+        uint4 lo[kUnroll], hi[kUnroll];
+        __nv_bfloat16 *dst[kUnroll];
+        int tok[kUnroll], chunk[kUnroll];
+        bool live[kUnroll];
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+            const uint32_t u = base + k * kThreads;
+            live[k] = false;
+            tok[k] = -1;
+            chunk[k] = 0;
+            dst[k] = nullptr;
+            if (u < units) {
+                uint32_t i, c;
+                const __nv_bfloat16 *src;
+                __nv_bfloat16 *out;
+                locate(u, i, c, src, out);
+                const int pos = s_pos[i];
+                if (pos >= 0 || !a.in_place) {
+                    lo[k] = load_stream(src);
+                    hi[k] = load_stream(src + h);
+                    live[k] = true;
+                    dst[k] = out;
+                    tok[k] = pos >= 0 ? static_cast<int>(i) : -1;
+                    chunk[k] = static_cast<int>(c);
+                }
+            }
+        }
 #pragma unroll
         for (int k = 0; k < kUnroll; ++k) {
             if (!live[k]) continue;
-            const bool inside = s_pos[tok[k]] >= 0;
-            if (inside) {
+            if (tok[k] >= 0) {
                 const float4 *cs = s_cs + (tok[k] * 4) * cph + chunk[k];
                 rotate2(lo[k].x, hi[k].x, cs[0]);
                 rotate2(lo[k].y, hi[k].y, cs[cph]);
                 rotate2(lo[k].z, hi[k].z, cs[2 * cph]);
                 rotate2(lo[k].w, hi[k].w, cs[3 * cph]);
             }
-            if (inside || !a.in_place) {
-                store_stream(dst[k], lo[k]);
-                store_stream(dst[k] + h, hi[k]);
-            }
-        }
-        base += kUnroll * kThreads;
-        if (base >= units) break;
-#pragma unroll
-        for (int k = 0; k < kUnroll; ++k) {
-            const uint32_t u = base + k * kThreads;
-            live[k] = false;
-            if (u < units) {
-                uint32_t i, c;
-                const __nv_bfloat16 *src;
-                locate(u, i, c, src, dst[k]);
-                if (s_pos[i] >= 0 || !a.in_place) {
-                    lo[k] = load_stream(src);
-                    hi[k] = load_stream(src + h);
-                    live[k] = true;
-                    tok[k] = static_cast<int>(i);
-                    chunk[k] = static_cast<int>(c);
-                }
-            }
+            store_stream(dst[k], lo[k]);
+            store_stream(dst[k] + h, hi[k]);
         }
     }
 }
@@ -686,6 +650,7 @@ const char *rope_strerror(int status)
     case ROPE_ERR_UNSUPPORTED: return "global token indices and cache rows must stay within 2^24 (exact fp32 positions)";
     case ROPE_ERR_LAUNCH: return "the CUDA runtime rejected a launch";
     case ROPE_ERR_THETA: return "theta and position_scale must be finite and > 0";
+    case ROPE_ERR_KIND: return "unknown activation kind";
     default: return "unknown rope status";
     }
 }

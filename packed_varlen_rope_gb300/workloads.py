@@ -170,3 +170,24 @@ def sampled_rows(w: Workload, n_random: int = 4096, rank: int = 0) -> np.ndarray
     fixed = [0, 1, T - 1, cross - 1, cross, cross + 1]
     rows = np.unique(np.concatenate([rand, np.asarray([f for f in fixed if 0 <= f < T])]))
     return rows.astype(np.int64)
+
+
+@dataclass(frozen=True)
+class GluWorkload:
+    name: str
+    rows: int            # tokens
+    cols: int            # MLP intermediate width
+    kind: str            # "swiglu", "geglu" or "geglu_tanh"
+    description: str = ""
+
+
+# The MLP of the TRL page's long-context section: 1,048,576 tokens, each widened from
+# 2,560 to 9,728 (Qwen3-4B), act_fn = SiLU; and a 64k-token slice of it.
+GLU_WORKLOADS = {
+    "qwen3-4b-mlp-1m": GluWorkload("qwen3-4b-mlp-1m", 1 << 20, 9728, "swiglu",
+                                   "1,048,576 tokens x 9,728 (10.2e9 elements per matrix, int64 offsets)"),
+    "qwen3-4b-mlp-64k": GluWorkload("qwen3-4b-mlp-64k", 65_536, 9728, "swiglu",
+                                    "65,536 tokens x 9,728"),
+    "qwen3-4b-mlp-16k": GluWorkload("qwen3-4b-mlp-16k", 16_384, 9728, "swiglu",
+                                    "16,384 tokens x 9,728 (319 MB per matrix; profiling size)"),
+}

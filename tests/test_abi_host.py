@@ -13,6 +13,8 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "rope_qk.h")
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+                 if f.endswith(".h"))
 
 OK, ERR_NULL, ERR_SHAPE, ERR_HEAD_DIM, ERR_ALIGN, ERR_OVERLAP, ERR_UNSUPPORTED, ERR_LAUNCH, ERR_THETA = \
     0, -1, -2, -3, -4, -5, -6, -7, -8
@@ -27,9 +29,11 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = re.findall(r"^\s*(?:const\s+)?(?:int|int64_t|char|void)\s*\*?\s*(rope_\w+)\s*\(", text, flags=re.M)
+    names = []
+    for path in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(path).read(), flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?(?:int|int64_t|char|void)\s*\*?\s*((?:rope|glu)_\w+)\s*\(",
+                            text, flags=re.M)
     return sorted(set(names))
 
 
@@ -49,7 +53,8 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_header_is_plain_c(tmp_path):
     src = tmp_path / "use_header.c"
-    src.write_text('#include "rope_qk.h"\nint main(void) { return ROPE_QK_ABI_VERSION == 2 ? 0 : 1; }\n')
+    src.write_text('#include "rope_qk.h"\n#include "glu.h"\n'
+                   'int main(void) { return ROPE_QK_ABI_VERSION == 2 && GLU_GEGLU_TANH == 2 ? 0 : 1; }\n')
     subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Werror", "-pedantic", "-I", os.path.dirname(HEADER),
                            "-c", str(src), "-o", str(tmp_path / "use_header.o")])
 
@@ -200,6 +205,26 @@ def test_apply_argument_checks(lib):
     assert a(q_out=QO) == ERR_NULL
     assert a(q_out=QO, q_out_stride_token=256, q_out_stride_head=64, k_out=Q, k_out_stride_token=128,
              k_out_stride_head=64) == ERR_OVERLAP
+
+
+def test_glu_argument_checks(lib):
+    ERR_KIND = -9
+    E, G, H, DH = 0x10000000, 0x20000000, 0x30000000, 0x40000000
+    f = lambda kind=0, e=E, es=64, g=G, gs=64, h=H, hs=64, rows=4, cols=64: \
+        lib.glu_fwd(kind, e, es, g, gs, h, hs, rows, cols, None)  # noqa: E731
+    assert f(rows=0) == OK and f(cols=0) == OK
+    assert f(kind=3) == ERR_KIND and f(kind=-1) == ERR_KIND
+    assert f(rows=-1) == ERR_SHAPE and f(cols=12) == ERR_SHAPE and f(es=32) == ERR_SHAPE
+    assert f(rows=1 << 20, cols=1 << 14) == ERR_SHAPE                      # units >= 2^31
+    assert f(e=None) == ERR_NULL and f(h=None) == ERR_NULL
+    assert f(e=E + 8) == ERR_ALIGN and f(gs=68) == ERR_ALIGN
+    assert f(h=E + 64) == ERR_OVERLAP                                      # partial overlap
+    assert f(h=E, hs=128) == ERR_OVERLAP                                   # same start, other stride
+    b = lambda de=E + 0x8000000, dg=G + 0x8000000, **kw: lib.glu_bwd(  # noqa: E731
+        kw.get("kind", 0), DH, 64, E, 64, G, 64, de, 64, dg, 64, 4, 64, None)
+    assert b(de=H, dg=H) == ERR_OVERLAP                                    # outputs collide
+    assert b(de=DH + 16) == ERR_OVERLAP
+    assert b(kind=7) == ERR_KIND
 
 
 def test_binding_rejects_cpu_tensors():

@@ -64,7 +64,13 @@ static const double kInvSqrt2Pi = 0.39894228040143267793994605993438;    /* 1/sq
 static const double kInvSqrt2 = 0.70710678118654752440084436210485;      /* 1/sqrt(2) */
 static const double kGeluTanhC = 0.044715;
 
-static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+/* 1 / (1 + exp(-x)), evaluated through exp(-|x|) so that it cannot overflow: for
+ * x < 0 it is exp(x) / (1 + exp(x)), which keeps its value far in the left tail. */
+static double sigmoid(double x)
+{
+    double t = exp(-fabs(x));
+    return x >= 0.0 ? 1.0 / (1.0 + t) : t / (1.0 + t);
+}
 
 /* act(x) and act'(x) for kind 0 = SwiGLU, 1 = GeGLU (erf), 2 = GeGLU (tanh), written in
  * forms without cancellation in the tails (identical in exact arithmetic):

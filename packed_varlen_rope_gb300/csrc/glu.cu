@@ -42,13 +42,17 @@ struct GluArgs {
     FastDiv div_cols8;
 };
 
-// sigmoid(y) and sigmoid(-y) from one exponential: with t = exp(-y),
-// sigmoid(y) = 1 / (1 + t) and sigmoid(-y) = t / (1 + t) (= 1 once t overflows).
+// sigmoid(y) and sigmoid(-y) from one exponential that cannot overflow: with
+// t = exp(-|y|) in (0, 1], sigmoid(|y|) = 1 / (1 + t) and sigmoid(-|y|) = t / (1 + t),
+// so far in the tails the small one keeps its (possibly subnormal) value instead of
+// collapsing to zero.
 __device__ __forceinline__ void sigmoid_pair(float y, float &sp, float &sm)
 {
-    const float t = expf(-y);
-    sp = __frcp_rn(1.0f + t);
-    sm = isinf(t) ? 1.0f : t * sp;
+    const float t = expf(-fabsf(y));
+    const float big = __frcp_rn(1.0f + t);
+    const float small = t * big;
+    sp = y >= 0.0f ? big : small;
+    sm = y >= 0.0f ? small : big;
 }
 
 // act(x) and act'(x), in forms without cancellation in the tails.

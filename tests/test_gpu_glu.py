@@ -132,8 +132,12 @@ def test_glu_fused_gate_up_and_in_place(dev, kind):
 
 
 def test_glu_special_values(dev):
+    # includes the far left tails where sigmoid, Phi or sigmoid(2u) are tiny but the
+    # products are still normal bf16 numbers (-87.5 ... -95 for SiLU, about -10 for the
+    # tanh form, -13 for erf)
     vals = np.array([0.0, -0.0, 1.0, -1.0, 8.0, -8.0, 20.0, -20.0, 88.0, -88.0, 100.0, -100.0, 1e-30, -1e-30,
-                     -1.2784645, 3.0e38, -3.0e38, 1e-40], dtype=np.float32)
+                     -1.2784645, 3.0e38, -3.0e38, 1e-40, -87.5, -89.0, -95.0, -9.9, -10.1, -10.5, -13.0,
+                     -13.5], dtype=np.float32)
     rng = np.random.Generator(np.random.PCG64(4))
     shape = (64, 64)
     eb = torch.from_numpy(rng.choice(vals, size=shape).astype(np.float32)).to(torch.bfloat16) \

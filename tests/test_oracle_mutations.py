@@ -34,7 +34,7 @@ MUTATIONS = {
     "scale-multiplies": ("w_out[j] = (float)(pow(theta, e) / scale);", "w_out[j] = (float)(pow(theta, e) * scale);"),
     "scale-ignored": ("w_out[j] = (float)(pow(theta, e) / scale);", "w_out[j] = (float)pow(theta, e);"),
     # SwiGLU / GeGLU oracle
-    "glu-sigmoid-sign": ("return 1.0 / (1.0 + exp(-x));", "return 1.0 / (1.0 + exp(x));", GLU),
+    "glu-sigmoid-sign": ("return x >= 0.0 ? 1.0 / (1.0 + t) : t / (1.0 + t);", "return x >= 0.0 ? t / (1.0 + t) : 1.0 / (1.0 + t);", GLU),
     "glu-silu-derivative": ("*dact = s * (1.0 + x * sigmoid(-x));", "*dact = s * (1.0 + x * sigmoid(x));", GLU),
     "glu-erf-argument": ("0.5 * erfc(-x * kInvSqrt2);", "0.5 * erfc(-x * kSqrt2OverPi);", GLU),
     "glu-erfc-sign": ("0.5 * erfc(-x * kInvSqrt2);", "0.5 * erfc(x * kInvSqrt2);", GLU),

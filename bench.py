@@ -397,24 +397,24 @@ def run_ours(args, rank, world, local):
 
 
 def end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev):
-    """Same metric through the public call with the inputs in pinned host memory:
-    every step copies Q, K, dQ, dK host->device, runs forward and backward, and copies
-    the four results device->host."""
+    """Same metric through the public host-buffer call (rope_qk_host) with the inputs in
+    pinned host memory: every step streams Q, K (forward) and dQ, dK (backward) from the
+    host through a device workspace in chunks and back, copies overlapped with the
+    rotation; the results are complete in host memory when the step's stream ends."""
     import torch
 
-    host_in = [t.to("cpu").pin_memory() for t in (q, k, dq, dk)]
-    host_out = [torch.empty_like(t).pin_memory() for t in host_in]
-    dev_buf = [torch.empty_like(t) for t in (q, k, dq, dk)]
-    h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    host = [t.to("cpu").pin_memory() for t in (q, k, dq, dk)]
+    work = [t.clone().pin_memory() for t in host]
+    per_token = (w.n_q_heads + w.n_kv_heads) * w.head_dim * 2
+    chunk = max(8, (pack.total_tokens // 16) // 8 * 8)
+    ws = torch.empty(2 * chunk * per_token + 4096, dtype=torch.uint8, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in host)
 
     def step():
-        for d, h in zip(dev_buf, host_in):
-            d.copy_(h, non_blocking=True)
-        pr.rope_qk_fwd(dev_buf[0], dev_buf[1], cu, w.theta, cos_sin_cache=cache)
-        pr.rope_qk_bwd(dev_buf[2], dev_buf[3], cu, w.theta, cos_sin_cache=cache)
-        for h, d in zip(host_out, dev_buf):
-            h.copy_(d, non_blocking=True)
+        pr.rope_qk_host(host[0], host[1], w.theta, ws, cu_seqlens=cu, cos_sin_cache=cache,
+                        q_out=work[0], k_out=work[1])
+        pr.rope_qk_host(host[2], host[3], w.theta, ws, cu_seqlens=cu, cos_sin_cache=cache, backward=True,
+                        q_out=work[2], k_out=work[3])
 
     step()
     torch.cuda.synchronize()
@@ -430,7 +430,8 @@ def end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev):
     torch.cuda.synchronize()
     ms = max_over_ranks(s.elapsed_time(e) / E, world, dev)
     return {"value": whole_job_tokens_per_s(world, pack.valid_tokens, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": E}
+            "d2h_bytes_per_step": h2d, "ms_per_step": ms, "steps": E,
+            "path": "rope_qk_host: pinned host buffers streamed in %d-token chunks" % chunk}
 
 
 def run_glu(args, rank, world, local):

@@ -31,8 +31,10 @@
  *
  * Aliasing.  An output may be exactly one of the inputs (same pointer and stride): it
  * is then overwritten in place element by element (e.g. h over g, or de over e and dg
- * over g, which needs no extra memory).  Otherwise every output must share no address
- * range with any input, and the two outputs of the backward none with each other.
+ * over g, which needs no extra memory).  Otherwise every output must share no element
+ * with any input, and the two outputs of the backward none with each other: either
+ * their address ranges are disjoint, or they have the same row stride and sit side by
+ * side inside it (the two halves of one [rows, 2I] buffer).
  *
  * Ownership, streams and errors as in rope_qk.h: device pointers owned by the caller,
  * no allocation, asynchronous on `stream`, ROPE_OK or a negative rope_status, checked

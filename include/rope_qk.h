@@ -178,6 +178,30 @@ typedef struct rope_qk_desc {
 int rope_qk_apply(const rope_qk_desc *desc, void *stream);
 
 /*
+ * Host-buffer form of rope_qk_apply, for Q and K that live in host memory.  desc->q,
+ * k, q_out, k_out are HOST pointers to contiguous bf16 [total_tokens, heads, head_dim]
+ * (q_out, k_out both NULL: results go back into q and k).  Pinned memory makes the
+ * copies asynchronous and overlapped; pageable memory works, with synchronous copies.
+ * Every other field is as for rope_qk_apply (cu_seqlens, position_ids and the cache
+ * are DEVICE pointers).
+ *
+ * workspace: DEVICE staging memory of workspace_bytes, 256-byte aligned, owned by the
+ * caller.  It holds two slots of `chunk` tokens' Q and K rows, chunk =
+ * workspace_bytes / (2 * (n_q_heads + n_kv_heads) * head_dim * 2) rounded down to a
+ * multiple of 8 (ROPE_ERR_UNSUPPORTED below 8).  The pack is walked chunk by chunk:
+ * the host-to-device copy of one chunk, the rotation of the previous one and the
+ * device-to-host copy of the one before overlap, the copies on two streams the library
+ * creates per device on first use and keeps.  Each chunk is rotated with its global
+ * token offset (or its slice of position_ids), so the result is that of one rotation
+ * of the whole pack.
+ *
+ * `stream` runs the rotations and then waits for the last copy to the host: once it
+ * reaches that point, the host outputs are complete.  The host buffers and the
+ * workspace must stay untouched until then.  Enqueueing is serialised by a lock.
+ */
+int rope_qk_host(const rope_qk_desc *desc, void *workspace, int64_t workspace_bytes, void *stream);
+
+/*
  * Fill a cos/sin cache with (c, s) of every position p < cache_rows and frequency
  * j < head_dim/2, by the arithmetic above (binary64 cos/sin on the device, rounded to
  * binary32).  cache: device float[cache_rows][4][head_dim/16][4], 16-byte aligned,

@@ -29,6 +29,7 @@ from ._binding import (  # noqa: F401
     rope_qk_apply,
     rope_qk_bwd,
     rope_qk_fwd,
+    rope_qk_host,
     rope_qk_inv_freq,
     rope_qk_positions,
     rope_strerror,

@@ -18,7 +18,7 @@ EXPORTS = (
     "rope_qk_fwd", "rope_qk_bwd", "rope_qk_apply", "rope_cos_sin_cache_build",
     "rope_cos_sin_cache_build_scaled", "rope_cos_sin_cache_bytes", "rope_qk_positions",
     "rope_validate_cu_seqlens", "rope_qk_inv_freq", "rope_strerror", "rope_qk_abi_version",
-    "glu_fwd", "glu_bwd",
+    "glu_fwd", "glu_bwd", "rope_qk_host",
 )
 
 GLU_KINDS = {"swiglu": 0, "geglu": 1, "geglu_tanh": 2}
@@ -71,6 +71,8 @@ def load_library(path: Optional[str] = None):
         getattr(lib, name).restype = ctypes.c_int
     lib.rope_qk_apply.argtypes = [ctypes.POINTER(RopeQKDesc), vp]
     lib.rope_qk_apply.restype = ctypes.c_int
+    lib.rope_qk_host.argtypes = [ctypes.POINTER(RopeQKDesc), vp, i64, vp]
+    lib.rope_qk_host.restype = ctypes.c_int
     lib.rope_cos_sin_cache_build.argtypes = [vp, i64, i32, dbl, vp]
     lib.rope_cos_sin_cache_build.restype = ctypes.c_int
     lib.rope_cos_sin_cache_build_scaled.argtypes = [vp, i64, i32, dbl, dbl, vp]
@@ -361,3 +363,53 @@ def glu_bwd(kind: str, dh, e, g, de=None, dg=None, stream=None):
     st = load_library().glu_bwd(GLU_KINDS[kind], *args, shape[0], shape[1], _stream(stream, e.device))
     _check("glu_bwd", st)
     return de, dg
+
+
+def rope_qk_host(q, k, theta: float, workspace, cu_seqlens=None, position_ids=None, backward: bool = False,
+                 q_out=None, k_out=None, token_offset: int = 0, position_scale: float = 1.0,
+                 cos_sin_cache=None, stream=None):
+    """Rotate Q [T, Hq, d] and K [T, Hkv, d] that live in HOST memory (contiguous bf16 CPU
+    tensors, pinned for overlapped copies), streaming them through ``workspace`` (a
+    CUDA tensor of any dtype used as raw staging memory).  cu_seqlens / position_ids /
+    cos_sin_cache are CUDA tensors.  Asynchronous on ``stream``: synchronise it before
+    reading the results.  Returns (q, k) or (q_out, k_out)."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("q_out", q_out), ("k_out", k_out)):
+        if t is None:
+            continue
+        if t.dtype != torch.bfloat16 or t.is_cuda or not t.is_contiguous() or t.dim() != 3:
+            raise ValueError("%s must be a contiguous host (CPU) bf16 tensor [tokens, heads, head_dim]" % name)
+    if q.shape[0] != k.shape[0] or q.shape[2] != k.shape[2]:
+        raise ValueError("q and k must share tokens and head_dim")
+    if (q_out is None) != (k_out is None):
+        raise ValueError("give both q_out and k_out, or neither")
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    T, hq, d = q.shape
+    dev = workspace.device
+    desc = RopeQKDesc()
+    desc.q, desc.q_stride_token, desc.q_stride_head = _ptr(q), hq * d, d
+    desc.k, desc.k_stride_token, desc.k_stride_head = _ptr(k), k.shape[1] * d, d
+    if q_out is not None:
+        desc.q_out, desc.q_out_stride_token, desc.q_out_stride_head = _ptr(q_out), hq * d, d
+        desc.k_out, desc.k_out_stride_token, desc.k_out_stride_head = _ptr(k_out), k.shape[1] * d, d
+    if position_ids is not None:
+        if position_ids.dtype != torch.int32 or position_ids.device != dev or position_ids.numel() != T:
+            raise ValueError("position_ids must be an int32 [tokens] tensor on the workspace's device")
+        desc.position_ids = _ptr(position_ids)
+    elif cu_seqlens is not None:
+        _check_cu(cu_seqlens, dev)
+        desc.cu_seqlens, desc.n_seqs = _ptr(cu_seqlens), cu_seqlens.numel() - 1
+    else:
+        raise ValueError("give cu_seqlens or position_ids")
+    desc.n_q_heads, desc.n_kv_heads, desc.head_dim = hq, k.shape[1], d
+    desc.total_tokens, desc.token_offset = T, int(token_offset)
+    desc.theta, desc.position_scale = float(theta), float(position_scale)
+    if cos_sin_cache is not None:
+        desc.cos_sin_cache, desc.cache_rows = _ptr(cos_sin_cache), cos_sin_cache.shape[0]
+    desc.backward = 1 if backward else 0
+    nbytes = workspace.numel() * workspace.element_size()
+    st = load_library().rope_qk_host(ctypes.byref(desc), _ptr(workspace), nbytes, _stream(stream, dev))
+    _check("rope_qk_host", st)
+    return (q, k) if q_out is None else (q_out, k_out)

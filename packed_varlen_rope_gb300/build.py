@@ -8,7 +8,7 @@ import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
-SOURCES = [os.path.join(HERE, "csrc", "rope_qk.cu"), os.path.join(HERE, "csrc", "glu.cu")]
+SOURCES = [os.path.join(HERE, "csrc", n) for n in ("rope_qk.cu", "rope_host.cu", "glu.cu")]
 HEADERS = [os.path.join(ROOT, "include", "rope_qk.h"), os.path.join(ROOT, "include", "glu.h"),
            os.path.join(HERE, "csrc", "fastdiv.cuh")]
 LIB_PATH = os.path.join(HERE, "librope_qk.so")

@@ -171,12 +171,27 @@ bool ranges_overlap(const Mat &a, const Mat &b, int64_t rows, int64_t cols)
            pb < pa + static_cast<uintptr_t>(span_bytes(a, rows, cols));
 }
 
-// An output is fine if it is exactly an input, else it must not touch any input.
+// Two matrices share no element: their address ranges are disjoint, or they have the
+// same row stride S and b's row block sits beside a's inside every period of S (the
+// gate and up halves of one [rows, 2I] buffer).
+bool mats_disjoint(const Mat &a, const Mat &b, int64_t rows, int64_t cols)
+{
+    if (!ranges_overlap(a, b, rows, cols)) return true;
+    if (rows <= 1 || a.stride != b.stride || a.stride < cols) return false;
+    const int64_t S = a.stride;
+    const int64_t delta_bytes = static_cast<int64_t>(reinterpret_cast<uintptr_t>(b.p)) -
+                                static_cast<int64_t>(reinterpret_cast<uintptr_t>(a.p));
+    if (delta_bytes % 2 != 0) return false;
+    const int64_t r = ((delta_bytes / 2) % S + S) % S;
+    return r >= cols && r + cols <= S;
+}
+
+// An output is fine if it is exactly an input, else it must share no element with it.
 int check_output(const Mat &o, const Mat *in, int n_in, int64_t rows, int64_t cols)
 {
     for (int i = 0; i < n_in; ++i) {
         if (o.p == in[i].p && o.stride == in[i].stride) continue;
-        if (ranges_overlap(o, in[i], rows, cols)) return ROPE_ERR_OVERLAP;
+        if (!mats_disjoint(o, in[i], rows, cols)) return ROPE_ERR_OVERLAP;
     }
     return ROPE_OK;
 }
@@ -275,7 +290,7 @@ int glu_bwd(int32_t kind, const void *dh, int64_t dh_stride, const void *e, int6
     const Mat out[2] = {{de, de_stride}, {dg, dg_stride}};
     if ((rc = check_mats(in, 3, rows, cols)) != ROPE_OK) return rc;
     if ((rc = check_mats(out, 2, rows, cols)) != ROPE_OK) return rc;
-    if (ranges_overlap(out[0], out[1], rows, cols)) return ROPE_ERR_OVERLAP;
+    if (!mats_disjoint(out[0], out[1], rows, cols)) return ROPE_ERR_OVERLAP;
     for (const Mat &o : out)
         if ((rc = check_output(o, in, 3, rows, cols)) != ROPE_OK) return rc;
     a.dh = static_cast<const __nv_bfloat16 *>(dh);

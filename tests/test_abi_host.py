@@ -223,6 +223,9 @@ def test_glu_argument_checks(lib):
     b = lambda de=E + 0x8000000, dg=G + 0x8000000, **kw: lib.glu_bwd(  # noqa: E731
         kw.get("kind", 0), DH, 64, E, 64, G, 64, de, 64, dg, 64, 4, 64, None)
     assert b(de=H, dg=H) == ERR_OVERLAP                                    # outputs collide
+    # side-by-side halves of one [4, 128] buffer are disjoint; shifted by 8 they are not
+    fused = lambda off: lib.glu_fwd(0, E, 128, E + 128, 128, E + off, 128, 4, 64, None)  # noqa: E731
+    assert fused(16) == ERR_OVERLAP and fused(64) == ERR_OVERLAP
     assert b(de=DH + 16) == ERR_OVERLAP
     assert b(kind=7) == ERR_KIND
 

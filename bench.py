@@ -79,8 +79,13 @@ def measured_peak():
 
 
 def kernel_source_hash() -> str:
-    with open(KERNEL_SOURCE, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+    """sha256 of the RoPE kernel's device code: rope_qk.cu up to its host-side section,
+    then fastdiv.cuh.  Host-only edits (argument checks, error strings) keep it."""
+    text = open(KERNEL_SOURCE).read()
+    device_part = text.split("// ------------------------------------------------------------------ host side")[0]
+    h = hashlib.sha256(device_part.encode())
+    h.update(open(os.path.join(os.path.dirname(KERNEL_SOURCE), "fastdiv.cuh")).read().encode())
+    return h.hexdigest()
 
 
 def profiled_traffic():

@@ -65,7 +65,8 @@ typedef enum rope_status {
                                    are exact in binary32 only up to there) */
     ROPE_ERR_LAUNCH = -7,       /* the CUDA runtime refused a launch or copy */
     ROPE_ERR_THETA = -8,        /* theta or position_scale not finite and > 0 */
-    ROPE_ERR_KIND = -9          /* unknown activation kind (glu.h) */
+    ROPE_ERR_KIND = -9,         /* unknown activation kind (glu.h) */
+    ROPE_ERR_WORKSPACE = -10    /* one token's Q and K rows do not fit the static staging */
 } rope_status;
 
 /* Bits of the word rope_validate_cu_seqlens writes. */
@@ -200,6 +201,30 @@ int rope_qk_apply(const rope_qk_desc *desc, void *stream);
  * workspace must stay untouched until then.  Enqueueing is serialised by a lock.
  */
 int rope_qk_host(const rope_qk_desc *desc, void *workspace, int64_t workspace_bytes, void *stream);
+
+/*
+ * rope_qk_host for callers that cannot allocate device memory.  The source pages
+ * describe nothing like it; it exists for code that may not call cudaMalloc/cudaFree
+ * or any allocating routine: a plugin or embedding runtime that hands out no device
+ * allocator, a process whose device memory is entirely reserved by another allocator
+ * (a framework's caching allocator), or a loop that must not add the implicit
+ * synchronisation of cudaMalloc/cudaFree.  It takes no workspace: it stages the chunks
+ * in a 32 MiB device array that is part of this library (every GPU that loads the
+ * library keeps those 32 MiB until the process exits), and it allocates nothing.
+ *
+ * Same descriptor and results as rope_qk_host.  Chunks of up to
+ * 32 MiB / ((n_q_heads + n_kv_heads) * head_dim * 2) tokens are copied in, rotated and
+ * copied out one after the other, all on `stream` (no overlap of copies and rotation).
+ * A shape whose single token does not fit is rejected with ROPE_ERR_WORKSPACE.
+ *
+ * The first call on a device looks up the array's device address (once per device,
+ * that device current); make that first call before any stream capture.  Every call
+ * uses the same array, which keeps whatever the last call left in it (nothing in it
+ * needs to start at zero).  Calls that overlap on the GPU (on different streams
+ * without ordering between them, or from several host threads at once) race on it:
+ * order them.
+ */
+int rope_qk_host_static(const rope_qk_desc *desc, void *stream);
 
 /*
  * Fill a cos/sin cache with (c, s) of every position p < cache_rows and frequency

@@ -18,7 +18,7 @@ EXPORTS = (
     "rope_qk_fwd", "rope_qk_bwd", "rope_qk_apply", "rope_cos_sin_cache_build",
     "rope_cos_sin_cache_build_scaled", "rope_cos_sin_cache_bytes", "rope_qk_positions",
     "rope_validate_cu_seqlens", "rope_qk_inv_freq", "rope_strerror", "rope_qk_abi_version",
-    "glu_fwd", "glu_bwd", "rope_qk_host",
+    "glu_fwd", "glu_bwd", "rope_qk_host", "rope_qk_host_static",
 )
 
 GLU_KINDS = {"swiglu": 0, "geglu": 1, "geglu_tanh": 2}
@@ -73,6 +73,8 @@ def load_library(path: Optional[str] = None):
     lib.rope_qk_apply.restype = ctypes.c_int
     lib.rope_qk_host.argtypes = [ctypes.POINTER(RopeQKDesc), vp, i64, vp]
     lib.rope_qk_host.restype = ctypes.c_int
+    lib.rope_qk_host_static.argtypes = [ctypes.POINTER(RopeQKDesc), vp]
+    lib.rope_qk_host_static.restype = ctypes.c_int
     lib.rope_cos_sin_cache_build.argtypes = [vp, i64, i32, dbl, vp]
     lib.rope_cos_sin_cache_build.restype = ctypes.c_int
     lib.rope_cos_sin_cache_build_scaled.argtypes = [vp, i64, i32, dbl, dbl, vp]
@@ -365,14 +367,16 @@ def glu_bwd(kind: str, dh, e, g, de=None, dg=None, stream=None):
     return de, dg
 
 
-def rope_qk_host(q, k, theta: float, workspace, cu_seqlens=None, position_ids=None, backward: bool = False,
+def rope_qk_host(q, k, theta: float, workspace=None, cu_seqlens=None, position_ids=None, backward: bool = False,
                  q_out=None, k_out=None, token_offset: int = 0, position_scale: float = 1.0,
-                 cos_sin_cache=None, stream=None):
+                 cos_sin_cache=None, stream=None, device=None):
     """Rotate Q [T, Hq, d] and K [T, Hkv, d] that live in HOST memory (contiguous bf16 CPU
     tensors, pinned for overlapped copies), streaming them through ``workspace`` (a
-    CUDA tensor of any dtype used as raw staging memory).  cu_seqlens / position_ids /
-    cos_sin_cache are CUDA tensors.  Asynchronous on ``stream``: synchronise it before
-    reading the results.  Returns (q, k) or (q_out, k_out)."""
+    CUDA tensor of any dtype used as raw staging memory).  Without a workspace the
+    library's built-in 32 MiB staging array is used and nothing is allocated
+    (``rope_qk_host_static``; ``device`` then names the GPU).  cu_seqlens /
+    position_ids / cos_sin_cache are CUDA tensors.  Asynchronous on ``stream``:
+    synchronise it before reading the results.  Returns (q, k) or (q_out, k_out)."""
     import torch
 
     for name, t in (("q", q), ("k", k), ("q_out", q_out), ("k_out", k_out)):
@@ -384,10 +388,15 @@ def rope_qk_host(q, k, theta: float, workspace, cu_seqlens=None, position_ids=No
         raise ValueError("q and k must share tokens and head_dim")
     if (q_out is None) != (k_out is None):
         raise ValueError("give both q_out and k_out, or neither")
-    if not workspace.is_cuda or not workspace.is_contiguous():
+    if workspace is not None and (not workspace.is_cuda or not workspace.is_contiguous()):
         raise ValueError("workspace must be a contiguous CUDA tensor")
     T, hq, d = q.shape
-    dev = workspace.device
+    if workspace is not None:
+        dev = workspace.device
+    elif device is not None:
+        dev = torch.device(device)
+    else:
+        dev = torch.device("cuda", torch.cuda.current_device())
     desc = RopeQKDesc()
     desc.q, desc.q_stride_token, desc.q_stride_head = _ptr(q), hq * d, d
     desc.k, desc.k_stride_token, desc.k_stride_head = _ptr(k), k.shape[1] * d, d
@@ -409,7 +418,12 @@ def rope_qk_host(q, k, theta: float, workspace, cu_seqlens=None, position_ids=No
     if cos_sin_cache is not None:
         desc.cos_sin_cache, desc.cache_rows = _ptr(cos_sin_cache), cos_sin_cache.shape[0]
     desc.backward = 1 if backward else 0
-    nbytes = workspace.numel() * workspace.element_size()
-    st = load_library().rope_qk_host(ctypes.byref(desc), _ptr(workspace), nbytes, _stream(stream, dev))
-    _check("rope_qk_host", st)
+    if workspace is None:
+        # no workspace: the library's own static staging array (rope_qk_host_static)
+        st = load_library().rope_qk_host_static(ctypes.byref(desc), _stream(stream, dev))
+        _check("rope_qk_host_static", st)
+    else:
+        nbytes = workspace.numel() * workspace.element_size()
+        st = load_library().rope_qk_host(ctypes.byref(desc), _ptr(workspace), nbytes, _stream(stream, dev))
+        _check("rope_qk_host", st)
     return (q, k) if q_out is None else (q_out, k_out)

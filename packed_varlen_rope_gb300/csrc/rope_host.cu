@@ -157,3 +157,92 @@ extern "C" int rope_qk_host(const rope_qk_desc *desc, void *workspace, int64_t w
 {
     return rope_qk_host_impl(desc, workspace, workspace_bytes, stream);
 }
+
+// ---------------------------------------------------------------- allocation-free variant
+//
+// Staging memory that needs no allocation call: a file-scope device array.  Every GPU on
+// which this library's device code is loaded keeps these 32 MiB until the process
+// exits.  Host code must not use the array's name as a device address (on the host it
+// is only a stand-in); the address is looked up once per device with
+// cudaGetSymbolAddress, with that device current.
+namespace {
+
+constexpr int64_t kStaticStagingBytes = int64_t(32) << 20;
+std::mutex g_static_mutex;
+void *g_static_staging_addr[kMaxDevices];
+
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_static_staging[kStaticStagingBytes];
+
+extern "C" int rope_qk_host_static(const rope_qk_desc *desc, void *stream)
+{
+    if (desc == nullptr) return ROPE_ERR_NULL;
+    const rope_qk_desc &p = *desc;
+    if (p.total_tokens < 0 || p.n_q_heads < 1 || p.n_kv_heads < 1) return ROPE_ERR_SHAPE;
+    if (p.head_dim < 16 || p.head_dim > 256 || p.head_dim % 16 != 0) return ROPE_ERR_HEAD_DIM;
+    if (p.total_tokens == 0) return ROPE_OK;
+    const int64_t q_row = static_cast<int64_t>(p.n_q_heads) * p.head_dim * 2;
+    const int64_t k_row = static_cast<int64_t>(p.n_kv_heads) * p.head_dim * 2;
+    // one chunk must hold at least one token's Q and K rows
+    if (q_row + k_row > kStaticStagingBytes) return ROPE_ERR_WORKSPACE;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ROPE_ERR_LAUNCH;
+    void *staging = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_static_mutex);
+        if (g_static_staging_addr[dev] == nullptr) {
+            void *addr = nullptr;
+            if (cudaGetSymbolAddress(&addr, g_static_staging) != cudaSuccess || addr == nullptr)
+                return ROPE_ERR_LAUNCH;
+            g_static_staging_addr[dev] = addr;
+        }
+        staging = g_static_staging_addr[dev];
+    }
+    if (p.q == nullptr || p.k == nullptr) return ROPE_ERR_NULL;
+    if ((p.q_out == nullptr) != (p.k_out == nullptr)) return ROPE_ERR_NULL;
+    const int32_t d = p.head_dim;
+    if (!contiguous(p.q, p.q_stride_token, p.q_stride_head, p.n_q_heads, d) ||
+        !contiguous(p.k, p.k_stride_token, p.k_stride_head, p.n_kv_heads, d) ||
+        !contiguous(p.q_out, p.q_out_stride_token, p.q_out_stride_head, p.n_q_heads, d) ||
+        !contiguous(p.k_out, p.k_out_stride_token, p.k_out_stride_head, p.n_kv_heads, d))
+        return ROPE_ERR_SHAPE;
+
+    // one slot, everything in order on the caller's stream: copy a chunk in, rotate it,
+    // copy it out, next chunk
+    const int64_t T = p.total_tokens;
+    int64_t chunk = kStaticStagingBytes / (q_row + k_row);
+    if (chunk > T) chunk = T;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *const dq = static_cast<char *>(staging);
+    char *const dk = dq + chunk * q_row;
+    char *const q_host = static_cast<char *>(p.q);
+    char *const k_host = static_cast<char *>(p.k);
+    char *const qo_host = static_cast<char *>(p.q_out != nullptr ? p.q_out : p.q);
+    char *const ko_host = static_cast<char *>(p.k_out != nullptr ? p.k_out : p.k);
+    for (int64_t t0 = 0; t0 < T; t0 += chunk) {
+        const int64_t n = (T - t0) < chunk ? (T - t0) : chunk;
+        if (cudaMemcpyAsync(dq, q_host + t0 * q_row, n * q_row, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaMemcpyAsync(dk, k_host + t0 * k_row, n * k_row, cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return ROPE_ERR_LAUNCH;
+        rope_qk_desc cd = p;
+        cd.q = dq;
+        cd.k = dk;
+        cd.q_stride_token = q_row / 2;
+        cd.q_stride_head = d;
+        cd.k_stride_token = k_row / 2;
+        cd.k_stride_head = d;
+        cd.q_out = nullptr;
+        cd.k_out = nullptr;
+        cd.total_tokens = n;
+        if (p.position_ids != nullptr) cd.position_ids = p.position_ids + t0;
+        else cd.token_offset = p.token_offset + t0;
+        const int rc = rope_qk_apply(&cd, stream);
+        if (rc != ROPE_OK) return rc;
+        if (cudaMemcpyAsync(qo_host + t0 * q_row, dq, n * q_row, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+            cudaMemcpyAsync(ko_host + t0 * k_row, dk, n * k_row, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+            return ROPE_ERR_LAUNCH;
+    }
+    return ROPE_OK;
+}

@@ -651,6 +651,7 @@ const char *rope_strerror(int status)
     case ROPE_ERR_LAUNCH: return "the CUDA runtime rejected a launch";
     case ROPE_ERR_THETA: return "theta and position_scale must be finite and > 0";
     case ROPE_ERR_KIND: return "unknown activation kind";
+    case ROPE_ERR_WORKSPACE: return "one token's Q and K rows exceed the 32 MiB static staging array";
     default: return "unknown rope status";
     }
 }

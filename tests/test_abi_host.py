@@ -62,7 +62,7 @@ def test_header_is_plain_c(tmp_path):
 def test_abi_version_and_strerror(lib):
     assert lib.rope_qk_abi_version() == 2
     for code in (OK, ERR_NULL, ERR_SHAPE, ERR_HEAD_DIM, ERR_ALIGN, ERR_OVERLAP, ERR_UNSUPPORTED,
-                 ERR_LAUNCH, ERR_THETA):
+                 ERR_LAUNCH, ERR_THETA, -9, -10):
         assert lib.rope_strerror(code)
     assert lib.rope_strerror(-99) == b"unknown rope status"
 

@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define ROPE_QK_ABI_VERSION 2
+#define ROPE_QK_ABI_VERSION 3
 
 typedef enum rope_status {
     ROPE_OK = 0,
@@ -141,6 +141,10 @@ int rope_qk_bwd(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs,
  * tokens [a, b) of a pack pass the whole pack's cu_seqlens with token_offset = a
  * (token_offset + total_tokens <= 2^24).
  *
+ * seq_used.  Optional, with cu_seqlens: sample s uses only its first seq_used[s]
+ * tokens; the rest of its rows (the padding of a padded batch laid out with uniform
+ * cu_seqlens) are left out like tokens outside the pack.  Ignored with position_ids.
+ *
  * position_scale.  Linear position rescale (> 0; 1.0 = none): every frequency is
  * divided by it in binary64 before the rounding to binary32, i.e. position p acts as
  * p / position_scale.  A cos/sin cache must come from rope_cos_sin_cache_build_scaled
@@ -173,6 +177,7 @@ typedef struct rope_qk_desc {
     int64_t cache_rows;
     int32_t backward;              /* 0: rotation; nonzero: transpose (sin negated)   */
     int32_t reserved;              /* set to 0                                        */
+    const int32_t *seq_used;       /* optional device int32 [n_seqs], with cu_seqlens */
 } rope_qk_desc;
 
 /* Apply the rotation a descriptor describes (asynchronous on `stream`). */

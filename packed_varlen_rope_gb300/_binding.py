@@ -45,6 +45,7 @@ class RopeQKDesc(ctypes.Structure):
         ("theta", ctypes.c_double), ("position_scale", ctypes.c_double),
         ("cos_sin_cache", ctypes.c_void_p), ("cache_rows", ctypes.c_int64),
         ("backward", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("seq_used", ctypes.c_void_p),
     ]
 
 
@@ -263,14 +264,15 @@ def _view_args(t, name):
 
 def rope_qk_apply(q, k, theta: float, cu_seqlens=None, position_ids=None, backward: bool = False,
                   q_out=None, k_out=None, token_offset: int = 0, position_scale: float = 1.0,
-                  cos_sin_cache=None, stream=None):
+                  cos_sin_cache=None, stream=None, seq_used=None):
     """General form of the rotation (C entry point ``rope_qk_apply``).
 
     q, k: bf16 CUDA views [T, Hq, d] and [T, Hkv, d] with any token/head strides
     (head_dim contiguous) -- e.g. the Q and K slices of one fused QKV output, rotated in
     place.  Positions come from ``position_ids`` (int32 [T]) if given, else from
-    ``cu_seqlens`` with row r read as token ``token_offset + r``.  ``position_scale``
-    is the linear position rescale (1 = none).  Returns (q, k) in place, else (q_out,
+    ``cu_seqlens`` with row r read as token ``token_offset + r`` (and, with
+    ``seq_used``, only the first seq_used[s] tokens of sample s rotated).
+    ``position_scale`` is the linear position rescale (1 = none).  Returns (q, k) in place, else (q_out,
     k_out)."""
     qp, q_ts, q_hs = _view_args(q, "q")
     kp, k_ts, k_hs = _view_args(k, "k")
@@ -298,6 +300,11 @@ def rope_qk_apply(q, k, theta: float, cu_seqlens=None, position_ids=None, backwa
         _check_cu(cu_seqlens, q.device)
         desc.cu_seqlens = _ptr(cu_seqlens)
         desc.n_seqs = cu_seqlens.numel() - 1
+        if seq_used is not None:
+            _check_cu(seq_used, q.device)
+            if seq_used.numel() != desc.n_seqs:
+                raise ValueError("seq_used must hold one int32 per sample")
+            desc.seq_used = _ptr(seq_used)
     else:
         raise ValueError("give cu_seqlens or position_ids")
     desc.n_q_heads, desc.n_kv_heads, desc.head_dim = hq, k.shape[1], d

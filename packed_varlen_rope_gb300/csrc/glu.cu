@@ -42,14 +42,40 @@ struct GluArgs {
     FastDiv div_cols8;
 };
 
+// 2^x and 1/x from the special-function unit (PTX ex2.approx / rcp.approx, a few units
+// in the last binary32 place; they flush subnormal results, so they are used only where
+// results stay normal).
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // sigmoid(y) and sigmoid(-y) from one exponential that cannot overflow: with
 // t = exp(-|y|) in (0, 1], sigmoid(|y|) = 1 / (1 + t) and sigmoid(-|y|) = t / (1 + t),
 // so far in the tails the small one keeps its (possibly subnormal) value instead of
-// collapsing to zero.
+// collapsing to zero.  For |y| < 86, exp(-|y|) = 2^(-|y| log2 e) >= 2^-124 is normal
+// and the special-function unit is accurate enough (a few binary32 units against the
+// bf16 rounding of every result); beyond, the accurate expf and IEEE reciprocal.
 __device__ __forceinline__ void sigmoid_pair(float y, float &sp, float &sm)
 {
-    const float t = expf(-fabsf(y));
-    const float big = __frcp_rn(1.0f + t);
+    const float ay = fabsf(y);
+    float t, big;
+    if (ay < 86.0f) {
+        t = ex2_approx(ay * -1.44269504088896340736f);   // -log2(e)
+        big = rcp_approx(1.0f + t);
+    } else {
+        t = expf(-ay);
+        big = __frcp_rn(1.0f + t);
+    }
     const float small = t * big;
     sp = y >= 0.0f ? big : small;
     sm = y >= 0.0f ? small : big;

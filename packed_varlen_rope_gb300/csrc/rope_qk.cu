@@ -35,7 +35,7 @@
 namespace {
 
 constexpr int kThreads = 256;           // threads per CTA
-constexpr int kUnroll = 4;              // pair units in flight per thread (8 x 16 B loads)
+constexpr int kUnroll = 2;              // pair units in flight per thread (4 x 16 B loads; 48 registers, 5 CTAs per SM)
 constexpr int kMaxHalf = 128;           // head_dim <= 256
 constexpr int kMaxTileTokens = 32;      // one warp resolves the tile's positions
 constexpr int64_t kMaxTokens = int64_t(1) << 24;   // positions < 2^24 are exact in fp32
@@ -53,6 +53,7 @@ struct RopeArgs {
     int64_t qo_ts, qo_hs, ko_ts, ko_hs;      // output strides
     const int32_t *cu;
     const int32_t *pos_ids;                  // optional per-row positions (replaces cu)
+    const int32_t *seq_used;                 // optional tokens used per sample (with cu)
     const float4 *cache;
     int32_t n_seqs;
     int32_t n_tokens;
@@ -71,10 +72,12 @@ struct RopeArgs {
 };
 
 // Position of token t: t - cu[s] for the last s in [0, n) with cu[s] <= t, or -1 when
-// t lies outside [cu[0], cu[n]).  The loop is bounded by log2(n) steps whatever cu
-// holds; a result that would not be a valid position (start < 0 or start > t, only
-// possible for a cu that is not non-decreasing) is reported as outside.
-__device__ __forceinline__ int token_position(const int32_t *__restrict__ cu, int n, int t)
+// t lies outside [cu[0], cu[n]) or, given seq_used, at or past seq_used[s] tokens into
+// its sample.  The loop is bounded by log2(n) steps whatever cu holds; a result that
+// would not be a valid position (start < 0 or start > t, only possible for a cu that is
+// not non-decreasing) is reported as outside.
+__device__ __forceinline__ int token_position(const int32_t *__restrict__ cu, int n, int t,
+                                              const int32_t *__restrict__ seq_used = nullptr)
 {
     if (n <= 0) return -1;
     const int first = __ldg(cu);
@@ -88,7 +91,9 @@ __device__ __forceinline__ int token_position(const int32_t *__restrict__ cu, in
     }
     const int start = __ldg(cu + lo);
     if (start < 0 || start > t) return -1;
-    return t - start;
+    const int pos = t - start;
+    if (seq_used != nullptr && pos >= __ldg(seq_used + lo)) return -1;
+    return pos;
 }
 
 // (cos phi, sin phi) with phi = RN32(pos * w): the angle is one binary32 multiply; the
@@ -188,7 +193,7 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
                 const int p = __ldg(a.pos_ids + r);
                 pos = (p >= 0 && p < static_cast<int>(kMaxTokens)) ? p : -1;
             } else {
-                pos = token_position(a.cu, a.n_seqs, a.token_offset + r);
+                pos = token_position(a.cu, a.n_seqs, a.token_offset + r, a.seq_used);
             }
         }
         s_pos[threadIdx.x] = pos;
@@ -478,6 +483,7 @@ int rope_qk_apply_impl(const rope_qk_desc *dp, void *stream)
     a.qo_ts = qo.ts; a.qo_hs = qo.hs; a.ko_ts = ko.ts; a.ko_hs = ko.hs;
     a.cu = p.cu_seqlens;
     a.pos_ids = p.position_ids;
+    a.seq_used = p.position_ids != nullptr ? nullptr : p.seq_used;
     a.cache = reinterpret_cast<const float4 *>(p.cos_sin_cache);
     a.n_seqs = p.position_ids != nullptr ? 0 : p.n_seqs;
     a.n_tokens = static_cast<int32_t>(T);

@@ -54,13 +54,13 @@ def test_library_exports_every_declared_symbol(lib):
 def test_header_is_plain_c(tmp_path):
     src = tmp_path / "use_header.c"
     src.write_text('#include "rope_qk.h"\n#include "glu.h"\n'
-                   'int main(void) { return ROPE_QK_ABI_VERSION == 2 && GLU_GEGLU_TANH == 2 ? 0 : 1; }\n')
+                   'int main(void) { return ROPE_QK_ABI_VERSION == 3 && GLU_GEGLU_TANH == 2 ? 0 : 1; }\n')
     subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Werror", "-pedantic", "-I", os.path.dirname(HEADER),
                            "-c", str(src), "-o", str(tmp_path / "use_header.o")])
 
 
 def test_abi_version_and_strerror(lib):
-    assert lib.rope_qk_abi_version() == 2
+    assert lib.rope_qk_abi_version() == 3
     for code in (OK, ERR_NULL, ERR_SHAPE, ERR_HEAD_DIM, ERR_ALIGN, ERR_OVERLAP, ERR_UNSUPPORTED,
                  ERR_LAUNCH, ERR_THETA, -9, -10):
         assert lib.rope_strerror(code)

@@ -268,3 +268,30 @@ def test_long_strided_fused_qkv(dev):
     for sl in (slice(0, hq), slice(hq, hq + hkv)):
         _check(after[:, sl], _expect(before[:, sl], pos, 1.0e6), before[:, sl], "long fused")
     assert np.array_equal(after[:, hq + hkv:], before[:, hq + hkv:])
+
+
+def test_seq_used_skips_padding(dev):
+    """Llama-3-8B shape padded to 8 x 2048 with uniform cu_seqlens and seq_used = the
+    samples' lengths: pad rows are not touched, valid rows equal the packed run."""
+    from packed_varlen_rope_gb300 import workloads as wl
+
+    w = wl.WORKLOADS[3]
+    padded, packed = wl.make_pack(w, "padded"), wl.make_pack(w, "packed")
+    T = padded.total_tokens
+    q = wl.normal_bf16((T, w.n_q_heads, w.head_dim), 31, device="cuda")
+    k = wl.normal_bf16((T, w.n_kv_heads, w.head_dim), 32, device="cuda")
+    q0, k0 = to_bits(q), to_bits(k)
+    used = torch.tensor(padded.lengths, dtype=torch.int32, device=dev)
+    pr().rope_qk_apply(q, k, w.theta, cu_seqlens=torch.from_numpy(padded.cu_seqlens).to(dev), seq_used=used)
+    torch.cuda.synchronize()
+    valid = padded.valid_mask
+    pos = np.where(valid, oracle.positions(padded.cu_seqlens, T), -1).astype(np.int32)
+    _check(to_bits(q), _expect(q0, pos, w.theta), q0, "seq_used q")
+    _check(to_bits(k), _expect(k0, pos, w.theta), k0, "seq_used k")
+    assert np.array_equal(to_bits(q)[~valid], q0[~valid])
+    # the valid rows are the packed run's rows
+    qp, kp = torch.from_numpy(q0[valid].view(np.int16)).view(torch.bfloat16).to(dev), \
+        torch.from_numpy(k0[valid].view(np.int16)).view(torch.bfloat16).to(dev)
+    pr().rope_qk_fwd(qp, kp, torch.from_numpy(packed.cu_seqlens).to(dev), w.theta)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_bits(qp), to_bits(q)[valid])

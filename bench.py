@@ -49,7 +49,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=4)
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target seconds of oracle work for the CPU baseline sample")
     ap.add_argument("--no-e2e", action="store_true")
@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--path", choices=["rope", "glu"], default="rope",
                     help="rope: the QK-RoPE step (default); glu: SwiGLU/GeGLU forward+backward")
     ap.add_argument("--glu-workload", default="qwen3-4b-mlp-1m")
+    ap.add_argument("--glu-kind", choices=["swiglu", "geglu", "geglu_tanh"], default=None,
+                    help="activation (default: the workload's)")
     return ap.parse_args()
 
 
@@ -258,10 +260,9 @@ def cpu_baseline(args, w, pack, q_sample, k_sample, dq_sample, dk_sample):
 
     def run(n):
         p = pos[:n]
-        oracle.rope_rows(q_sample[:n], p, w.theta)
-        oracle.rope_rows(k_sample[:n], p, w.theta)
-        oracle.rope_rows(dq_sample[:n], p, w.theta, bwd=True)
-        oracle.rope_rows(dk_sample[:n], p, w.theta, bwd=True)
+        return (oracle.rope_rows(q_sample[:n], p, w.theta), oracle.rope_rows(k_sample[:n], p, w.theta),
+                oracle.rope_rows(dq_sample[:n], p, w.theta, bwd=True),
+                oracle.rope_rows(dk_sample[:n], p, w.theta, bwd=True))
 
     cal = min(256, n_all)
     t = time.perf_counter()
@@ -269,11 +270,33 @@ def cpu_baseline(args, w, pack, q_sample, k_sample, dq_sample, dk_sample):
     per_token = (time.perf_counter() - t) / cal
     n = int(max(cal, min(n_all, args.cpu_seconds / per_token)))
     t = time.perf_counter()
-    run(n)
+    outputs = run(n)
     el = time.perf_counter() - t
     return {"value": n / el, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": "first %d tokens of the %s pack, fwd+bwd of Q and K, %.1f s on one host core"
-                      % (n, w.name, el)}
+                      % (n, w.name, el)}, outputs
+
+
+def parity_block(gpu_outputs, oracle_outputs, inputs):
+    """Element-by-element comparison of the timed launch configuration's results with
+    the oracle on the CPU-baseline sample: counts of differing bf16 elements and the
+    largest difference in bf16 units in the last place."""
+    import numpy as np
+
+    n_el = mism = 0
+    max_ulp = 0
+    for got, ref, x in zip(gpu_outputs, oracle_outputs, inputs):
+        g = got[: ref.shape[0]]
+        n_el += g.size
+        diff = g != ref
+        mism += int(np.count_nonzero(diff))
+        if diff.any():
+            gi = g[diff].astype(np.int32)
+            ri = ref[diff].astype(np.int32)
+            to_ordered = lambda b: np.where(b & 0x8000, 0x8000 - (b & 0x7FFF), 0x8000 + b)  # noqa: E731
+            max_ulp = max(max_ulp, int(np.abs(to_ordered(gi) - to_ordered(ri)).max()))
+    return {"elements": n_el, "bit_mismatch": mism, "max_bf16_ulp": max_ulp,
+            "bar": "<= 2 bf16 ULP and <= 1e-2 (tests/parity_util.py); expected bit-identical"}
 
 
 # ---------------------------------------------------------------- our arm
@@ -308,10 +331,11 @@ def run_ours(args, rank, world, local):
 
     do_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
     samples = None
+    to_np = lambda t, n: t[:n].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)  # noqa: E731
     if do_cpu:
         n = min(T, 65536)
-        to_np = lambda t: t[:n].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)  # noqa: E731
-        samples = (to_np(q), to_np(k), to_np(dq), to_np(dk))
+        samples = tuple(to_np(t, n) for t in (q, k, dq, dk))
+        pristine = [t.clone() for t in (q, k, dq, dk)]      # for the parity check after timing
 
     bytes_per_pass = 4 * (w.n_q_heads + w.n_kv_heads) * w.head_dim * pack.valid_tokens
 
@@ -360,9 +384,16 @@ def run_ours(args, rank, world, local):
     if not args.no_e2e:
         e2e = end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev)
 
-    cpu = None
+    cpu = parity = None
     if do_cpu:
-        cpu = cpu_baseline(args, w, pack, *samples)
+        cpu, ref_outputs = cpu_baseline(args, w, pack, *samples)
+        pq, pk, pdq, pdk = pristine
+        pr.rope_qk_fwd(pq, pk, cu, w.theta, cos_sin_cache=cache)
+        pr.rope_qk_bwd(pdq, pdk, cu, w.theta, cos_sin_cache=cache)
+        torch.cuda.synchronize()
+        n = ref_outputs[0].shape[0]
+        parity = parity_block([to_np(t, n) for t in (pq, pk, pdq, pdk)], ref_outputs, samples)
+        del pristine, pq, pk, pdq, pdk
 
     if rank != 0:
         if world > 1:
@@ -395,6 +426,7 @@ def run_ours(args, rank, world, local):
         line["e2e"] = e2e
     if cpu is not None:
         line["cpu_baseline"] = cpu
+        line["parity"] = parity
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -458,6 +490,8 @@ def run_glu(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = wl.GLU_WORKLOADS[args.glu_workload]
+    if args.glu_kind is not None:
+        w = wl.GluWorkload(w.name, w.rows, w.cols, args.glu_kind, w.description)
     shape = (w.rows, w.cols)
     e = wl.normal_bf16(shape, 7001 + rank * wl.RANK_SEED_STRIDE, device=dev)
     g = wl.normal_bf16(shape, 7002 + rank * wl.RANK_SEED_STRIDE, device=dev)

@@ -34,7 +34,7 @@
 
 namespace {
 
-constexpr int kThreads = 256;           // threads per CTA
+constexpr int kThreads = 128;           // threads per CTA (10 CTAs per SM at 48 registers)
 constexpr int kUnroll = 2;              // pair units in flight per thread (4 x 16 B loads; 48 registers, 5 CTAs per SM)
 constexpr int kMaxHalf = 128;           // head_dim <= 256
 constexpr int kMaxTileTokens = 32;      // one warp resolves the tile's positions

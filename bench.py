@@ -80,13 +80,21 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and with whitespace collapsed."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash() -> str:
     """sha256 of the RoPE kernel's device code: rope_qk.cu up to its host-side section,
-    then fastdiv.cuh.  Host-only edits (argument checks, error strings) keep it."""
+    then fastdiv.cuh, comments and whitespace left out.  Host-only edits (argument
+    checks, error strings) and comment edits keep it."""
     text = open(KERNEL_SOURCE).read()
     device_part = text.split("// ------------------------------------------------------------------ host side")[0]
-    h = hashlib.sha256(device_part.encode())
-    h.update(open(os.path.join(os.path.dirname(KERNEL_SOURCE), "fastdiv.cuh")).read().encode())
+    h = hashlib.sha256(_code_only(device_part).encode())
+    h.update(_code_only(open(os.path.join(os.path.dirname(KERNEL_SOURCE), "fastdiv.cuh")).read()).encode())
     return h.hexdigest()
 
 

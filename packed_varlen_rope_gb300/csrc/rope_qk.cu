@@ -35,7 +35,7 @@
 namespace {
 
 constexpr int kThreads = 128;           // threads per CTA (10 CTAs per SM at 48 registers)
-constexpr int kUnroll = 2;              // pair units in flight per thread (4 x 16 B loads; 48 registers, 5 CTAs per SM)
+constexpr int kUnroll = 2;              // pair units in flight per thread (4 x 16-byte loads)
 constexpr int kMaxHalf = 128;           // head_dim <= 256
 constexpr int kMaxTileTokens = 32;      // one warp resolves the tile's positions
 constexpr int64_t kMaxTokens = int64_t(1) << 24;   // positions < 2^24 are exact in fp32
@@ -226,7 +226,7 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
     }
     __syncthreads();
 
-    // 3. stream the tile: load a batch of units (kUnroll per thread, 8 loads of 16 B in
+    // 3. stream the tile: load a batch of units (kUnroll per thread, 4 loads of 16 B in
     //    flight), rotate, store.  Rows of tokens outside the pack are not touched in
     //    place and are copied unchanged out of place.
     for (uint32_t base = threadIdx.x; base < units; base += kUnroll * kThreads) {

@@ -18,11 +18,14 @@
  * width the TRL page uses).
  *
  * Arithmetic.  bf16 inputs are widened exactly; act and act' are evaluated in binary32
- * with the accurate CUDA math functions (expf, erfcf) in forms without cancellation
- * (1 - sigmoid(x) = sigmoid(-x), Phi(x) = erfc(-x/sqrt2)/2, (1 + tanh u)/2 =
- * sigmoid(2u)); every result is rounded once to bf16 (nearest even).  Results agree
- * with a binary64 evaluation rounded once to bf16 within one bf16 unit in the last
- * place, plus a few binary32 units of the magnitude of the terms summed in act'.
+ * in forms without cancellation (1 - sigmoid(x) = sigmoid(-x), Phi(x) = erfc(-x/sqrt2)/2,
+ * (1 + tanh u)/2 = sigmoid(2u)).  Exponentials and reciprocals come from the
+ * special-function unit, and erfc from a fitted approximation (relative error < 4e-6
+ * for |x| < 6.4, < 2e-5 up to |x| = 12.5), wherever the results stay normal numbers;
+ * further out the accurate expf / erfcf.  Every result is rounded once to bf16 (nearest
+ * even).  Results agree with a binary64 evaluation rounded once to bf16 within one bf16
+ * unit in the last place, plus a few binary32 units of the magnitude of the terms
+ * summed in act'.
  *
  * Layout.  Each matrix is bf16 [rows][cols] with cols contiguous and a row stride in
  * elements (>= cols when rows > 1, a multiple of 8); cols is a multiple of 8; pointers

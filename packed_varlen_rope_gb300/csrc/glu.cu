@@ -81,6 +81,17 @@ __device__ __forceinline__ void sigmoid_pair(float y, float &sp, float &sm)
     sm = y >= 0.0f ? small : big;
 }
 
+// erfc(z) for 0 <= z < 8.84 as t * 2^((P(t) - z^2) log2 e), t = 1 / (1 + z/2): the form
+// of the Chebyshev-fitted erfc in Press et al., "Numerical Recipes", section 6.2, with a
+// degree-9 P fitted by csrc/fit_erfc.py (mpmath, |P - log(erfc(z)/t) - z^2| < 2e-7).
+// Evaluated in binary32 its relative error stays below 4e-6 for z <= 4.5 and 2e-5 up to
+// 8.84, where every intermediate is still a normal number.
+__device__ __constant__ float kErfcFit[10] = {
+    1.820451054e-01f, -8.726416530e-01f, 1.583596734e+00f, -1.231761465e+00f, 3.360064744e-01f,
+    -2.061395608e-01f, 1.006541982e-01f, 3.737148406e-01f, 1.000037772e+00f, -1.265512311e+00f,
+};
+constexpr float kLog2e = 1.44269504088896340736f;
+
 // act(x) and act'(x), in forms without cancellation in the tails.
 template <int KIND>
 __device__ __forceinline__ void activation(float x, float &a, float &da)
@@ -91,8 +102,23 @@ __device__ __forceinline__ void activation(float x, float &a, float &da)
         a = x * sp;
         da = sp * (1.0f + x * sm);
     } else if (KIND == GLU_GEGLU) {
-        const float Phi = 0.5f * erfcf(-x * kInvSqrt2);
-        const float phi = expf(-0.5f * x * x) * kInvSqrt2Pi;
+        // Phi(x) = erfc(-x/sqrt2)/2 and phi(x) = exp(-x^2/2)/sqrt(2 pi), with z = |x|/sqrt2
+        const float ax = fabsf(x);
+        float Phi, phi;
+        if (ax < 12.5f) {
+            const float z = ax * kInvSqrt2;
+            const float t = rcp_approx(1.0f + 0.5f * z);
+            float p = kErfcFit[0];
+#pragma unroll
+            for (int i = 1; i < 10; ++i) p = p * t + kErfcFit[i];
+            const float z2 = z * z;
+            const float half_erfc = 0.5f * t * ex2_approx((p - z2) * kLog2e);
+            Phi = x >= 0.0f ? 1.0f - half_erfc : half_erfc;
+            phi = ex2_approx(-z2 * kLog2e) * kInvSqrt2Pi;
+        } else {
+            Phi = 0.5f * erfcf(-x * kInvSqrt2);
+            phi = expf(-0.5f * x * x) * kInvSqrt2Pi;
+        }
         a = x * Phi;
         da = Phi + x * phi;
     } else {

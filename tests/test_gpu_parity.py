@@ -410,3 +410,30 @@ def test_autograd(dev):
     assert np.array_equal(to_bits(yq), oracle.rope_packed(q0, pack.cu_seqlens, w.theta))
     assert np.array_equal(to_bits(qleaf.grad), oracle.rope_packed(g_q, pack.cu_seqlens, w.theta, bwd=True))
     assert np.array_equal(to_bits(kleaf.grad), oracle.rope_packed(g_k, pack.cu_seqlens, w.theta, bwd=True))
+
+
+def test_maximum_token_count(dev):
+    """The largest pack the library takes: 2^24 tokens, so positions run to 2^24 - 1 (the
+    last integer binary32 holds exactly) and the angles reach their largest values.  A
+    small head shape keeps it to 1 GiB; sampled rows against the oracle, and one token
+    more is refused."""
+    T, hq, hkv, d = 1 << 24, 1, 1, 16
+    q = torch.empty((T, hq, d), dtype=torch.bfloat16, device=dev).normal_()
+    k = torch.empty((T, hkv, d), dtype=torch.bfloat16, device=dev).normal_()
+    rng = np.random.Generator(np.random.PCG64(50))
+    rows = np.unique(np.concatenate([rng.integers(0, T, 2000), [0, 1, T - 2, T - 1, (1 << 23), (1 << 23) + 1]]))
+    rows_dev = torch.from_numpy(rows).to(dev)
+    q0, k0 = to_bits(q[rows_dev]), to_bits(k[rows_dev])
+    cu_np = np.array([0, T], dtype=np.int32)
+    cu = torch.from_numpy(cu_np).to(dev)
+    _run("rope_qk_fwd", q, k, cu, 1.0e6)
+    pos = rows.astype(np.int32)
+    for x, y in ((q0, q), (k0, k)):
+        s = compare(to_bits(y[rows_dev]), oracle.rope_rows(x, pos, 1.0e6), x)
+        assert_parity(s, "max T")
+        assert s["bit_mismatch"] == 0, s
+    over = torch.empty((T + 1, hq, d), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(pr().RopeError) as err:
+        pr().rope_qk_fwd(over, torch.empty((T + 1, hkv, d), dtype=torch.bfloat16, device=dev),
+                         torch.tensor([0, T + 1], dtype=torch.int32, device=dev), 1.0e6)
+    assert err.value.status == -6

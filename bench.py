@@ -461,21 +461,24 @@ def end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev):
         pr.rope_qk_host(host[2], host[3], w.theta, ws, cu_seqlens=cu, cos_sin_cache=cache, backward=True,
                         q_out=work[2], k_out=work[3])
 
-    step()
+    for _ in range(2):
+        step()
     torch.cuda.synchronize()
     E = max(1, args.e2e_steps)
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(E + 1)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    s.record(stream)
-    for _ in range(E):
+    marks[0].record(stream)
+    for i in range(E):
         step()
-    e.record(stream)
+        marks[i + 1].record(stream)
     torch.cuda.synchronize()
-    ms = max_over_ranks(s.elapsed_time(e) / E, world, dev)
+    steps_ms = [marks[i].elapsed_time(marks[i + 1]) for i in range(E)]
+    ms = max_over_ranks(marks[0].elapsed_time(marks[E]) / E, world, dev)
     return {"value": whole_job_tokens_per_s(world, pack.valid_tokens, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": h2d, "ms_per_step": ms, "steps": E,
+            "step_ms_min": min(steps_ms), "step_ms_median": statistics.median(steps_ms),
             "path": "rope_qk_host: pinned host buffers streamed in %d-token chunks" % chunk}
 
 

@@ -5,7 +5,9 @@
 // in flight.  64-bit offsets are a compile-time specialisation used only when an
 // element offset of a matrix reaches 2^31 (unsloth.ai "3x faster training with
 // packing", section "Indexage int64 pour les kernels Triton"); the intermediate matrix
-// of 1,048,576 tokens x 9,728 (TRL "training beyond 1M tokens") needs it.
+// of 1,048,576 tokens x 9,728 (TRL "training beyond 1M tokens") needs it.  On the fast
+// path two elements go through each binary32 instruction (packed FFMA2/FMUL2/FADD2),
+// which halves the arithmetic that otherwise limits the erf form below HBM speed.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -156,6 +158,51 @@ __device__ __forceinline__ void activation(float x, float &a, float &da)
     }
 }
 
+// Packed binary32 pairs: __ffma2_rn / __fmul2_rn / __fadd2_rn (sm_100 and later) round
+// each component exactly like fmaf / a * b / a + b, in one instruction for both, so the
+// pair code below gives the scalar code's results bit for bit at half the issue cost.
+__device__ __forceinline__ float2 splat(float v) { return make_float2(v, v); }
+
+// Fast-path act and act' of two elements at once (MODE == kFast: the caller has checked
+// |x| < fast_limit<KIND>() for both).  The erf form runs the same operations as
+// activation<GLU_GEGLU, kFast>, and SiLU as sigmoid_pair<kFast> with a = x sp,
+// da = sp (1 + x sm); the tanh form evaluates each element with the scalar code.
+template <int KIND>
+__device__ __forceinline__ void activation_pair_fast(float2 x, float2 &a, float2 &da)
+{
+    if (KIND == GLU_GEGLU) {
+        const float2 ax = make_float2(fabsf(x.x), fabsf(x.y));
+        const float2 den = __ffma2_rn(ax, splat(kHalfInvSqrt2), splat(1.0f));
+        const float2 t = make_float2(rcp_approx(den.x), rcp_approx(den.y));
+        float2 p = splat(kErfcFit[0]);
+#pragma unroll
+        for (int i = 1; i < 10; ++i) p = __ffma2_rn(p, t, splat(kErfcFit[i]));
+        const float2 xx = __fmul2_rn(x, x);
+        const float2 arg = __ffma2_rn(p, splat(kLog2e), __ffma2_rn(splat(-0.5f * kLog2e), xx, splat(-1.0f)));
+        const float2 half_erfc = __fmul2_rn(t, make_float2(ex2_approx(arg.x), ex2_approx(arg.y)));
+        const float2 upper = __fadd2_rn(splat(1.0f), make_float2(-half_erfc.x, -half_erfc.y));
+        const float2 Phi = make_float2(x.x >= 0.0f ? upper.x : half_erfc.x, x.y >= 0.0f ? upper.y : half_erfc.y);
+        const float2 parg = __ffma2_rn(splat(-0.5f * kLog2e), xx, splat(kLog2InvSqrt2Pi));
+        const float2 phi = make_float2(ex2_approx(parg.x), ex2_approx(parg.y));
+        a = __fmul2_rn(x, Phi);
+        da = __ffma2_rn(x, phi, Phi);
+    } else if (KIND == GLU_SWIGLU) {
+        const float2 ay = make_float2(fabsf(x.x), fabsf(x.y));
+        const float2 targ = __fmul2_rn(ay, splat(-1.44269504088896340736f));
+        const float2 t = make_float2(ex2_approx(targ.x), ex2_approx(targ.y));
+        const float2 den = __fadd2_rn(splat(1.0f), t);
+        const float2 big = make_float2(rcp_approx(den.x), rcp_approx(den.y));
+        const float2 small = __fmul2_rn(t, big);
+        const float2 sp = make_float2(x.x >= 0.0f ? big.x : small.x, x.y >= 0.0f ? big.y : small.y);
+        const float2 sm = make_float2(x.x >= 0.0f ? small.x : big.x, x.y >= 0.0f ? small.y : big.y);
+        a = __fmul2_rn(x, sp);
+        da = __fmul2_rn(sp, __ffma2_rn(x, sm, splat(1.0f)));
+    } else {
+        activation<KIND, kFast>(x.x, a.x, da.x);
+        activation<KIND, kFast>(x.y, a.y, da.y);
+    }
+}
+
 __device__ __forceinline__ uint4 load_stream(const __nv_bfloat16 *p)
 {
     return __ldcs(reinterpret_cast<const uint4 *>(p));
@@ -206,30 +253,44 @@ __device__ __forceinline__ void glu_unit(const float2 (&x)[4], const uint32_t *w
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
         const float2 gg = unpack(wg[w]);
-        float a0, d0, a1, d1;
-        if (MODE != kCareful) {
-            activation<KIND, MODE>(x[w].x, a0, d0);
-            activation<KIND, MODE>(x[w].y, a1, d1);
+        float2 av, dv;
+        if (MODE == kFast) {
+            activation_pair_fast<KIND>(x[w], av, dv);
+        } else if (MODE == kGuarded) {
+            activation<KIND, MODE>(x[w].x, av.x, dv.x);
+            activation<KIND, MODE>(x[w].y, av.y, dv.y);
         } else {
             const float2 r0 = activation_careful<KIND>(x[w].x);
             const float2 r1 = activation_careful<KIND>(x[w].y);
-            a0 = r0.x;
-            d0 = r0.y;
-            a1 = r1.x;
-            d1 = r1.y;
+            av = make_float2(r0.x, r1.x);
+            dv = make_float2(r0.y, r1.y);
         }
         if (!BWD) {
-            p0[w] = pack(a0 * gg.x, a1 * gg.y);
+            const float2 h = __fmul2_rn(av, gg);
+            p0[w] = pack(h.x, h.y);
         } else {
             const float2 dh = unpack(wd[w]);
-            p0[w] = pack(dh.x * gg.x * d0, dh.y * gg.y * d1);   // de
-            p1[w] = pack(dh.x * a0, dh.y * a1);                 // dg
+            const float2 de = __fmul2_rn(__fmul2_rn(dh, gg), dv);
+            const float2 dg = __fmul2_rn(dh, av);
+            p0[w] = pack(de.x, de.y);
+            p1[w] = pack(dg.x, dg.y);
         }
     }
 }
 
+// Blocks per SM the register allocation must leave room for, as measured on 65,536 x
+// 9,728: 4 for the forward kernels (at most 64 registers; without the bound the erf
+// form takes 74 and runs at 0.94 of the copy rate instead of 1.01), 3 for the erf-form
+// backward (at most 80 registers; 0.91 -> 1.03), and 0 (no bound, the compiler's own
+// allocation) for the other backward kernels, which lose 1-2 % under a bound.
+template <int KIND, bool BWD>
+__host__ __device__ constexpr int kMinBlocks()
+{
+    return !BWD ? 4 : (KIND == GLU_GEGLU ? 3 : 0);
+}
+
 template <int KIND, bool LONG, bool BWD>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, (kMinBlocks<KIND, BWD>()))
 glu_kernel(const __grid_constant__ GluArgs a)
 {
     using Index = typename std::conditional<LONG, int64_t, uint32_t>::type;

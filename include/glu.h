@@ -11,11 +11,10 @@
  *
  * elementwise over rows x cols bf16 matrices, act = SiLU (SwiGLU) or GELU (GeGLU, the
  * exact erf form or the tanh form).  The unsloth.ai page "3x faster training with
- * packing" lists these kernels as updated with int64 indexing for long contexts, and
- * its section "Indexage int64 pour les kernels Triton" makes the 64-bit offsets a
- * compile-time specialisation taken only when needed: here, when an element offset of
- * one of the matrices reaches 2^31 (e.g. 1,048,576 tokens x 9,728, the intermediate
- * width the TRL page uses).
+ * packing" lists these kernels as updated with int64 indexing for long contexts
+ * (section "Indexage int64 pour les kernels Triton"): a matrix may span more than 2^31
+ * elements (1,048,576 tokens x 9,728, the intermediate width the TRL page uses, spans
+ * 1.0e10), and every address is formed in 64 bits.
  *
  * Arithmetic.  bf16 inputs are widened exactly; act and act' are evaluated in binary32
  * in forms without cancellation (1 - sigmoid(x) = sigmoid(-x), Phi(x) = erfc(-x/sqrt2)/2,
@@ -28,8 +27,8 @@
  * summed in act'.
  *
  * Layout.  Each matrix is bf16 [rows][cols] with cols contiguous and a row stride in
- * elements (>= cols when rows > 1, a multiple of 8); cols is a multiple of 8; pointers
- * are 16-byte aligned; rows * cols / 8 < 2^31.  The gate and up halves of one fused
+ * elements (a multiple of 8; when rows > 1, at least cols and below cols + 2^31); cols
+ * is a multiple of 8; pointers are 16-byte aligned; rows * cols / 8 < 2^31.  The gate and up halves of one fused
  * [rows, 2*I] projection output are views with row stride 2*I.
  *
  * Aliasing.  An output may be exactly one of the inputs (same pointer and stride): it
@@ -62,7 +61,8 @@ typedef enum glu_kind {
 
 /* Forward: h = act(e) * g.  Strides in elements.  Returns ROPE_ERR_KIND for an unknown
  * kind, ROPE_ERR_SHAPE for negative sizes, cols not a multiple of 8, a row stride below
- * cols or rows * cols / 8 >= 2^31, ROPE_ERR_ALIGN, ROPE_ERR_NULL, ROPE_ERR_OVERLAP. */
+ * cols or at least cols + 2^31 (rows > 1), or rows * cols / 8 >= 2^31, ROPE_ERR_ALIGN,
+ * ROPE_ERR_NULL, ROPE_ERR_OVERLAP. */
 int glu_fwd(int32_t kind, const void *e, int64_t e_stride, const void *g, int64_t g_stride,
             void *h, int64_t h_stride, int64_t rows, int64_t cols, void *stream);
 

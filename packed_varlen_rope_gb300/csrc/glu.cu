@@ -2,10 +2,14 @@
 //
 // Elementwise and HBM-bound (forward 6 bytes per element, backward 10): each thread owns
 // units of 8 consecutive elements of a row (16-byte loads and stores) and keeps 4 units
-// in flight.  64-bit offsets are a compile-time specialisation used only when an
-// element offset of a matrix reaches 2^31 (unsloth.ai "3x faster training with
-// packing", section "Indexage int64 pour les kernels Triton"); the intermediate matrix
-// of 1,048,576 tokens x 9,728 (TRL "training beyond 1M tokens") needs it.  On the fast
+// in flight.  Matrices may span more than 2^31 elements (1,048,576 tokens x 9,728, the
+// intermediate matrix of TRL "training beyond 1M tokens"), so addresses are 64-bit; the
+// source page (unsloth.ai "3x faster training with packing", section "Indexage int64
+// pour les kernels Triton") makes int64 indexing a compile-time specialisation because
+// 64-bit index arithmetic costs more.  Here every address is base + 16 u + row * pad
+// (u the unit index, pad the bytes a row stride adds beyond the row): two 32 x 32 -> 64
+// bit multiply-adds, as cheap as 32-bit offsets, so one code path serves every size,
+// and matrices whose rows are back to back (pad 0) skip the row division.  On the fast
 // path two elements go through each binary32 instruction (packed FFMA2/FMUL2/FADD2),
 // which halves the arithmetic that otherwise limits the erf form below HBM speed.
 
@@ -38,11 +42,22 @@ struct GluArgs {
     const __nv_bfloat16 *g;
     __nv_bfloat16 *out0;      // h (forward) or de (backward)
     __nv_bfloat16 *out1;      // dg (backward)
-    int64_t s_dh, s_e, s_g, s_out0, s_out1;
+    // bytes a row stride adds beyond the row, (stride - cols) * 2, per matrix (0 when
+    // the rows are back to back or there is one row)
+    uint32_t pad_dh, pad_e, pad_g, pad_out0, pad_out1;
     uint32_t units;           // rows * cols / 8
     uint32_t cols8;
     FastDiv div_cols8;
 };
+
+// Address of unit u (row `row`) of a matrix: base + 16 u + row * pad, in 64 bits.
+template <typename T>
+__device__ __forceinline__ T *unit_ptr(T *base, uint32_t u, uint32_t row, uint32_t pad)
+{
+    using Byte = typename std::conditional<std::is_const<T>::value, const char, char>::type;
+    return reinterpret_cast<T *>(reinterpret_cast<Byte *>(base) + (static_cast<uint64_t>(u) * 16u +
+                                                                   static_cast<uint64_t>(row) * pad));
+}
 
 // 2^x and 1/x from the special-function unit (PTX ex2.approx / rcp.approx, a few units
 // in the last binary32 place; they flush subnormal results, so they are used only where
@@ -289,28 +304,25 @@ __host__ __device__ constexpr int kMinBlocks()
     return !BWD ? 4 : (KIND == GLU_GEGLU ? 3 : 0);
 }
 
-template <int KIND, bool LONG, bool BWD>
+// PADDED: some matrix has a row stride wider than its rows, so each unit's row is
+// needed (a division by cols / 8); otherwise every matrix is one run of units.
+template <int KIND, bool PADDED, bool BWD>
 __global__ void __launch_bounds__(kThreads, (kMinBlocks<KIND, BWD>()))
 glu_kernel(const __grid_constant__ GluArgs a)
 {
-    using Index = typename std::conditional<LONG, int64_t, uint32_t>::type;
     const uint32_t base = blockIdx.x * static_cast<uint32_t>(kUnroll * kThreads) + threadIdx.x;
     uint4 ve[kUnroll], vg[kUnroll], vd[kUnroll];
-    Index row[kUnroll], col[kUnroll];
+    uint32_t row[kUnroll];
     bool live[kUnroll];
 #pragma unroll
     for (int k = 0; k < kUnroll; ++k) {
         const uint32_t u = base + k * kThreads;
         live[k] = u < a.units;
-        row[k] = 0;
-        col[k] = 0;
+        row[k] = PADDED ? fast_div(u, a.div_cols8) : 0u;
         if (live[k]) {
-            const uint32_t r = fast_div(u, a.div_cols8);
-            row[k] = static_cast<Index>(r);
-            col[k] = static_cast<Index>((u - r * a.cols8) * 8u);
-            ve[k] = load_stream(a.e + (row[k] * static_cast<Index>(a.s_e) + col[k]));
-            vg[k] = load_stream(a.g + (row[k] * static_cast<Index>(a.s_g) + col[k]));
-            if (BWD) vd[k] = load_stream(a.dh + (row[k] * static_cast<Index>(a.s_dh) + col[k]));
+            ve[k] = load_stream(unit_ptr(a.e, u, row[k], a.pad_e));
+            vg[k] = load_stream(unit_ptr(a.g, u, row[k], a.pad_g));
+            if (BWD) vd[k] = load_stream(unit_ptr(a.dh, u, row[k], a.pad_dh));
         }
     }
 #pragma unroll
@@ -349,8 +361,9 @@ glu_kernel(const __grid_constant__ GluArgs a)
                 }
             }
         }
-        store_stream(a.out0 + (row[k] * static_cast<Index>(a.s_out0) + col[k]), o0);
-        if (BWD) store_stream(a.out1 + (row[k] * static_cast<Index>(a.s_out1) + col[k]), o1);
+        const uint32_t u = base + k * kThreads;
+        store_stream(unit_ptr(a.out0, u, row[k], a.pad_out0), o0);
+        if (BWD) store_stream(unit_ptr(a.out1, u, row[k], a.pad_out1), o1);
     }
 }
 
@@ -402,33 +415,34 @@ int check_mats(const Mat *m, int n, int64_t rows, int64_t cols)
     for (int i = 0; i < n; ++i) {
         if (m[i].p == nullptr) return ROPE_ERR_NULL;
         if (!aligned16(m[i].p) || m[i].stride % 8 != 0) return ROPE_ERR_ALIGN;
-        if (rows > 1 && m[i].stride < cols) return ROPE_ERR_SHAPE;
+        if (rows > 1 && (m[i].stride < cols || m[i].stride - cols >= (int64_t(1) << 31))) return ROPE_ERR_SHAPE;
     }
     return ROPE_OK;
 }
 
-template <int KIND, bool LONG, bool BWD>
+template <int KIND, bool PADDED, bool BWD>
 cudaError_t launch(const GluArgs &a, cudaStream_t s)
 {
     const uint32_t per_block = kUnroll * kThreads;
     const uint32_t grid = (a.units + per_block - 1) / per_block;
-    glu_kernel<KIND, LONG, BWD><<<grid, kThreads, 0, s>>>(a);
+    glu_kernel<KIND, PADDED, BWD><<<grid, kThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
 template <bool BWD>
-int run(int32_t kind, const GluArgs &a, bool long_index, cudaStream_t s)
+int run(int32_t kind, const GluArgs &a, cudaStream_t s)
 {
+    const bool padded = (a.pad_dh | a.pad_e | a.pad_g | a.pad_out0 | a.pad_out1) != 0;
     cudaError_t err;
     switch (kind) {
     case GLU_SWIGLU:
-        err = long_index ? launch<GLU_SWIGLU, true, BWD>(a, s) : launch<GLU_SWIGLU, false, BWD>(a, s);
+        err = padded ? launch<GLU_SWIGLU, true, BWD>(a, s) : launch<GLU_SWIGLU, false, BWD>(a, s);
         break;
     case GLU_GEGLU:
-        err = long_index ? launch<GLU_GEGLU, true, BWD>(a, s) : launch<GLU_GEGLU, false, BWD>(a, s);
+        err = padded ? launch<GLU_GEGLU, true, BWD>(a, s) : launch<GLU_GEGLU, false, BWD>(a, s);
         break;
     default:
-        err = long_index ? launch<GLU_GEGLU_TANH, true, BWD>(a, s) : launch<GLU_GEGLU_TANH, false, BWD>(a, s);
+        err = padded ? launch<GLU_GEGLU_TANH, true, BWD>(a, s) : launch<GLU_GEGLU_TANH, false, BWD>(a, s);
         break;
     }
     return err == cudaSuccess ? ROPE_OK : ROPE_ERR_LAUNCH;
@@ -446,11 +460,10 @@ int prepare(int32_t kind, int64_t rows, int64_t cols, GluArgs &a)
     return ROPE_OK;
 }
 
-bool needs_long(const Mat *m, int n, int64_t rows, int64_t cols)
+// Bytes a row stride adds beyond the row (check_mats has bounded it below 2^32).
+uint32_t pad_bytes(const Mat &m, int64_t rows, int64_t cols)
 {
-    for (int i = 0; i < n; ++i)
-        if ((rows - 1) * m[i].stride + cols > INT32_MAX) return true;
-    return false;
+    return rows > 1 ? static_cast<uint32_t>((m.stride - cols) * 2) : 0u;
 }
 
 }  // namespace
@@ -472,11 +485,10 @@ int glu_fwd(int32_t kind, const void *e, int64_t e_stride, const void *g, int64_
     a.e = static_cast<const __nv_bfloat16 *>(e);
     a.g = static_cast<const __nv_bfloat16 *>(g);
     a.out0 = static_cast<__nv_bfloat16 *>(h);
-    a.s_e = e_stride;
-    a.s_g = g_stride;
-    a.s_out0 = h_stride;
-    const Mat all[3] = {in[0], in[1], out};
-    return run<false>(kind, a, needs_long(all, 3, rows, cols), static_cast<cudaStream_t>(stream));
+    a.pad_e = pad_bytes(in[0], rows, cols);
+    a.pad_g = pad_bytes(in[1], rows, cols);
+    a.pad_out0 = pad_bytes(out, rows, cols);
+    return run<false>(kind, a, static_cast<cudaStream_t>(stream));
 }
 
 int glu_bwd(int32_t kind, const void *dh, int64_t dh_stride, const void *e, int64_t e_stride,
@@ -499,13 +511,12 @@ int glu_bwd(int32_t kind, const void *dh, int64_t dh_stride, const void *e, int6
     a.g = static_cast<const __nv_bfloat16 *>(g);
     a.out0 = static_cast<__nv_bfloat16 *>(de);
     a.out1 = static_cast<__nv_bfloat16 *>(dg);
-    a.s_dh = dh_stride;
-    a.s_e = e_stride;
-    a.s_g = g_stride;
-    a.s_out0 = de_stride;
-    a.s_out1 = dg_stride;
-    const Mat all[5] = {in[0], in[1], in[2], out[0], out[1]};
-    return run<true>(kind, a, needs_long(all, 5, rows, cols), static_cast<cudaStream_t>(stream));
+    a.pad_dh = pad_bytes(in[0], rows, cols);
+    a.pad_e = pad_bytes(in[1], rows, cols);
+    a.pad_g = pad_bytes(in[2], rows, cols);
+    a.pad_out0 = pad_bytes(out[0], rows, cols);
+    a.pad_out1 = pad_bytes(out[1], rows, cols);
+    return run<true>(kind, a, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

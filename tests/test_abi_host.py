@@ -216,6 +216,8 @@ def test_glu_argument_checks(lib):
     assert f(kind=3) == ERR_KIND and f(kind=-1) == ERR_KIND
     assert f(rows=-1) == ERR_SHAPE and f(cols=12) == ERR_SHAPE and f(es=32) == ERR_SHAPE
     assert f(rows=1 << 20, cols=1 << 14) == ERR_SHAPE                      # units >= 2^31
+    assert f(es=64 + (1 << 31)) == ERR_SHAPE                               # stride - cols >= 2^31
+    assert f(es=64 + (1 << 31), rows=1) != ERR_SHAPE                       # one row: stride unused
     assert f(e=None) == ERR_NULL and f(h=None) == ERR_NULL
     assert f(e=E + 8) == ERR_ALIGN and f(gs=68) == ERR_ALIGN
     assert f(h=E + 64) == ERR_OVERLAP                                      # partial overlap

@@ -153,9 +153,34 @@ def test_glu_special_values(dev):
         _fwd_bwd_check(kind, eb, gb, dhb, h, de, dg, (kind, "special"))
 
 
+def test_glu_wide_row_stride(dev):
+    """gate, up and h side by side in one buffer whose row stride is 2^30 elements, so
+    row 1 starts 2 GiB after row 0 and the row term of every address passes 2^31 bytes;
+    the gaps between rows keep their canary values."""
+    cols, stride, rows = 64, 1 << 30, 3
+    n = (rows - 1) * stride + 3 * cols
+    store = torch.full((n,), 6.5, dtype=torch.bfloat16, device=dev)
+    view = lambda c: store.as_strided((rows, cols), (stride, 1), c * cols)  # noqa: E731
+    rng = np.random.Generator(np.random.PCG64(26))
+    eb, gb, dhb = (_bits(rng, (rows, cols), 2.0) for _ in range(3))
+    e, g, h = view(0), view(1), view(2)
+    e.copy_(from_bits(eb, dev))
+    g.copy_(from_bits(gb, dev))
+    for kind in KINDS:
+        pr().glu_fwd(kind, e, g, h)
+        torch.cuda.synchronize()
+        _fwd_bwd_check(kind, eb, gb, dhb, h.clone(), None, None, (kind, "wide stride"))
+    dh = from_bits(dhb, dev)
+    pr().glu_bwd("geglu", dh, e, g, de=e, dg=g)
+    torch.cuda.synchronize()
+    _fwd_bwd_check("geglu", eb, gb, dhb, None, e.clone(), g.clone(), "wide stride bwd")
+    gap = store[3 * cols:stride]
+    assert torch.all(gap == 6.5) and torch.all(store[stride + 3 * cols:2 * stride] == 6.5)
+
+
 def test_glu_long_1m_by_9728(dev):
     """1,048,576 tokens x 9,728 (the TRL page's MLP width at 1M tokens): every matrix
-    spans 10.2e9 elements, so the 64-bit-offset kernels run.  Sampled rows, including
+    spans 10.2e9 elements, so addresses pass 2^32 and 2^33 bytes.  Sampled rows, including
     those around element offset 2^31 and 2^32, against the oracle; canaries after the
     last element survive; the backward runs in place (de over e, dg over g)."""
     from packed_varlen_rope_gb300 import workloads as wl

@@ -282,7 +282,43 @@ def cpu_baseline(args, w, pack, q_sample, k_sample, dq_sample, dk_sample):
     el = time.perf_counter() - t
     return {"value": n / el, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": "first %d tokens of the %s pack, fwd+bwd of Q and K, %.1f s on one host core"
-                      % (n, w.name, el)}, outputs
+                      % (n, w.name, el)}, outputs, cpu_all_cores(w, pos[:n], q_sample[:n], k_sample[:n],
+                                                                  dq_sample[:n], dk_sample[:n])
+
+
+def cpu_all_cores(w, pos, q, k, dq, dk, seconds=2.0):
+    """The same oracle calls split into equal token ranges, one per host core the
+    process may run on (the C calls release the GIL), repeated for about `seconds`."""
+    import concurrent.futures as cf
+
+    import numpy as np
+
+    import oracle
+
+    cores = len(os.sched_getaffinity(0))
+    n = q.shape[0]
+    bounds = np.linspace(0, n, cores + 1).astype(np.int64)
+
+    def part(i):
+        lo, hi = bounds[i], bounds[i + 1]
+        p = pos[lo:hi]
+        oracle.rope_rows(q[lo:hi], p, w.theta)
+        oracle.rope_rows(k[lo:hi], p, w.theta)
+        oracle.rope_rows(dq[lo:hi], p, w.theta, bwd=True)
+        oracle.rope_rows(dk[lo:hi], p, w.theta, bwd=True)
+
+    reps = 0
+    with cf.ThreadPoolExecutor(cores) as ex:
+        t = time.perf_counter()
+        while True:
+            list(ex.map(part, range(cores)))
+            reps += 1
+            el = time.perf_counter() - t
+            if el >= seconds:
+                break
+    return {"value": reps * n / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "first %d tokens of the %s pack in %d token ranges on %d threads, %d passes in %.1f s"
+                      % (n, w.name, cores, cores, reps, el)}
 
 
 def parity_block(gpu_outputs, oracle_outputs, inputs):
@@ -394,7 +430,7 @@ def run_ours(args, rank, world, local):
 
     cpu = parity = None
     if do_cpu:
-        cpu, ref_outputs = cpu_baseline(args, w, pack, *samples)
+        cpu, ref_outputs, cpu_all = cpu_baseline(args, w, pack, *samples)
         pq, pk, pdq, pdk = pristine
         pr.rope_qk_fwd(pq, pk, cu, w.theta, cos_sin_cache=cache)
         pr.rope_qk_bwd(pdq, pdk, cu, w.theta, cos_sin_cache=cache)
@@ -434,6 +470,7 @@ def run_ours(args, rank, world, local):
         line["e2e"] = e2e
     if cpu is not None:
         line["cpu_baseline"] = cpu
+        line["cpu_baseline_all_cores"] = cpu_all
         line["parity"] = parity
     print(json.dumps(line), flush=True)
     if world > 1:

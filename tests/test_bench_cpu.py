@@ -26,3 +26,21 @@ def test_committed_profile_matches_kernel():
 
 def test_whole_job_value_is_weak_scaling():
     assert bench.whole_job_tokens_per_s(4, 65536, 1.0) == 4 * 65536 / 1e-3
+
+
+def test_all_core_oracle_timing_runs_every_range():
+    """The all-core CPU figure splits the token sample into one range per core and
+    rotates all of it (tiny workload, short repeat window)."""
+    import oracle
+    from packed_varlen_rope_gb300 import workloads as wl
+
+    oracle.build()
+    w = wl.WORKLOADS[1]
+    pack = wl.make_pack(w)
+    rng = np.random.Generator(np.random.PCG64(0))
+    q, k, dq, dk = (rng.integers(0, 1 << 16, size=(pack.total_tokens, h, w.head_dim), dtype=np.uint16) & 0x3FFF
+                    for h in (w.n_q_heads, w.n_kv_heads, w.n_q_heads, w.n_kv_heads))
+    pos = oracle.positions(pack.cu_seqlens, pack.total_tokens)
+    r = bench.cpu_all_cores(w, pos, q, k, dq, dk, seconds=0.05)
+    assert r["cores"] >= 1 and r["value"] > 0 and r["kind"] == "oracle"
+    assert "%d token ranges" % r["cores"] in r["sample"]

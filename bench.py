@@ -54,7 +54,7 @@ def parse_args():
                     help="target seconds of oracle work for the CPU baseline sample")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", choices=["rope", "glu"], default="rope",
+    ap.add_argument("--path", choices=["rope", "glu", "rope-forms"], default="rope",
                     help="rope: the QK-RoPE step (default); glu: SwiGLU/GeGLU forward+backward")
     ap.add_argument("--glu-workload", default="qwen3-4b-mlp-1m")
     ap.add_argument("--glu-kind", choices=["swiglu", "geglu", "geglu_tanh"], default=None,
@@ -602,6 +602,144 @@ def run_glu(args, rank, world, local):
     return 0
 
 
+def run_rope_forms(args, rank, world, local):
+    """The forward rotation of one workload through each input form of the C ABI: the
+    median time per launch (or per group of launches, for shards), algorithmic GB/s and
+    its fraction of the measured copy rate, and a check of the result -- bit-identical
+    to the contiguous path where the form computes the same thing, and against the
+    oracle on seeded sample tokens for the rescaled rotation."""
+    import numpy as np
+    import torch
+
+    from packed_varlen_rope_gb300 import build as _build
+
+    _build.build()
+    import packed_varlen_rope_gb300 as pr
+    from packed_varlen_rope_gb300 import workloads as wl
+
+    if rank != 0:
+        return 0
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = wl.WORKLOADS[args.workload]
+    pack = wl.make_pack(w)
+    T, Hq, Hkv, d = pack.total_tokens, w.n_q_heads, w.n_kv_heads, w.head_dim
+    q0 = wl.normal_bf16((T, Hq, d), wl.seed(w.index, "q"), device=dev)
+    k0 = wl.normal_bf16((T, Hkv, d), wl.seed(w.index, "k"), device=dev)
+    cu = torch.from_numpy(pack.cu_seqlens).to(dev)
+    rows = max(pack.lengths)
+    cache = pr.new_cos_sin_cache(rows, d, w.theta, device=dev)
+    q_ref, k_ref = q0.clone(), k0.clone()
+    pr.rope_qk_fwd(q_ref, k_ref, cu, w.theta, cos_sin_cache=cache)
+    nbytes = 4 * (Hq + Hkv) * d * pack.valid_tokens
+    peak, peak_kind = measured_peak()
+    bits = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)  # noqa: E731
+
+    def timed(fn, reps=50):
+        for _ in range(3):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        torch.cuda.synchronize()
+        for a, b in ev:
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ev) / 1e3
+
+    def same(q, k):
+        return "bit-identical to contiguous" if torch.equal(q, q_ref) and torch.equal(k, k_ref) else "MISMATCH"
+
+    forms = {}
+
+    def record(name, fn, check, launches=1):
+        sec = timed(fn)
+        forms[name] = {"us": sec * 1e6, "gbs": nbytes / sec / 1e9, "frac": nbytes / sec / 1e9 / peak,
+                       "launches": launches, "check": check}
+
+    # contiguous [T, H, d]
+    q, k = q0.clone(), k0.clone()
+    pr.rope_qk_fwd(q, k, cu, w.theta, cos_sin_cache=cache)
+    record("contiguous [T,H,d], rope_qk_fwd", lambda: pr.rope_qk_fwd(q, k, cu, w.theta, cos_sin_cache=cache),
+           same(q, k))
+    # Q and K slices of one fused [T, Hq + 2 Hkv, d] QKV output
+    qkv = torch.empty((T, Hq + 2 * Hkv, d), dtype=torch.bfloat16, device=dev)
+    qkv[:, :Hq].copy_(q0)
+    qkv[:, Hq:Hq + Hkv].copy_(k0)
+    qkv[:, Hq + Hkv:].fill_(1.5)
+    qs, ks = qkv[:, :Hq], qkv[:, Hq:Hq + Hkv]
+    pr.rope_qk_apply(qs, ks, w.theta, cu_seqlens=cu, cos_sin_cache=cache)
+    check = same(qs, ks) + ("" if torch.all(qkv[:, Hq + Hkv:] == 1.5) else ", V CHANGED")
+    record("fused QKV slices in place, rope_qk_apply",
+           lambda: pr.rope_qk_apply(qs, ks, w.theta, cu_seqlens=cu, cos_sin_cache=cache), check)
+    del qkv, qs, ks
+    # head-major [H, T, d] storage, passed as [T, H, d] views
+    qh = q0.transpose(0, 1).contiguous().transpose(0, 1)
+    kh = k0.transpose(0, 1).contiguous().transpose(0, 1)
+    pr.rope_qk_apply(qh, kh, w.theta, cu_seqlens=cu, cos_sin_cache=cache)
+    record("head-major [H,T,d] views, rope_qk_apply",
+           lambda: pr.rope_qk_apply(qh, kh, w.theta, cu_seqlens=cu, cos_sin_cache=cache), same(qh, kh))
+    del qh, kh
+    # out of place
+    q, k = q0.clone(), k0.clone()
+    qo, ko = torch.empty_like(q0), torch.empty_like(k0)
+    pr.rope_qk_apply(q, k, w.theta, cu_seqlens=cu, cos_sin_cache=cache, q_out=qo, k_out=ko)
+    check = same(qo, ko) + ("" if torch.equal(q, q0) and torch.equal(k, k0) else ", INPUT CHANGED")
+    record("out of place, rope_qk_apply",
+           lambda: pr.rope_qk_apply(q, k, w.theta, cu_seqlens=cu, cos_sin_cache=cache, q_out=qo, k_out=ko), check)
+    del qo, ko
+    # explicit position ids
+    pos = pr.rope_qk_positions(cu, T)
+    q, k = q0.clone(), k0.clone()
+    pr.rope_qk_apply(q, k, w.theta, position_ids=pos, cos_sin_cache=cache)
+    record("position_ids int32 [T], rope_qk_apply",
+           lambda: pr.rope_qk_apply(q, k, w.theta, position_ids=pos, cos_sin_cache=cache), same(q, k))
+    # context-parallel shards: 2 contiguous halves, and the load-balanced 2*cp chunks (cp = 2)
+    for name, bounds in (("2 contiguous CP shards (token_offset)", [(0, T // 2), (T // 2, T)]),
+                         ("cp=2 load-balanced chunks 0,3 | 1,2 (token_offset)",
+                          [(0, T // 4), (3 * T // 4, T), (T // 4, T // 2), (T // 2, 3 * T // 4)])):
+        q, k = q0.clone(), k0.clone()
+
+        def shards():
+            for a, b in bounds:
+                pr.rope_qk_apply(q[a:b], k[a:b], w.theta, cu_seqlens=cu, token_offset=a, cos_sin_cache=cache)
+
+        shards()
+        record(name, shards, same(q, k), launches=len(bounds))
+    # binary64 cos/sin on the fly (no cache)
+    q, k = q0.clone(), k0.clone()
+    pr.rope_qk_fwd(q, k, cu, w.theta)
+    record("no cos/sin cache (binary64 sincos per tile), rope_qk_fwd",
+           lambda: pr.rope_qk_fwd(q, k, cu, w.theta), same(q, k))
+    # linear position rescale, factor 4, with its own cache; oracle on sampled tokens
+    import oracle
+
+    oracle.build()
+    cache4 = pr.new_cos_sin_cache(rows, d, w.theta, device=dev, position_scale=4.0)
+    q, k = q0.clone(), k0.clone()
+    pr.rope_qk_apply(q, k, w.theta, cu_seqlens=cu, position_scale=4.0, cos_sin_cache=cache4)
+    pick = np.unique(np.random.Generator(np.random.PCG64(wl.seed(w.index, "rows"))).integers(0, T, 2048))
+    pick_dev = torch.from_numpy(pick).to(dev)
+    opos = oracle.positions(pack.cu_seqlens, T)[pick]
+    n_el = mism = 0
+    for got, src in ((q, q0), (k, k0)):
+        ref = oracle.rope_rows(bits(src[pick_dev]), opos, w.theta, scale=4.0)
+        g = bits(got[pick_dev])
+        n_el += g.size
+        mism += int(np.count_nonzero(g != ref))
+    record("position_scale 4 (scaled cache), rope_qk_apply",
+           lambda: pr.rope_qk_apply(q, k, w.theta, cu_seqlens=cu, position_scale=4.0, cos_sin_cache=cache4),
+           "oracle on %d sampled tokens: %d elements, %d differ" % (pick.size, n_el, mism))
+    line = {"metric": "QK-RoPE forward per input form", "unit": "GB/s", "workload": w.name,
+            "algorithmic_bytes_per_launch": nbytes, "peak": peak, "peak_kind": peak_kind + " (hbm_gbs)",
+            "timing": "median of 50 launches (CUDA events), inputs %.2f GB > L2" % (nbytes / 2e9),
+            "forms": forms}
+    print(json.dumps(line), flush=True)
+    bad = [n for n, f in forms.items() if "MISMATCH" in f["check"] or "CHANGED" in f["check"] or
+           not f["check"].endswith(" 0 differ") and f["check"].startswith("oracle")]
+    return 1 if bad else 0
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_env()
@@ -612,6 +750,8 @@ def main():
         return run_reference(args, rank, world)
     if args.path == "glu":
         return run_glu(args, rank, world, local)
+    if args.path == "rope-forms":
+        return run_rope_forms(args, rank, world, local)
     return run_ours(args, rank, world, local)
 
 

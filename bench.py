@@ -39,7 +39,7 @@ UNIT = "tokens/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCE = os.path.join(ROOT, "packed_varlen_rope_gb300", "csrc", "rope_qk.cu")
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "rope_qk_tile_kernel_qwen3-32b-64k.md")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "rope_qk_tile_kernel_%s.md")   # per workload name
 
 
 def parse_args():
@@ -98,11 +98,11 @@ def kernel_source_hash() -> str:
     return h.hexdigest()
 
 
-def profiled_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current kernel source; else None."""
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this workload, if there is
+    one and it was taken on the current kernel source; else None."""
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(PROFILE_SUMMARY % workload).read()
     except OSError:
         return None
     h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
@@ -459,7 +459,7 @@ def run_ours(args, rank, world, local):
         "hbm_frac_of_measured": 2 * bytes_per_pass / (ms_per_step / 1e3) / 1e9 / peak,
         "hbm_frac_of_nominal_8tbs": 2 * bytes_per_pass / (ms_per_step / 1e3) / 1e9 / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": profiled_traffic(),
+                     "frac": achieved / peak, "traffic": profiled_traffic(w.name),
                      "kernel": "rope_qk_tile_kernel<128,false>",
                      "algorithmic_bytes_per_launch": bytes_per_pass,
                      "avg_launch_us": avg_launch_s * 1e6, "peak_kind": peak_kind + " (hbm_gbs)"},

@@ -21,7 +21,8 @@ def test_kernel_hash_ignores_comments_and_spacing():
 
 def test_committed_profile_matches_kernel():
     """The traffic figure in profiles/ was taken on the kernel as it is now."""
-    assert bench.profiled_traffic() is not None
+    assert bench.profiled_traffic("qwen3-32b-64k") is not None
+    assert bench.profiled_traffic("qwen3-4b-16k") is None          # no capture of that workload
 
 
 def test_whole_job_value_is_weak_scaling():

@@ -1,0 +1,54 @@
+"""bench.py's measurement modes on small workloads (needs a GB300): each prints one
+JSON line with the keys its consumers read, and the self-checking forms mode finds
+every input form's result equal to the contiguous path's (or to the oracle)."""
+from __future__ import annotations
+
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench(*args, timeout=600):
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
+                       capture_output=True, text=True, timeout=timeout)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    return json.loads(lines[0])
+
+
+def test_rope_forms_on_qwen3_4b_16k():
+    d = _bench("--path", "rope-forms", "--workload", "2")
+    assert d["workload"] == "qwen3-4b-16k" and len(d["forms"]) == 9
+    for name, f in d["forms"].items():
+        assert f["us"] > 0 and f["gbs"] > 0, name
+        assert f["check"].startswith("bit-identical") or f["check"].endswith(" 0 differ"), (name, f["check"])
+
+
+def test_glu_bench_line_on_16k_slice():
+    d = _bench("--path", "glu", "--glu-workload", "qwen3-4b-mlp-16k", "--glu-kind", "geglu",
+               "--steps", "5", "--warmup", "3")
+    k = d["roofline"]["kernels"]
+    assert d["config"]["kind"] == "geglu" and d["gpu_launches"] == 10
+    assert k["glu_fwd"]["algorithmic_bytes_per_launch"] == 6 * 16384 * 9728
+    assert k["glu_bwd"]["algorithmic_bytes_per_launch"] == 10 * 16384 * 9728
+    assert 0 < k["glu_fwd"]["frac"] < 2 and 0 < k["glu_bwd"]["frac"] < 2
+
+
+def test_rope_bench_line_small():
+    d = _bench("--workload", "2", "--steps", "20", "--warmup", "3", "--e2e-steps", "2", "--cpu-seconds", "1")
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "roofline",
+                "cpu_baseline", "cpu_baseline_all_cores", "e2e", "clocks", "gpu_launches", "parity"):
+        assert key in d, key
+    assert d["parity"]["bit_mismatch"] == 0 and d["gpu_launches"] == 40
+    assert d["e2e"]["h2d_bytes_per_step"] == d["e2e"]["d2h_bytes_per_step"] > 0

@@ -203,7 +203,8 @@ int rope_qk_apply(const rope_qk_desc *desc, void *stream);
  *
  * `stream` runs the rotations and then waits for the last copy to the host: once it
  * reaches that point, the host outputs are complete.  The host buffers and the
- * workspace must stay untouched until then.  Enqueueing is serialised by a lock.
+ * workspace must stay untouched until then.  Enqueueing is serialised by a lock.  On an
+ * error return after copies were queued, `stream` is still ordered after all of them.
  */
 int rope_qk_host(const rope_qk_desc *desc, void *workspace, int64_t workspace_bytes, void *stream);
 

@@ -103,6 +103,13 @@ int rope_qk_host_impl(const rope_qk_desc *dp, void *workspace, int64_t workspace
     int rc = queues_for_current_device(&qs);
     if (rc != ROPE_OK) return rc;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // On an early return the caller's stream still waits for every copy already queued,
+    // so that freeing or reusing the workspace or the host buffers after the error is
+    // ordered after them.
+    auto join = [&]() {
+        if (cudaEventRecord(qs->loaded[0], qs->h2d) == cudaSuccess) cudaStreamWaitEvent(s, qs->loaded[0], 0);
+        if (cudaEventRecord(qs->drained[0], qs->d2h) == cudaSuccess) cudaStreamWaitEvent(s, qs->drained[0], 0);
+    };
     bool ok = cudaEventRecord(qs->entry, s) == cudaSuccess &&
               cudaStreamWaitEvent(qs->h2d, qs->entry, 0) == cudaSuccess &&
               cudaStreamWaitEvent(qs->d2h, qs->entry, 0) == cudaSuccess;
@@ -139,7 +146,10 @@ int rope_qk_host_impl(const rope_qk_desc *dp, void *workspace, int64_t workspace
         if (p.position_ids != nullptr) cd.position_ids = p.position_ids + t0;
         else cd.token_offset = p.token_offset + t0;
         rc = rope_qk_apply(&cd, stream);
-        if (rc != ROPE_OK) return rc;
+        if (rc != ROPE_OK) {
+            join();
+            return rc;
+        }
         ok = cudaEventRecord(qs->rotated[slot], s) == cudaSuccess;
         // 3. device -> host
         ok = ok && cudaStreamWaitEvent(qs->d2h, qs->rotated[slot], 0) == cudaSuccess;
@@ -150,6 +160,7 @@ int rope_qk_host_impl(const rope_qk_desc *dp, void *workspace, int64_t workspace
     // the caller's stream continues only after the last copies to the host
     for (int slot = 0; ok && slot < kSlots && slot < n_chunks; ++slot)
         ok = cudaStreamWaitEvent(s, qs->drained[slot], 0) == cudaSuccess;
+    if (!ok) join();
     return ok ? ROPE_OK : ROPE_ERR_LAUNCH;
 }
 

@@ -45,23 +45,25 @@ def _autograd_function():
         backward applies the transpose rotation to the incoming gradients."""
 
         @staticmethod
-        def forward(ctx, q, k, cu_seqlens, theta, cos_sin_cache):
-            rope_qk_fwd(q, k, cu_seqlens, theta, in_place=True, cos_sin_cache=cos_sin_cache)
+        def forward(ctx, q, k, theta, cu_seqlens, position_ids, token_offset, position_scale, cos_sin_cache):
+            rope_qk_apply(q, k, theta, cu_seqlens=cu_seqlens, position_ids=position_ids,
+                          token_offset=token_offset, position_scale=position_scale, cos_sin_cache=cos_sin_cache)
             ctx.mark_dirty(q, k)
-            ctx.save_for_backward(cu_seqlens, cos_sin_cache)
-            ctx.theta = theta
+            ctx.save_for_backward(cu_seqlens, position_ids, cos_sin_cache)
+            ctx.args = (theta, token_offset, position_scale)
             return q, k
 
         @staticmethod
         def backward(ctx, dq, dk):
-            cu_seqlens, cache = ctx.saved_tensors
-            dq = dq.contiguous()
-            dk = dk.contiguous()
-            dq_out = torch.empty_like(dq)
-            dk_out = torch.empty_like(dk)
-            rope_qk_bwd(dq, dk, cu_seqlens, ctx.theta, in_place=False, q_out=dq_out, k_out=dk_out,
-                        cos_sin_cache=cache)
-            return dq_out, dk_out, None, None, None
+            cu_seqlens, position_ids, cache = ctx.saved_tensors
+            theta, token_offset, position_scale = ctx.args
+            dq, dk = dq.contiguous(), dk.contiguous()      # e.g. broadcast (stride 0) gradients
+            dq_out = torch.empty(dq.shape, dtype=dq.dtype, device=dq.device)
+            dk_out = torch.empty(dk.shape, dtype=dk.dtype, device=dk.device)
+            rope_qk_apply(dq, dk, theta, cu_seqlens=cu_seqlens, position_ids=position_ids, backward=True,
+                          q_out=dq_out, k_out=dk_out, token_offset=token_offset,
+                          position_scale=position_scale, cos_sin_cache=cache)
+            return dq_out, dk_out, None, None, None, None, None, None
 
     return RopeQK
 
@@ -69,9 +71,64 @@ def _autograd_function():
 _RopeQK = None
 
 
-def apply_rope_qk(q, k, cu_seqlens, theta: float, cos_sin_cache=None):
-    """Differentiable in-place RoPE of packed q [T, Hq, d] and k [T, Hkv, d]."""
+def apply_rope_qk(q, k, cu_seqlens, theta: float, cos_sin_cache=None, position_ids=None, token_offset: int = 0,
+                  position_scale: float = 1.0):
+    """Differentiable in-place RoPE of packed q [T, Hq, d] and k [T, Hkv, d] (any
+    token/head strides).  Positions from ``position_ids`` if given, else from
+    ``cu_seqlens`` (row r is token ``token_offset + r``)."""
     global _RopeQK
     if _RopeQK is None:
         _RopeQK = _autograd_function()
-    return _RopeQK.apply(q, k, cu_seqlens, theta, cos_sin_cache)
+    return _RopeQK.apply(q, k, theta, cu_seqlens, position_ids, int(token_offset), float(position_scale),
+                         cos_sin_cache)
+
+
+def cache_rows_for(needed: int, current: int) -> int:
+    """Rows a growing cos/sin cache is built with: ``current`` if it covers ``needed``,
+    else the next power of two >= needed (at least 1024), so that a run of growing packs
+    rebuilds it O(log) times."""
+    if needed <= current:
+        return current
+    return max(1024, 1 << (int(needed) - 1).bit_length())
+
+
+class RotaryEmbedding:
+    """The rotation of one attention layout (head_dim, theta, linear position_scale)
+    with its cos/sin cache managed per device.
+
+    Positions taken from ``cu_seqlens`` are below ``token_offset + T``, a bound known on
+    the host, so the cache is grown to that many rows before the call (no device
+    synchronisation); with explicit ``position_ids`` it is grown to ``T`` rows and
+    positions beyond it are evaluated on the fly, with the same bits.
+
+        >>> rope = RotaryEmbedding(128, 1e6)
+        >>> q, k = rope(q, k, cu_seqlens=cu)          # in place, differentiable
+    """
+
+    def __init__(self, head_dim: int, theta: float, position_scale: float = 1.0):
+        if head_dim % 16 != 0 or not 16 <= head_dim <= 256:
+            raise ValueError("head_dim must be a multiple of 16 in [16, 256]")
+        self.head_dim, self.theta, self.position_scale = int(head_dim), float(theta), float(position_scale)
+        self._caches = {}
+
+    def cache(self, device, rows: int):
+        """The cos/sin cache of ``device`` with at least ``rows`` rows (built or grown)."""
+        import torch
+
+        device = torch.device(device)
+        cur = self._caches.get(device)
+        want = cache_rows_for(rows, 0 if cur is None else cur.shape[0])
+        if cur is None or want != cur.shape[0]:
+            cur = new_cos_sin_cache(want, self.head_dim, self.theta, device=device,
+                                    position_scale=self.position_scale)
+            self._caches[device] = cur
+        return cur
+
+    def __call__(self, q, k, cu_seqlens=None, position_ids=None, token_offset: int = 0):
+        if q.shape[-1] != self.head_dim:
+            raise ValueError("q and k must have head_dim %d" % self.head_dim)
+        T = q.shape[0]
+        rows = T if position_ids is not None else int(token_offset) + T
+        cache = self.cache(q.device, max(rows, 1))
+        return apply_rope_qk(q, k, cu_seqlens, self.theta, cos_sin_cache=cache, position_ids=position_ids,
+                             token_offset=token_offset, position_scale=self.position_scale)

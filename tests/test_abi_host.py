@@ -242,3 +242,12 @@ def test_binding_rejects_cpu_tensors():
     cu = torch.tensor([0, 4], dtype=torch.int32)
     with pytest.raises(ValueError):
         pr.rope_qk_fwd(q, k, cu, 1e4)
+
+
+def test_rotary_cache_growth_rule():
+    from packed_varlen_rope_gb300 import cache_rows_for
+
+    assert cache_rows_for(1, 0) == 1024 and cache_rows_for(1024, 0) == 1024
+    assert cache_rows_for(1025, 1024) == 2048 and cache_rows_for(16384, 0) == 16384
+    assert cache_rows_for(20000, 16384) == 32768 and cache_rows_for(500, 32768) == 32768
+    assert cache_rows_for((1 << 20) + 1, 1 << 20) == 1 << 21

@@ -437,3 +437,61 @@ def test_maximum_token_count(dev):
         pr().rope_qk_fwd(over, torch.empty((T + 1, hkv, d), dtype=torch.bfloat16, device=dev),
                          torch.tensor([0, T + 1], dtype=torch.int32, device=dev), 1.0e6)
     assert err.value.status == -6
+
+
+def test_rotary_embedding_module(dev):
+    """RotaryEmbedding keeps a per-device cache sized from the host-known position bound:
+    forward and backward equal the oracle (tiny pack) and the plain entry points (bit for
+    bit, 16k pack), the cache grows to the next power of two when a longer pack comes,
+    context-parallel halves with token_offset equal the whole pack, and a broadcast
+    gradient (sum().backward()) is accepted."""
+    from packed_varlen_rope_gb300 import RotaryEmbedding
+
+    w, pack, q, k, dq, dk = _workload_inputs(1)
+    cu_dev = torch.from_numpy(pack.cu_seqlens).to(dev)
+    rope = RotaryEmbedding(w.head_dim, w.theta)
+    q0, k0, g_q = (to_bits(t) for t in (q, k, dq))
+    qleaf = torch.zeros_like(q, requires_grad=True)
+    kleaf = torch.zeros_like(k, requires_grad=True)
+    yq, yk = rope(qleaf + q, kleaf + k, cu_seqlens=cu_dev)
+    torch.autograd.backward([yq, yk], [dq, dk])
+    assert np.array_equal(to_bits(yq), oracle.rope_packed(q0, pack.cu_seqlens, w.theta))
+    assert np.array_equal(to_bits(yk), oracle.rope_packed(k0, pack.cu_seqlens, w.theta))
+    assert np.array_equal(to_bits(qleaf.grad), oracle.rope_packed(g_q, pack.cu_seqlens, w.theta, bwd=True))
+    assert rope.cache(dev, 1).shape[0] == 1024
+
+    w2, pack2, q2, k2, dq2, dk2 = _workload_inputs(2)
+    cu2 = torch.from_numpy(pack2.cu_seqlens).to(dev)
+    rope2 = RotaryEmbedding(w2.head_dim, w2.theta)
+    ref_q, ref_k = q2.clone(), k2.clone()
+    pr().rope_qk_fwd(ref_q, ref_k, cu2, w2.theta)
+    got_q, got_k = rope2(q2.clone(), k2.clone(), cu_seqlens=cu2)
+    assert torch.equal(got_q, ref_q) and torch.equal(got_k, ref_k)
+    assert rope2.cache(dev, 1).shape[0] == 16384
+    # two context-parallel halves of the same pack
+    half = pack2.total_tokens // 2
+    qa, ka = q2.clone(), k2.clone()
+    rope2(qa[:half], ka[:half], cu_seqlens=cu2, token_offset=0)
+    rope2(qa[half:], ka[half:], cu_seqlens=cu2, token_offset=half)
+    assert torch.equal(qa, ref_q) and torch.equal(ka, ref_k)
+    # a longer pack grows the cache
+    T3 = 20000
+    cu3 = torch.tensor([0, T3], dtype=torch.int32, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(31)
+    q3 = torch.randn((T3, 2, w2.head_dim), device=dev, generator=gen).to(torch.bfloat16)
+    k3 = torch.randn((T3, 1, w2.head_dim), device=dev, generator=gen).to(torch.bfloat16)
+    ref3 = (q3.clone(), k3.clone())
+    pr().rope_qk_fwd(ref3[0], ref3[1], cu3, w2.theta)
+    out3 = rope2(q3, k3, cu_seqlens=cu3)
+    assert rope2.cache(dev, 1).shape[0] == 32768
+    assert torch.equal(out3[0], ref3[0]) and torch.equal(out3[1], ref3[1])
+    # broadcast gradient
+    ql = torch.zeros((64, 2, w2.head_dim), dtype=torch.bfloat16, device=dev, requires_grad=True)
+    kl = torch.zeros((64, 1, w2.head_dim), dtype=torch.bfloat16, device=dev, requires_grad=True)
+    yq, yk = rope2(ql + 1, kl + 1, cu_seqlens=torch.tensor([0, 64], dtype=torch.int32, device=dev))
+    (yq.float().sum() + yk.float().sum()).backward()
+    ones = torch.ones((64, 2, w2.head_dim), dtype=torch.bfloat16, device=dev)
+    expect = pr().rope_qk_bwd(ones.clone(), ones[:, :1].clone(), torch.tensor([0, 64], dtype=torch.int32,
+                                                                               device=dev), w2.theta)
+    assert torch.equal(ql.grad, expect[0]) and torch.equal(kl.grad, expect[1])

@@ -54,6 +54,8 @@ def parse_args():
                     help="target seconds of oracle work for the CPU baseline sample")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cache", action="store_true",
+                    help="rope path: no cos/sin cache, binary64 sincos evaluated per tile")
     ap.add_argument("--path", choices=["rope", "glu", "rope-forms"], default="rope",
                     help="rope: the QK-RoPE step (default); glu: SwiGLU/GeGLU forward+backward")
     ap.add_argument("--glu-workload", default="qwen3-4b-mlp-1m")
@@ -370,7 +372,7 @@ def run_ours(args, rank, world, local):
     dq = wl.normal_bf16(shape_q, wl.seed(args.workload, "dq", rank), device=dev)
     dk = wl.normal_bf16(shape_k, wl.seed(args.workload, "dk", rank), device=dev)
     cu = torch.from_numpy(pack.cu_seqlens).to(dev)
-    cache = pr.new_cos_sin_cache(max(pack.lengths), w.head_dim, w.theta, device=dev)
+    cache = None if args.no_cache else pr.new_cos_sin_cache(max(pack.lengths), w.head_dim, w.theta, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     do_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
@@ -453,13 +455,14 @@ def run_ours(args, rank, world, local):
             "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "theta": w.theta,
             "layout": "packed [T, H, d] bf16, in place", "parallelism": "dp%d (independent packs)" % world,
             "l2": "no flush: Q, K, dQ, dK = %.2f GB per step > 129 MB L2" % (bytes_per_pass / 1e9),
-            "cos_sin": "fp32 cache of %d positions built once before timing" % max(pack.lengths),
+            "cos_sin": ("binary64 sincos per tile, no cache" if cache is None else
+                        "fp32 cache of %d positions built once before timing" % max(pack.lengths)),
         },
         "hbm_gbs": 2 * bytes_per_pass / (ms_per_step / 1e3) / 1e9,
         "hbm_frac_of_measured": 2 * bytes_per_pass / (ms_per_step / 1e3) / 1e9 / peak,
         "hbm_frac_of_nominal_8tbs": 2 * bytes_per_pass / (ms_per_step / 1e3) / 1e9 / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": profiled_traffic(w.name),
+                     "frac": achieved / peak, "traffic": profiled_traffic(w.name) if cache is not None else None,
                      "kernel": "rope_qk_tile_kernel<128,false>",
                      "algorithmic_bytes_per_launch": bytes_per_pass,
                      "avg_launch_us": avg_launch_s * 1e6, "peak_kind": peak_kind + " (hbm_gbs)"},

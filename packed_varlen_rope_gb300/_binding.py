@@ -124,6 +124,15 @@ def _stream(stream, device) -> int:
     return int(stream.cuda_stream)
 
 
+def _on(device, fn, *args):
+    """Call library entry point ``fn`` with ``device`` current: the library launches on
+    the calling thread's current device, and the stream passed belongs to ``device``."""
+    import torch
+
+    with torch.cuda.device(device):
+        return fn(*args)
+
+
 def _check_qk(q, k):
     import torch
 
@@ -150,8 +159,8 @@ def _rope(fn_name, q, k, cu_seqlens, theta, in_place, q_out, k_out, cos_sin_cach
         if q_out is None or k_out is None:
             raise ValueError("q_out and k_out are required when in_place is False")
         _check_qk(q_out, k_out)
-        if q_out.shape != q.shape or k_out.shape != k.shape:
-            raise ValueError("q_out/k_out must have the shapes of q/k")
+        if q_out.shape != q.shape or k_out.shape != k.shape or q_out.device != q.device:
+            raise ValueError("q_out/k_out must have the shapes and device of q/k")
     rows = 0
     if cos_sin_cache is not None:
         if cos_sin_cache.dim() != 4 or tuple(cos_sin_cache.shape[1:]) != (4, d // 16, 4) or \
@@ -159,10 +168,10 @@ def _rope(fn_name, q, k, cu_seqlens, theta, in_place, q_out, k_out, cos_sin_cach
             raise ValueError("cos_sin_cache must be a contiguous float32 [rows, 4, head_dim/16, 4] tensor")
         rows = cos_sin_cache.shape[0]
     fn = getattr(load_library(), fn_name)
-    st = fn(_ptr(q), _ptr(k), _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, hq, hkv, d,
-            float(theta), 1 if in_place else 0, _ptr(q_out) if not in_place else None,
-            _ptr(k_out) if not in_place else None, _ptr(cos_sin_cache), rows,
-            _stream(stream, q.device))
+    st = _on(q.device, fn, _ptr(q), _ptr(k), _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, hq, hkv, d,
+             float(theta), 1 if in_place else 0, _ptr(q_out) if not in_place else None,
+             _ptr(k_out) if not in_place else None, _ptr(cos_sin_cache), rows,
+             _stream(stream, q.device))
     _check(fn_name, st)
     return (q, k) if in_place else (q_out, k_out)
 
@@ -193,11 +202,12 @@ def rope_cos_sin_cache_build(cache, theta: float, stream=None, position_scale: f
     lib = load_library()
     st_ = _stream(stream, cache.device)
     if position_scale == 1.0:
-        st = lib.rope_cos_sin_cache_build(_ptr(cache), cache.shape[0], 16 * cache.shape[2], float(theta), st_)
+        st = _on(cache.device, lib.rope_cos_sin_cache_build, _ptr(cache), cache.shape[0], 16 * cache.shape[2],
+                 float(theta), st_)
         _check("rope_cos_sin_cache_build", st)
     else:
-        st = lib.rope_cos_sin_cache_build_scaled(_ptr(cache), cache.shape[0], 16 * cache.shape[2], float(theta),
-                                                 float(position_scale), st_)
+        st = _on(cache.device, lib.rope_cos_sin_cache_build_scaled, _ptr(cache), cache.shape[0],
+                 16 * cache.shape[2], float(theta), float(position_scale), st_)
         _check("rope_cos_sin_cache_build_scaled", st)
     return cache
 
@@ -224,8 +234,8 @@ def rope_qk_positions(cu_seqlens, total_tokens: int, pos_out=None, stream=None):
     if pos_out is None:
         pos_out = torch.empty(int(total_tokens), dtype=torch.int32, device=cu_seqlens.device)
     _check_cu(cu_seqlens, pos_out.device)
-    st = load_library().rope_qk_positions(_ptr(cu_seqlens), cu_seqlens.numel() - 1, int(total_tokens),
-                                          _ptr(pos_out), _stream(stream, cu_seqlens.device))
+    st = _on(cu_seqlens.device, load_library().rope_qk_positions, _ptr(cu_seqlens), cu_seqlens.numel() - 1,
+             int(total_tokens), _ptr(pos_out), _stream(stream, cu_seqlens.device))
     _check("rope_qk_positions", st)
     return pos_out
 
@@ -236,9 +246,8 @@ def rope_validate_cu_seqlens(cu_seqlens, total_tokens: int, err_word=None, strea
 
     if err_word is None:
         err_word = torch.empty(1, dtype=torch.int32, device=cu_seqlens.device)
-    st = load_library().rope_validate_cu_seqlens(_ptr(cu_seqlens), cu_seqlens.numel() - 1,
-                                                 int(total_tokens), _ptr(err_word),
-                                                 _stream(stream, cu_seqlens.device))
+    st = _on(cu_seqlens.device, load_library().rope_validate_cu_seqlens, _ptr(cu_seqlens),
+             cu_seqlens.numel() - 1, int(total_tokens), _ptr(err_word), _stream(stream, cu_seqlens.device))
     _check("rope_validate_cu_seqlens", st)
     return err_word
 
@@ -285,8 +294,9 @@ def rope_qk_apply(q, k, theta: float, cu_seqlens=None, position_ids=None, backwa
     if (q_out is None) != (k_out is None):
         raise ValueError("give both q_out and k_out, or neither (in place)")
     if q_out is not None:
-        if q_out.shape != q.shape or k_out.shape != k.shape:
-            raise ValueError("q_out/k_out must have the shapes of q/k")
+        if q_out.shape != q.shape or k_out.shape != k.shape or q_out.device != q.device or \
+                k_out.device != q.device:
+            raise ValueError("q_out/k_out must have the shapes and device of q/k")
         desc.q_out, desc.q_out_stride_token, desc.q_out_stride_head = _view_args(q_out, "q_out")
         desc.k_out, desc.k_out_stride_token, desc.k_out_stride_head = _view_args(k_out, "k_out")
     if position_ids is not None:
@@ -319,7 +329,7 @@ def rope_qk_apply(q, k, theta: float, cu_seqlens=None, position_ids=None, backwa
         desc.cos_sin_cache = _ptr(cos_sin_cache)
         desc.cache_rows = cos_sin_cache.shape[0]
     desc.backward = 1 if backward else 0
-    st = load_library().rope_qk_apply(ctypes.byref(desc), _stream(stream, q.device))
+    st = _on(q.device, load_library().rope_qk_apply, ctypes.byref(desc), _stream(stream, q.device))
     _check("rope_qk_apply", st)
     return (q, k) if q_out is None else (q_out, k_out)
 
@@ -328,11 +338,13 @@ def rope_qk_abi_version() -> int:
     return int(load_library().rope_qk_abi_version())
 
 
-def _mat_args(t, name, shape):
+def _mat_args(t, name, shape, device):
     import torch
 
     if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 2 or (t.numel() and t.stride(1) != 1):
         raise ValueError("%s must be a CUDA bf16 [rows, cols] view with contiguous rows" % name)
+    if t.device != device:
+        raise ValueError("%s must be on %s" % (name, device))
     if tuple(t.shape) != tuple(shape):
         raise ValueError("%s must have shape %s" % (name, tuple(shape)))
     return _ptr(t), t.stride(0)
@@ -347,11 +359,11 @@ def glu_fwd(kind: str, e, g, h=None, stream=None):
     shape = tuple(e.shape)
     if h is None:
         h = torch.empty(shape, dtype=torch.bfloat16, device=e.device)
-    ep, es = _mat_args(e, "e", shape)
-    gp, gs = _mat_args(g, "g", shape)
-    hp, hs = _mat_args(h, "h", shape)
-    st = load_library().glu_fwd(GLU_KINDS[kind], ep, es, gp, gs, hp, hs, shape[0], shape[1],
-                                _stream(stream, e.device))
+    ep, es = _mat_args(e, "e", shape, e.device)
+    gp, gs = _mat_args(g, "g", shape, e.device)
+    hp, hs = _mat_args(h, "h", shape, e.device)
+    st = _on(e.device, load_library().glu_fwd, GLU_KINDS[kind], ep, es, gp, gs, hp, hs, shape[0], shape[1],
+             _stream(stream, e.device))
     _check("glu_fwd", st)
     return h
 
@@ -368,8 +380,9 @@ def glu_bwd(kind: str, dh, e, g, de=None, dg=None, stream=None):
         dg = torch.empty(shape, dtype=torch.bfloat16, device=e.device)
     args = []
     for name, t in (("dh", dh), ("e", e), ("g", g), ("de", de), ("dg", dg)):
-        args += list(_mat_args(t, name, shape))
-    st = load_library().glu_bwd(GLU_KINDS[kind], *args, shape[0], shape[1], _stream(stream, e.device))
+        args += list(_mat_args(t, name, shape, e.device))
+    st = _on(e.device, load_library().glu_bwd, GLU_KINDS[kind], *args, shape[0], shape[1],
+             _stream(stream, e.device))
     _check("glu_bwd", st)
     return de, dg
 
@@ -427,10 +440,11 @@ def rope_qk_host(q, k, theta: float, workspace=None, cu_seqlens=None, position_i
     desc.backward = 1 if backward else 0
     if workspace is None:
         # no workspace: the library's own static staging array (rope_qk_host_static)
-        st = load_library().rope_qk_host_static(ctypes.byref(desc), _stream(stream, dev))
+        st = _on(dev, load_library().rope_qk_host_static, ctypes.byref(desc), _stream(stream, dev))
         _check("rope_qk_host_static", st)
     else:
         nbytes = workspace.numel() * workspace.element_size()
-        st = load_library().rope_qk_host(ctypes.byref(desc), _ptr(workspace), nbytes, _stream(stream, dev))
+        st = _on(dev, load_library().rope_qk_host, ctypes.byref(desc), _ptr(workspace), nbytes,
+                 _stream(stream, dev))
         _check("rope_qk_host", st)
     return (q, k) if q_out is None else (q_out, k_out)

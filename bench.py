@@ -255,6 +255,8 @@ def run_reference(args, rank, world):
                                    % (n, w.name)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
+        # the same oracle calls split over every host core, beside the single-core figure
+        "cpu_baseline_all_cores": cpu_all_cores(w, pos[:qs.shape[0]], qs, ks, qs, ks),
     }
     print(json.dumps(line), flush=True)
     return 0

@@ -49,7 +49,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=4)
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target seconds of oracle work for the CPU baseline sample")
     ap.add_argument("--no-e2e", action="store_true")
@@ -521,6 +521,7 @@ def end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev):
     return {"value": whole_job_tokens_per_s(world, pack.valid_tokens, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": h2d, "ms_per_step": ms, "steps": E,
             "step_ms_min": min(steps_ms), "step_ms_median": statistics.median(steps_ms),
+            "step_ms_max": max(steps_ms),
             "path": "rope_qk_host: pinned host buffers streamed in %d-token chunks" % chunk}
 
 

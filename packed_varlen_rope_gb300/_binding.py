@@ -115,9 +115,14 @@ def _ptr(t) -> Optional[int]:
 
 
 def _stream(stream, device) -> int:
+    """Raw cudaStream_t of ``stream`` (a torch stream or an int), else the current stream
+    of ``device``."""
     import torch
 
     if stream is None:
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            return int(raw(device.index if device.index is not None else torch.cuda.current_device()))
         return int(torch.cuda.current_stream(device).cuda_stream)
     if isinstance(stream, int):
         return stream
@@ -126,9 +131,12 @@ def _stream(stream, device) -> int:
 
 def _on(device, fn, *args):
     """Call library entry point ``fn`` with ``device`` current: the library launches on
-    the calling thread's current device, and the stream passed belongs to ``device``."""
+    the calling thread's current device, and the stream passed belongs to ``device``.
+    The device is switched (and restored) only when another one is current."""
     import torch
 
+    if device.index is None or device.index == torch.cuda.current_device():
+        return fn(*args)
     with torch.cuda.device(device):
         return fn(*args)
 

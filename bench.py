@@ -642,13 +642,24 @@ def run_rope_forms(args, rank, world, local):
     bits = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)  # noqa: E731
 
     def timed(fn, reps=50):
-        for _ in range(3):
+        # each form captured once in a CUDA graph and replayed, so that groups of short
+        # launches (the shard forms) are timed without the host's launch gaps
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                fn()
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
             fn()
+        for _ in range(3):
+            graph.replay()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
         torch.cuda.synchronize()
         for a, b in ev:
             a.record()
-            fn()
+            graph.replay()
             b.record()
         torch.cuda.synchronize()
         return statistics.median(a.elapsed_time(b) for a, b in ev) / 1e3
@@ -738,7 +749,8 @@ def run_rope_forms(args, rank, world, local):
            "oracle on %d sampled tokens: %d elements, %d differ" % (pick.size, n_el, mism))
     line = {"metric": "QK-RoPE forward per input form", "unit": "GB/s", "workload": w.name,
             "algorithmic_bytes_per_launch": nbytes, "peak": peak, "peak_kind": peak_kind + " (hbm_gbs)",
-            "timing": "median of 50 launches (CUDA events), inputs %.2f GB > L2" % (nbytes / 2e9),
+            "timing": "median of 50 CUDA-graph replays of each form (CUDA events), inputs %.2f GB > L2"
+                      % (nbytes / 2e9),
             "forms": forms}
     print(json.dumps(line), flush=True)
     bad = [n for n, f in forms.items() if "MISMATCH" in f["check"] or "CHANGED" in f["check"] or

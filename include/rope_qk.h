@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define ROPE_QK_ABI_VERSION 3
+#define ROPE_QK_ABI_VERSION 4
 
 typedef enum rope_status {
     ROPE_OK = 0,
@@ -68,6 +68,9 @@ typedef enum rope_status {
     ROPE_ERR_KIND = -9,         /* unknown activation kind (glu.h) */
     ROPE_ERR_WORKSPACE = -10    /* one token's Q and K rows do not fit the static staging */
 } rope_status;
+
+/* Bits of rope_qk_desc.flags. */
+#define ROPE_FLAG_POSITION_IDS_INT64 0x1   /* position_ids points to int64 values */
 
 /* Bits of the word rope_validate_cu_seqlens writes. */
 #define ROPE_CU_NEGATIVE_START   0x1   /* cu_seqlens[0] < 0 */
@@ -135,7 +138,10 @@ int rope_qk_bwd(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs,
  * Positions.  If position_ids is non-NULL (device int32 [total_tokens], the per-example
  * position ids a 1-D pack carries in databricks.com "Reducing Qwen training time 6x",
  * section on 1-D packing), row r has position position_ids[r]; a value outside
- * [0, 2^24) leaves the row out (in place: untouched; out of place: copied).  Otherwise
+ * [0, 2^24) leaves the row out (in place: untouched; out of place: copied).  With
+ * ROPE_FLAG_POSITION_IDS_INT64 in flags, position_ids points to int64 values instead
+ * (8-byte aligned; the dtype of the position ids a Hugging Face collator builds), with
+ * the same rule for values outside [0, 2^24).  Otherwise
  * row r is token token_offset + r of the stream cu_seqlens describes and its position
  * is derived as for rope_qk_fwd; token_offset lets a context-parallel shard holding
  * tokens [a, b) of a pack pass the whole pack's cu_seqlens with token_offset = a
@@ -176,7 +182,8 @@ typedef struct rope_qk_desc {
     const float *cos_sin_cache;    /* optional, as for rope_qk_fwd                    */
     int64_t cache_rows;
     int32_t backward;              /* 0: rotation; nonzero: transpose (sin negated)   */
-    int32_t reserved;              /* set to 0                                        */
+    int32_t flags;                 /* ROPE_FLAG_* bits, 0 for none; an unknown bit is
+                                      ROPE_ERR_UNSUPPORTED                             */
     const int32_t *seq_used;       /* optional device int32 [n_seqs], with cu_seqlens */
 } rope_qk_desc;
 

@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     ROPE_CU_NEGATIVE_START,
     ROPE_CU_NONZERO_START,
     ROPE_CU_PAST_END,
+    ROPE_FLAG_POSITION_IDS_INT64,
     RopeError,
     RopeQKDesc,
     glu_bwd,

@@ -27,6 +27,7 @@ ROPE_CU_NEGATIVE_START = 0x1
 ROPE_CU_DECREASING = 0x2
 ROPE_CU_PAST_END = 0x4
 ROPE_CU_NONZERO_START = 0x8
+ROPE_FLAG_POSITION_IDS_INT64 = 0x1
 
 _lib = None
 
@@ -44,7 +45,7 @@ class RopeQKDesc(ctypes.Structure):
         ("position_ids", ctypes.c_void_p), ("total_tokens", ctypes.c_int64), ("token_offset", ctypes.c_int64),
         ("theta", ctypes.c_double), ("position_scale", ctypes.c_double),
         ("cos_sin_cache", ctypes.c_void_p), ("cache_rows", ctypes.c_int64),
-        ("backward", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("backward", ctypes.c_int32), ("flags", ctypes.c_int32),
         ("seq_used", ctypes.c_void_p),
     ]
 
@@ -286,7 +287,7 @@ def rope_qk_apply(q, k, theta: float, cu_seqlens=None, position_ids=None, backwa
 
     q, k: bf16 CUDA views [T, Hq, d] and [T, Hkv, d] with any token/head strides
     (head_dim contiguous) -- e.g. the Q and K slices of one fused QKV output, rotated in
-    place.  Positions come from ``position_ids`` (int32 [T]) if given, else from
+    place.  Positions come from ``position_ids`` (int32 or int64 [T]) if given, else from
     ``cu_seqlens`` with row r read as token ``token_offset + r`` (and, with
     ``seq_used``, only the first seq_used[s] tokens of sample s rotated).
     ``position_scale`` is the linear position rescale (1 = none).  Returns (q, k) in place, else (q_out,
@@ -310,10 +311,12 @@ def rope_qk_apply(q, k, theta: float, cu_seqlens=None, position_ids=None, backwa
     if position_ids is not None:
         import torch
 
-        if position_ids.dtype != torch.int32 or position_ids.device != q.device or \
+        if position_ids.dtype not in (torch.int32, torch.int64) or position_ids.device != q.device or \
                 not position_ids.is_contiguous() or position_ids.numel() != T:
-            raise ValueError("position_ids must be a contiguous int32 [tokens] tensor on the device of q")
+            raise ValueError("position_ids must be a contiguous int32 or int64 [tokens] tensor on the device of q")
         desc.position_ids = _ptr(position_ids)
+        if position_ids.dtype == torch.int64:
+            desc.flags |= ROPE_FLAG_POSITION_IDS_INT64
     elif cu_seqlens is not None:
         _check_cu(cu_seqlens, q.device)
         desc.cu_seqlens = _ptr(cu_seqlens)
@@ -432,9 +435,13 @@ def rope_qk_host(q, k, theta: float, workspace=None, cu_seqlens=None, position_i
         desc.q_out, desc.q_out_stride_token, desc.q_out_stride_head = _ptr(q_out), hq * d, d
         desc.k_out, desc.k_out_stride_token, desc.k_out_stride_head = _ptr(k_out), k.shape[1] * d, d
     if position_ids is not None:
-        if position_ids.dtype != torch.int32 or position_ids.device != dev or position_ids.numel() != T:
-            raise ValueError("position_ids must be an int32 [tokens] tensor on the workspace's device")
+        if position_ids.dtype not in (torch.int32, torch.int64) or position_ids.device != dev or \
+                not position_ids.is_contiguous() or position_ids.numel() != T:
+            raise ValueError("position_ids must be a contiguous int32 or int64 [tokens] tensor on the "
+                             "workspace's device")
         desc.position_ids = _ptr(position_ids)
+        if position_ids.dtype == torch.int64:
+            desc.flags |= ROPE_FLAG_POSITION_IDS_INT64
     elif cu_seqlens is not None:
         _check_cu(cu_seqlens, dev)
         desc.cu_seqlens, desc.n_seqs = _ptr(cu_seqlens), cu_seqlens.numel() - 1

@@ -57,6 +57,14 @@ bool contiguous(const void *p, int64_t ts, int64_t hs, int32_t heads, int32_t d)
     return p == nullptr || (hs == d && ts == static_cast<int64_t>(heads) * d);
 }
 
+// The position ids of rows [t0, ...) of a chunk: int32 or, with the flag, int64 values.
+const int32_t *ids_from(const rope_qk_desc &p, int64_t t0)
+{
+    if ((p.flags & ROPE_FLAG_POSITION_IDS_INT64) != 0)
+        return reinterpret_cast<const int32_t *>(reinterpret_cast<const int64_t *>(p.position_ids) + t0);
+    return p.position_ids + t0;
+}
+
 }  // namespace
 
 // Shared by rope_qk_host and its static-workspace variant: stream the pack through
@@ -68,6 +76,7 @@ int rope_qk_host_impl(const rope_qk_desc *dp, void *workspace, int64_t workspace
     const int64_t T = p.total_tokens;
     if (T < 0 || p.n_q_heads < 1 || p.n_kv_heads < 1 || p.token_offset < 0 || workspace_bytes < 0)
         return ROPE_ERR_SHAPE;
+    if ((p.flags & ~ROPE_FLAG_POSITION_IDS_INT64) != 0) return ROPE_ERR_UNSUPPORTED;
     if (p.head_dim < 16 || p.head_dim > 256 || p.head_dim % 16 != 0) return ROPE_ERR_HEAD_DIM;
     if (T == 0) return ROPE_OK;
     if (p.q == nullptr || p.k == nullptr || workspace == nullptr) return ROPE_ERR_NULL;
@@ -143,7 +152,7 @@ int rope_qk_host_impl(const rope_qk_desc *dp, void *workspace, int64_t workspace
         cd.q_out = nullptr;
         cd.k_out = nullptr;
         cd.total_tokens = n;
-        if (p.position_ids != nullptr) cd.position_ids = p.position_ids + t0;
+        if (p.position_ids != nullptr) cd.position_ids = ids_from(p, t0);
         else cd.token_offset = p.token_offset + t0;
         rc = rope_qk_apply(&cd, stream);
         if (rc != ROPE_OK) {
@@ -191,6 +200,7 @@ extern "C" int rope_qk_host_static(const rope_qk_desc *desc, void *stream)
     if (desc == nullptr) return ROPE_ERR_NULL;
     const rope_qk_desc &p = *desc;
     if (p.total_tokens < 0 || p.n_q_heads < 1 || p.n_kv_heads < 1) return ROPE_ERR_SHAPE;
+    if ((p.flags & ~ROPE_FLAG_POSITION_IDS_INT64) != 0) return ROPE_ERR_UNSUPPORTED;
     if (p.head_dim < 16 || p.head_dim > 256 || p.head_dim % 16 != 0) return ROPE_ERR_HEAD_DIM;
     if (p.total_tokens == 0) return ROPE_OK;
     const int64_t q_row = static_cast<int64_t>(p.n_q_heads) * p.head_dim * 2;
@@ -247,7 +257,7 @@ extern "C" int rope_qk_host_static(const rope_qk_desc *desc, void *stream)
         cd.q_out = nullptr;
         cd.k_out = nullptr;
         cd.total_tokens = n;
-        if (p.position_ids != nullptr) cd.position_ids = p.position_ids + t0;
+        if (p.position_ids != nullptr) cd.position_ids = ids_from(p, t0);
         else cd.token_offset = p.token_offset + t0;
         const int rc = rope_qk_apply(&cd, stream);
         if (rc != ROPE_OK) return rc;

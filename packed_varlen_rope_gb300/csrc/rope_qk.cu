@@ -53,6 +53,7 @@ struct RopeArgs {
     int64_t qo_ts, qo_hs, ko_ts, ko_hs;      // output strides
     const int32_t *cu;
     const int32_t *pos_ids;                  // optional per-row positions (replaces cu)
+    const long long *pos_ids64;              // the same as int64 values
     const int32_t *seq_used;                 // optional tokens used per sample (with cu)
     const float4 *cache;
     int32_t n_seqs;
@@ -192,6 +193,9 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
             if (a.pos_ids != nullptr) {
                 const int p = __ldg(a.pos_ids + r);
                 pos = (p >= 0 && p < static_cast<int>(kMaxTokens)) ? p : -1;
+            } else if (a.pos_ids64 != nullptr) {
+                const long long p = __ldg(a.pos_ids64 + r);
+                pos = (p >= 0 && p < static_cast<long long>(kMaxTokens)) ? static_cast<int>(p) : -1;
             } else {
                 pos = token_position(a.cu, a.n_seqs, a.token_offset + r, a.seq_used);
             }
@@ -445,6 +449,8 @@ int rope_qk_apply_impl(const rope_qk_desc *dp, void *stream)
         p.token_offset < 0)
         return ROPE_ERR_SHAPE;
     if (p.n_q_heads > (1 << 20) || p.n_kv_heads > (1 << 20)) return ROPE_ERR_SHAPE;
+    if ((p.flags & ~ROPE_FLAG_POSITION_IDS_INT64) != 0) return ROPE_ERR_UNSUPPORTED;
+    const bool ids64 = (p.flags & ROPE_FLAG_POSITION_IDS_INT64) != 0;
     int rc = check_head_dim(p.head_dim);
     if (rc != ROPE_OK) return rc;
     if ((rc = check_theta(p.theta)) != ROPE_OK) return rc;
@@ -456,6 +462,7 @@ int rope_qk_apply_impl(const rope_qk_desc *dp, void *stream)
     if (T == 0) return ROPE_OK;     // nothing is read or written; pointers may be NULL
     if (p.position_ids == nullptr && p.cu_seqlens == nullptr) return ROPE_ERR_NULL;
     if (p.cos_sin_cache != nullptr && !aligned(p.cos_sin_cache, 16)) return ROPE_ERR_ALIGN;
+    if (ids64 && p.position_ids != nullptr && !aligned(p.position_ids, 8)) return ROPE_ERR_ALIGN;
 
     const int64_t d = p.head_dim;
     const View q{p.q, T, p.n_q_heads, p.q_stride_token, p.q_stride_head, d};
@@ -482,7 +489,8 @@ int rope_qk_apply_impl(const rope_qk_desc *dp, void *stream)
     a.q_ts = q.ts;  a.q_hs = q.hs;  a.k_ts = k.ts;  a.k_hs = k.hs;
     a.qo_ts = qo.ts; a.qo_hs = qo.hs; a.ko_ts = ko.ts; a.ko_hs = ko.hs;
     a.cu = p.cu_seqlens;
-    a.pos_ids = p.position_ids;
+    a.pos_ids = ids64 ? nullptr : p.position_ids;
+    a.pos_ids64 = ids64 ? reinterpret_cast<const long long *>(p.position_ids) : nullptr;
     a.seq_used = p.position_ids != nullptr ? nullptr : p.seq_used;
     a.cache = reinterpret_cast<const float4 *>(p.cos_sin_cache);
     a.n_seqs = p.position_ids != nullptr ? 0 : p.n_seqs;

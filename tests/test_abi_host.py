@@ -54,13 +54,13 @@ def test_library_exports_every_declared_symbol(lib):
 def test_header_is_plain_c(tmp_path):
     src = tmp_path / "use_header.c"
     src.write_text('#include "rope_qk.h"\n#include "glu.h"\n'
-                   'int main(void) { return ROPE_QK_ABI_VERSION == 3 && GLU_GEGLU_TANH == 2 ? 0 : 1; }\n')
+                   'int main(void) { return ROPE_QK_ABI_VERSION == 4 && GLU_GEGLU_TANH == 2 && ROPE_FLAG_POSITION_IDS_INT64 == 1 ? 0 : 1; }\n')
     subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Werror", "-pedantic", "-I", os.path.dirname(HEADER),
                            "-c", str(src), "-o", str(tmp_path / "use_header.o")])
 
 
 def test_abi_version_and_strerror(lib):
-    assert lib.rope_qk_abi_version() == 3
+    assert lib.rope_qk_abi_version() == 4
     for code in (OK, ERR_NULL, ERR_SHAPE, ERR_HEAD_DIM, ERR_ALIGN, ERR_OVERLAP, ERR_UNSUPPORTED,
                  ERR_LAUNCH, ERR_THETA, -9, -10):
         assert lib.rope_strerror(code)
@@ -192,6 +192,11 @@ def test_apply_argument_checks(lib):
     assert a(token_offset=-1) == ERR_SHAPE
     assert a(token_offset=(1 << 24) - 8) == ERR_UNSUPPORTED        # global tokens past 2^24
     assert a(cu_seqlens=None) == ERR_NULL
+    assert a(flags=2) == ERR_UNSUPPORTED and a(T=0, flags=4) == ERR_UNSUPPORTED   # unknown flag bits
+    assert a(flags=1, position_ids=CU + 4) == ERR_ALIGN              # int64 ids need 8-byte alignment
+    for entry in ("rope_qk_host", "rope_qk_host_static"):            # the host entries check them too
+        args = (ctypes.byref(_desc(flags=2)),) + ((Q, 1 << 20) if entry == "rope_qk_host" else ()) + (None,)
+        assert getattr(lib, entry)(*args) == ERR_UNSUPPORTED
     assert a(q_stride_token=4 * 64 + 4) == ERR_ALIGN                # stride not a multiple of 8
     assert a(k_stride_head=60) == ERR_ALIGN
     assert a(q_stride_head=56) == ERR_OVERLAP                       # heads overlap (stride < d)

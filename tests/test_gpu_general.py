@@ -147,19 +147,25 @@ def test_position_ids_equal_cu_path(dev):
     assert torch.equal(k.view(torch.int16), k2.view(torch.int16))
 
 
-def test_position_ids_arbitrary(dev):
-    """Explicit ids in any order, including ids outside [0, 2^24) which leave the row out."""
+@pytest.mark.parametrize("dtype", ["int32", "int64"])
+def test_position_ids_arbitrary(dev, dtype):
+    """Explicit ids in any order, including ids outside [0, 2^24) which leave the row out;
+    int64 ids (ROPE_FLAG_POSITION_IDS_INT64) also with values beyond the int32 range."""
     rng = np.random.Generator(np.random.PCG64(7))
     T, hq, hkv, d = 300, 3, 2, 64
     ids = rng.integers(0, 1 << 24, size=T).astype(np.int64)
     ids[:10] = [0, 1, (1 << 24) - 1, -1, -7, 1 << 24, (1 << 31) - 1, 5, 100000, 25000]
+    if dtype == "int64":
+        ids[10:15] = [1 << 33, -(1 << 40), (1 << 62), (1 << 32) + 5, -(1 << 63)]
+    ids_np = ids.astype(np.int32 if dtype == "int32" else np.int64)
     qb, kb = _bits(rng, (T, hq, d)), _bits(rng, (T, hkv, d))
     for bwd in (False, True):
         q, k = from_bits(qb, dev), from_bits(kb, dev)
-        pid = torch.from_numpy(ids.astype(np.int32)).to(dev)
+        pid = torch.from_numpy(ids_np).to(dev)
         pr().rope_qk_apply(q, k, 1.0e6, position_ids=pid, backward=bwd)
         torch.cuda.synchronize()
-        pos = np.where((ids >= 0) & (ids < (1 << 24)), ids, -1).astype(np.int32)
+        v = ids_np.astype(np.int64)
+        pos = np.where((v >= 0) & (v < (1 << 24)), v, -1).astype(np.int32)
         _check(to_bits(q), _expect(qb, pos, 1.0e6, bwd), qb, "ids q")
         _check(to_bits(k), _expect(kb, pos, 1.0e6, bwd), kb, "ids k")
 

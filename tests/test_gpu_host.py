@@ -82,6 +82,13 @@ def test_host_stream_out_of_place_ids_and_pageable(dev):
     assert torch.equal(qo.view(torch.int16), ref_q.cpu().view(torch.int16))
     assert torch.equal(ko.view(torch.int16), ref_k.cpu().view(torch.int16))
     assert torch.equal(q_in.view(torch.int16), q.view(torch.int16))   # inputs untouched
+    # the same with int64 ids: each chunk must read its own slice of the 8-byte ids
+    qo64, ko64 = torch.full_like(q, 2.0), torch.full_like(k, 2.0)
+    pr().rope_qk_host(q_in, k_in, w.theta, _workspace(dev, 96, w), position_ids=pos.to(torch.int64),
+                      q_out=qo64, k_out=ko64)
+    torch.cuda.current_stream(dev).synchronize()
+    assert torch.equal(qo64.view(torch.int16), qo.view(torch.int16))
+    assert torch.equal(ko64.view(torch.int16), ko.view(torch.int16))
 
 
 def test_host_stream_token_offset(dev):

@@ -54,6 +54,9 @@ def parse_args():
                     help="target seconds of oracle work for the CPU baseline sample")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layout", choices=["packed", "padded", "padded-seq-used"], default="packed",
+                    help="rope path: the pack as is, or (workloads with padded samples) the padded batch "
+                         "with every row rotated, or with the pad rows skipped through seq_used")
     ap.add_argument("--no-cache", action="store_true",
                     help="rope path: no cos/sin cache, binary64 sincos evaluated per tile")
     ap.add_argument("--path", choices=["rope", "glu", "rope-forms"], default="rope",
@@ -262,12 +265,24 @@ def run_reference(args, rank, world):
     return 0
 
 
-def cpu_baseline(args, w, pack, q_sample, k_sample, dq_sample, dk_sample):
-    """The oracle as it stands, single-threaded, on a contiguous token sample."""
+def valid_fraction(pack) -> float:
+    """Share of the rows that hold tokens: 1 for a pack, sum(L_b) / (B * pad_to) for a
+    padded batch (the padding waste of the unsloth.ai page, section "Pourquoi le
+    remplissage est-il nécessaire")."""
+    return pack.valid_tokens / pack.total_tokens
+
+
+def cpu_baseline(args, w, pack, q_sample, k_sample, dq_sample, dk_sample, skip_pad=False):
+    """The oracle as it stands, single-threaded, on a contiguous token sample (rows of a
+    padded batch left out when ``skip_pad``, as the seq_used form leaves them)."""
+    import numpy as np
+
     import oracle
 
     oracle.build()
     pos = oracle.positions(pack.cu_seqlens, pack.total_tokens)
+    if skip_pad and pack.valid_mask is not None:
+        pos = np.where(pack.valid_mask, pos, -1).astype(np.int32)
     n_all = q_sample.shape[0]
 
     def run(n):
@@ -284,13 +299,14 @@ def cpu_baseline(args, w, pack, q_sample, k_sample, dq_sample, dk_sample):
     t = time.perf_counter()
     outputs = run(n)
     el = time.perf_counter() - t
-    return {"value": n / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": "first %d tokens of the %s pack, fwd+bwd of Q and K, %.1f s on one host core"
-                      % (n, w.name, el)}, outputs, cpu_all_cores(w, pos[:n], q_sample[:n], k_sample[:n],
-                                                                  dq_sample[:n], dk_sample[:n])
+    valid = n if pack.valid_mask is None else int(np.count_nonzero(pack.valid_mask[:n]))
+    return {"value": valid / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "first %d rows (%d tokens) of the %s batch, fwd+bwd of Q and K, %.1f s on one host core"
+                      % (n, valid, w.name, el)}, outputs, cpu_all_cores(w, pos[:n], q_sample[:n], k_sample[:n],
+                                                                         dq_sample[:n], dk_sample[:n], valid=valid)
 
 
-def cpu_all_cores(w, pos, q, k, dq, dk, seconds=2.0):
+def cpu_all_cores(w, pos, q, k, dq, dk, seconds=2.0, valid=None):
     """The same oracle calls split into equal token ranges, one per host core the
     process may run on (the C calls release the GIL), repeated for about `seconds`."""
     import concurrent.futures as cf
@@ -320,7 +336,7 @@ def cpu_all_cores(w, pos, q, k, dq, dk, seconds=2.0):
             el = time.perf_counter() - t
             if el >= seconds:
                 break
-    return {"value": reps * n / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+    return {"value": reps * (n if valid is None else valid) / el, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": "first %d tokens of the %s pack in %d token ranges on %d threads, %d passes in %.1f s"
                       % (n, w.name, cores, cores, reps, el)}
 
@@ -366,16 +382,36 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = wl.WORKLOADS[args.workload]
-    pack = wl.make_pack(w, rank=rank)
+    if args.layout != "packed" and w.padded_samples is None:
+        print("--layout %s needs a workload with padded samples (3)" % args.layout, file=sys.stderr)
+        return 2
+    pack = wl.make_pack(w, "packed" if args.layout == "packed" else "padded", rank=rank)
     T = pack.total_tokens
+    if args.layout != "packed":
+        n_b, _, _, pad_to = w.padded_samples
+        assert abs(valid_fraction(pack) - sum(pack.lengths) / (n_b * pad_to)) < 1e-12
+    span = int(np.max(np.diff(pack.cu_seqlens)))          # longest sample, pad rows included
     shape_q, shape_k = (T, w.n_q_heads, w.head_dim), (T, w.n_kv_heads, w.head_dim)
     q = wl.normal_bf16(shape_q, wl.seed(args.workload, "q", rank), device=dev)
     k = wl.normal_bf16(shape_k, wl.seed(args.workload, "k", rank), device=dev)
     dq = wl.normal_bf16(shape_q, wl.seed(args.workload, "dq", rank), device=dev)
     dk = wl.normal_bf16(shape_k, wl.seed(args.workload, "dk", rank), device=dev)
     cu = torch.from_numpy(pack.cu_seqlens).to(dev)
-    cache = None if args.no_cache else pr.new_cos_sin_cache(max(pack.lengths), w.head_dim, w.theta, device=dev)
+    cache = None if args.no_cache else pr.new_cos_sin_cache(span, w.head_dim, w.theta, device=dev)
     stream = torch.cuda.current_stream(dev)
+    used = torch.tensor(pack.lengths, dtype=torch.int32, device=dev) if args.layout == "padded-seq-used" else None
+
+    def fwd(a, b):
+        if used is None:
+            pr.rope_qk_fwd(a, b, cu, w.theta, cos_sin_cache=cache)
+        else:
+            pr.rope_qk_apply(a, b, w.theta, cu_seqlens=cu, seq_used=used, cos_sin_cache=cache)
+
+    def bwd(a, b):
+        if used is None:
+            pr.rope_qk_bwd(a, b, cu, w.theta, cos_sin_cache=cache)
+        else:
+            pr.rope_qk_apply(a, b, w.theta, cu_seqlens=cu, seq_used=used, cos_sin_cache=cache, backward=True)
 
     do_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
     samples = None
@@ -386,11 +422,12 @@ def run_ours(args, rank, world, local):
         # written pageable host memory next to the e2e leg stalled its enqueueing thread)
         pristine = [t.clone() for t in (q, k, dq, dk)]
 
-    bytes_per_pass = 4 * (w.n_q_heads + w.n_kv_heads) * w.head_dim * pack.valid_tokens
+    rows_moved = T if args.layout == "padded" else pack.valid_tokens     # rows one launch reads and writes
+    bytes_per_pass = 4 * (w.n_q_heads + w.n_kv_heads) * w.head_dim * rows_moved
 
     def step():
-        pr.rope_qk_fwd(q, k, cu, w.theta, cos_sin_cache=cache)
-        pr.rope_qk_bwd(dq, dk, cu, w.theta, cos_sin_cache=cache)
+        fwd(q, k)
+        bwd(dq, dk)
 
     sampler = ClockSampler(physical_gpu_index(local))
     sampler.start()
@@ -408,10 +445,10 @@ def run_ours(args, rank, world, local):
     start.record(stream)
     for i in range(K):
         ev[4 * i].record(stream)
-        pr.rope_qk_fwd(q, k, cu, w.theta, cos_sin_cache=cache)
+        fwd(q, k)
         ev[4 * i + 1].record(stream)
         ev[4 * i + 2].record(stream)
-        pr.rope_qk_bwd(dq, dk, cu, w.theta, cos_sin_cache=cache)
+        bwd(dq, dk)
         ev[4 * i + 3].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
@@ -431,15 +468,15 @@ def run_ours(args, rank, world, local):
 
     e2e = None
     if not args.no_e2e:
-        e2e = end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev)
+        e2e = end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev, used)
 
     cpu = parity = None
     if do_cpu:
         samples = tuple(to_np(t, min(T, 65536)) for t in pristine)
-        cpu, ref_outputs, cpu_all = cpu_baseline(args, w, pack, *samples)
+        cpu, ref_outputs, cpu_all = cpu_baseline(args, w, pack, *samples, skip_pad=used is not None)
         pq, pk, pdq, pdk = pristine
-        pr.rope_qk_fwd(pq, pk, cu, w.theta, cos_sin_cache=cache)
-        pr.rope_qk_bwd(pdq, pdk, cu, w.theta, cos_sin_cache=cache)
+        fwd(pq, pk)
+        bwd(pdq, pdk)
         torch.cuda.synchronize()
         n = ref_outputs[0].shape[0]
         parity = parity_block([to_np(t, n) for t in (pq, pk, pdq, pdk)], ref_outputs, samples)
@@ -457,16 +494,22 @@ def run_ours(args, rank, world, local):
             "workload": w.name, "total_tokens": T, "valid_tokens": pack.valid_tokens,
             "n_seqs": pack.n_seqs, "max_seq_len": max(pack.lengths), "n_q_heads": w.n_q_heads,
             "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "theta": w.theta,
-            "layout": "packed [T, H, d] bf16, in place", "parallelism": "dp%d (independent packs)" % world,
+            "layout": {"packed": "packed [T, H, d] bf16, in place",
+                       "padded": "padded batch [B*pad_to, H, d] bf16, every row rotated, in place",
+                       "padded-seq-used": "padded batch [B*pad_to, H, d] bf16, pad rows skipped (seq_used)"
+                       }[args.layout],
+            "valid_fraction": valid_fraction(pack),
+            "parallelism": "dp%d (independent packs)" % world,
             "l2": "no flush: Q, K, dQ, dK = %.2f GB per step > 129 MB L2" % (bytes_per_pass / 1e9),
             "cos_sin": ("binary64 sincos per tile, no cache" if cache is None else
-                        "fp32 cache of %d positions built once before timing" % max(pack.lengths)),
+                        "fp32 cache of %d positions built once before timing" % span),
         },
         "hbm_gbs": 2 * bytes_per_pass / (ms_per_step / 1e3) / 1e9,
         "hbm_frac_of_measured": 2 * bytes_per_pass / (ms_per_step / 1e3) / 1e9 / peak,
         "hbm_frac_of_nominal_8tbs": 2 * bytes_per_pass / (ms_per_step / 1e3) / 1e9 / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": profiled_traffic(w.name) if cache is not None else None,
+                     "frac": achieved / peak,
+                     "traffic": profiled_traffic(w.name) if cache is not None and args.layout == "packed" else None,
                      "kernel": "rope_qk_tile_kernel<128,false>",
                      "algorithmic_bytes_per_launch": bytes_per_pass,
                      "avg_launch_us": avg_launch_s * 1e6, "peak_kind": peak_kind + " (hbm_gbs)"},
@@ -485,7 +528,7 @@ def run_ours(args, rank, world, local):
     return 0
 
 
-def end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev):
+def end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev, used=None):
     """Same metric through the public host-buffer call (rope_qk_host) with the inputs in
     pinned host memory: every step streams Q, K (forward) and dQ, dK (backward) from the
     host through a device workspace in chunks and back, copies overlapped with the
@@ -501,9 +544,9 @@ def end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev):
 
     def step():
         pr.rope_qk_host(host[0], host[1], w.theta, ws, cu_seqlens=cu, cos_sin_cache=cache,
-                        q_out=work[0], k_out=work[1])
+                        q_out=work[0], k_out=work[1], seq_used=used)
         pr.rope_qk_host(host[2], host[3], w.theta, ws, cu_seqlens=cu, cos_sin_cache=cache, backward=True,
-                        q_out=work[2], k_out=work[3])
+                        q_out=work[2], k_out=work[3], seq_used=used)
 
     for _ in range(2):
         step()

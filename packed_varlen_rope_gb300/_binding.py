@@ -400,13 +400,14 @@ def glu_bwd(kind: str, dh, e, g, de=None, dg=None, stream=None):
 
 def rope_qk_host(q, k, theta: float, workspace=None, cu_seqlens=None, position_ids=None, backward: bool = False,
                  q_out=None, k_out=None, token_offset: int = 0, position_scale: float = 1.0,
-                 cos_sin_cache=None, stream=None, device=None):
+                 cos_sin_cache=None, stream=None, device=None, seq_used=None):
     """Rotate Q [T, Hq, d] and K [T, Hkv, d] that live in HOST memory (contiguous bf16 CPU
     tensors, pinned for overlapped copies), streaming them through ``workspace`` (a
     CUDA tensor of any dtype used as raw staging memory).  Without a workspace the
     library's built-in 32 MiB staging array is used and nothing is allocated
     (``rope_qk_host_static``; ``device`` then names the GPU).  cu_seqlens /
-    position_ids / cos_sin_cache are CUDA tensors.  Asynchronous on ``stream``:
+    position_ids / cos_sin_cache / seq_used (with cu_seqlens: the used tokens of each
+    sample of a padded batch) are CUDA tensors.  Asynchronous on ``stream``:
     synchronise it before reading the results.  Returns (q, k) or (q_out, k_out)."""
     import torch
 
@@ -445,6 +446,11 @@ def rope_qk_host(q, k, theta: float, workspace=None, cu_seqlens=None, position_i
     elif cu_seqlens is not None:
         _check_cu(cu_seqlens, dev)
         desc.cu_seqlens, desc.n_seqs = _ptr(cu_seqlens), cu_seqlens.numel() - 1
+        if seq_used is not None:
+            _check_cu(seq_used, dev)
+            if seq_used.numel() != desc.n_seqs:
+                raise ValueError("seq_used must hold one int32 per sample")
+            desc.seq_used = _ptr(seq_used)
     else:
         raise ValueError("give cu_seqlens or position_ids")
     desc.n_q_heads, desc.n_kv_heads, desc.head_dim = hq, k.shape[1], d

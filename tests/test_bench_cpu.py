@@ -45,3 +45,17 @@ def test_all_core_oracle_timing_runs_every_range():
     r = bench.cpu_all_cores(w, pos, q, k, dq, dk, seconds=0.05)
     assert r["cores"] >= 1 and r["value"] > 0 and r["kind"] == "oracle"
     assert "%d token ranges" % r["cores"] in r["sample"]
+
+
+def test_padding_waste_algebra():
+    """The padded Llama-3-8B batch: valid fraction = sum of the sample lengths over
+    8 x 2048 rows; a pack wastes nothing."""
+    from packed_varlen_rope_gb300 import workloads as wl
+
+    w = wl.WORKLOADS[3]
+    padded, packed = wl.make_pack(w, "padded"), wl.make_pack(w, "packed")
+    assert padded.lengths == packed.lengths and padded.total_tokens == 8 * 2048
+    assert bench.valid_fraction(padded) == sum(padded.lengths) / (8 * 2048)
+    assert int(padded.valid_mask.sum()) == sum(padded.lengths) == packed.total_tokens
+    assert bench.valid_fraction(packed) == 1.0
+    assert 0.4 < bench.valid_fraction(padded) < 0.6          # U[64, 2048] samples: about half wasted

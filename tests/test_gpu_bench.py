@@ -52,3 +52,14 @@ def test_rope_bench_line_small():
         assert key in d, key
     assert d["parity"]["bit_mismatch"] == 0 and d["gpu_launches"] == 40
     assert d["e2e"]["h2d_bytes_per_step"] == d["e2e"]["d2h_bytes_per_step"] > 0
+
+
+@pytest.mark.parametrize("layout", ["padded", "padded-seq-used"])
+def test_rope_bench_padded_layouts(layout):
+    """The padded Llama-3-8B batch through the bench: every row rotated, or the pad rows
+    skipped with seq_used; the oracle parity block and the valid fraction are reported."""
+    d = _bench("--workload", "3", "--layout", layout, "--steps", "20", "--warmup", "3", "--e2e-steps", "2",
+               "--cpu-seconds", "1")
+    assert d["parity"]["bit_mismatch"] == 0 and 0.4 < d["config"]["valid_fraction"] < 0.6
+    rows = 16384 if layout == "padded" else d["config"]["valid_tokens"]
+    assert d["roofline"]["algorithmic_bytes_per_launch"] == 4 * 40 * 128 * rows

@@ -28,7 +28,8 @@
  *
  * Layout.  Each matrix is bf16 [rows][cols] with cols contiguous and a row stride in
  * elements (a multiple of 8; when rows > 1, at least cols and below cols + 2^31); cols
- * is a multiple of 8; pointers are 16-byte aligned; rows * cols / 8 < 2^31.  The gate and up halves of one fused
+ * is a multiple of 8; pointers are 16-byte aligned; rows * cols / 8 < 2^31; each
+ * matrix spans (rows - 1) * stride + cols < 2^56 elements.  The gate and up halves of one fused
  * [rows, 2*I] projection output are views with row stride 2*I.
  *
  * Aliasing.  An output may be exactly one of the inputs (same pointer and stride): it

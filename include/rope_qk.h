@@ -125,7 +125,9 @@ int rope_qk_bwd(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs,
  *
  * Views.  Each of q, k, q_out, k_out is a bf16 [total_tokens, heads, head_dim] view with
  * head_dim contiguous and element strides for tokens and heads (multiples of 8, >= 0;
- * pointers 16-byte aligned).  No two (token, head) rows of one view may share an
+ * pointers 16-byte aligned; the view's span, (tokens - 1) * token stride + (heads - 1)
+ * * head stride + head_dim, below 2^56 elements, else ROPE_ERR_SHAPE).  No two (token,
+ * head) rows of one view may share an
  * element (else ROPE_ERR_OVERLAP).  Q and K must share no element: either their address
  * ranges are disjoint, or they step tokens by the same stride and each token's Q block
  * and K block are disjoint -- the Q and K slices of one fused QKV projection output,

@@ -416,6 +416,9 @@ int check_mats(const Mat *m, int n, int64_t rows, int64_t cols)
         if (m[i].p == nullptr) return ROPE_ERR_NULL;
         if (!aligned16(m[i].p) || m[i].stride % 8 != 0) return ROPE_ERR_ALIGN;
         if (rows > 1 && (m[i].stride < cols || m[i].stride - cols >= (int64_t(1) << 31))) return ROPE_ERR_SHAPE;
+        // span (rows - 1) * stride + cols below 2^56 elements, computed without wrapping
+        if (static_cast<__int128>(rows - 1) * m[i].stride + cols >= (static_cast<__int128>(1) << 56))
+            return ROPE_ERR_SHAPE;
     }
     return ROPE_OK;
 }

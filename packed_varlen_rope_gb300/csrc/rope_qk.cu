@@ -431,11 +431,19 @@ bool views_disjoint(const View &a, const View &b)
     return r >= ea && r + eb <= S;
 }
 
+// The view's span in elements, computed without wrapping, stays below 2^56 (so that
+// the int64 span, byte counts and overlap tests below cannot overflow).
+bool span_fits(const View &v)
+{
+    const __int128 span = static_cast<__int128>(v.rows - 1) * v.ts + static_cast<__int128>(v.heads - 1) * v.hs + v.d;
+    return span < (static_cast<__int128>(1) << 56);
+}
+
 int check_view(const View &v)
 {
     if (v.base == nullptr) return ROPE_ERR_NULL;
     if (!aligned(v.base, 16) || v.ts % 8 != 0 || v.hs % 8 != 0) return ROPE_ERR_ALIGN;
-    if (v.ts < 0 || v.hs < 0) return ROPE_ERR_SHAPE;
+    if (v.ts < 0 || v.hs < 0 || !span_fits(v)) return ROPE_ERR_SHAPE;
     if (!view_injective(v)) return ROPE_ERR_OVERLAP;
     return ROPE_OK;
 }

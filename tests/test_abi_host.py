@@ -202,6 +202,8 @@ def test_apply_argument_checks(lib):
     assert a(q_stride_head=56) == ERR_OVERLAP                       # heads overlap (stride < d)
     assert a(q_stride_token=128) == ERR_OVERLAP                     # tokens overlap the 4 heads
     assert a(q_stride_token=-256) == ERR_SHAPE
+    assert a(q_stride_token=1 << 60) == ERR_SHAPE                   # span would overflow int64 bytes
+    assert a(k_stride_head=1 << 58, hkv=2) == ERR_SHAPE
     # fused QKV buffer: Q and K slices may interleave, but not share elements
     S = (4 + 2 * 2) * 64
     assert a(q_stride_token=S, k=Q + 3 * 64 * 2, k_stride_token=S) == ERR_OVERLAP   # K starts inside Q
@@ -223,6 +225,7 @@ def test_glu_argument_checks(lib):
     assert f(rows=1 << 20, cols=1 << 14) == ERR_SHAPE                      # units >= 2^31
     assert f(es=64 + (1 << 31)) == ERR_SHAPE                               # stride - cols >= 2^31
     assert f(es=64 + (1 << 31), rows=1) != ERR_SHAPE                       # one row: stride unused
+    assert f(rows=1 << 28, cols=8, es=1 << 31, gs=8, hs=8) == ERR_SHAPE     # span 2^59 elements
     assert f(e=None) == ERR_NULL and f(h=None) == ERR_NULL
     assert f(e=E + 8) == ERR_ALIGN and f(gs=68) == ERR_ALIGN
     assert f(h=E + 64) == ERR_OVERLAP                                      # partial overlap

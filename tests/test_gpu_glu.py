@@ -209,3 +209,36 @@ def test_glu_long_1m_by_9728(dev):
     _fwd_bwd_check("swiglu", eb, gb, dhb, h[pick_dev], e[pick_dev], g[pick_dev], "1M x 9728")
     for store in (es, gs, ds, hs):
         assert torch.all(store[n:] == 6.5)
+
+
+@pytest.mark.parametrize("padded", ["e", "g", "h", "dh", "de", "dg"])
+def test_glu_one_padded_matrix(dev, padded):
+    """Exactly one matrix has a row stride wider than its rows (the others are
+    contiguous), so each address term of the padded kernels is exercised on its own;
+    the gaps between that matrix's rows keep their canaries."""
+    rows, cols, stride = 37, 72, 72 + 24
+    rng = np.random.Generator(np.random.PCG64(60 + ["e", "g", "h", "dh", "de", "dg"].index(padded)))
+    eb, gb, dhb = (_bits(rng, (rows, cols), 2.0) for _ in range(3))
+    store = {}
+
+    def mat(name, bits=None):
+        if name != padded:
+            t = torch.empty((rows, cols), dtype=torch.bfloat16, device=dev)
+        else:
+            buf = torch.full((rows * stride,), 6.5, dtype=torch.bfloat16, device=dev)
+            store[name] = buf
+            t = buf.as_strided((rows, cols), (stride, 1))
+        if bits is not None:
+            t.copy_(from_bits(bits, dev))
+        return t
+
+    for kind in KINDS:
+        store.clear()
+        e, g, dh = mat("e", eb), mat("g", gb), mat("dh", dhb)
+        h, de, dg = mat("h"), mat("de"), mat("dg")
+        pr().glu_fwd(kind, e, g, h)
+        pr().glu_bwd(kind, dh, e, g, de, dg)
+        torch.cuda.synchronize()
+        _fwd_bwd_check(kind, eb, gb, dhb, h.clone(), de.clone(), dg.clone(), (kind, padded))
+        gaps = store[padded].view(rows, stride)[:, cols:]
+        assert torch.all(gaps == 6.5), (kind, padded)

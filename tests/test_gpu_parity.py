@@ -495,3 +495,24 @@ def test_rotary_embedding_module(dev):
     expect = pr().rope_qk_bwd(ones.clone(), ones[:, :1].clone(), torch.tensor([0, 64], dtype=torch.int32,
                                                                                device=dev), w2.theta)
     assert torch.equal(ql.grad, expect[0]) and torch.equal(kl.grad, expect[1])
+
+
+def test_rotary_embedding_int64_position_ids(dev):
+    """RotaryEmbedding with int64 position ids (a Hugging Face collator's dtype), forward
+    and autograd backward, against the oracle on the same positions."""
+    from packed_varlen_rope_gb300 import RotaryEmbedding
+
+    w, pack, q, k, dq, dk = _workload_inputs(1)
+    pos = oracle.positions(pack.cu_seqlens, pack.total_tokens).astype(np.int64)
+    ids = torch.from_numpy(pos).to(dev)
+    rope = RotaryEmbedding(w.head_dim, w.theta)
+    q0, k0, g_q, g_k = (to_bits(t) for t in (q, k, dq, dk))
+    qleaf = torch.zeros_like(q, requires_grad=True)
+    kleaf = torch.zeros_like(k, requires_grad=True)
+    yq, yk = rope(qleaf + q, kleaf + k, position_ids=ids)
+    torch.autograd.backward([yq, yk], [dq, dk])
+    p32 = pos.astype(np.int32)
+    assert np.array_equal(to_bits(yq), oracle.rope_rows(q0, p32, w.theta))
+    assert np.array_equal(to_bits(yk), oracle.rope_rows(k0, p32, w.theta))
+    assert np.array_equal(to_bits(qleaf.grad), oracle.rope_rows(g_q, p32, w.theta, bwd=True))
+    assert np.array_equal(to_bits(kleaf.grad), oracle.rope_rows(g_k, p32, w.theta, bwd=True))

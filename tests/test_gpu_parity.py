@@ -137,6 +137,32 @@ def test_cache_large_positions(dev):
     assert mism == 0
 
 
+def test_cache_every_position_matches_oracle(dev):
+    """All 2^20 x 64 (cos, sin) pairs of the cache the 1M-token workload uses, against
+    the oracle's binary64-then-round values: identical bits everywhere.  The oracle runs
+    over position ranges on every host core (its C calls release the GIL)."""
+    import concurrent.futures as cf
+    import ctypes
+    import os
+
+    theta, d, rows = 1.0e6, 128, 1 << 20
+    got = pr()._binding.cache_as_cos_sin(pr().new_cos_sin_cache(rows, d, theta, device=dev).cpu().numpy())
+    ref_c = np.empty((rows, d // 2), np.float32)
+    ref_s = np.empty((rows, d // 2), np.float32)
+    fn = oracle.get().lib.oracle_cos_sin_scaled
+    fp = ctypes.POINTER(ctypes.c_float)
+
+    def part(lo, hi):
+        for p in range(lo, hi):
+            fn(p, theta, d, 1.0, ref_c[p].ctypes.data_as(fp), ref_s[p].ctypes.data_as(fp))
+
+    n = len(os.sched_getaffinity(0))
+    bounds = np.linspace(0, rows, n + 1).astype(int)
+    with cf.ThreadPoolExecutor(n) as ex:
+        list(ex.map(lambda i: part(bounds[i], bounds[i + 1]), range(n)))
+    assert np.array_equal(got[:, :, 0], ref_c) and np.array_equal(got[:, :, 1], ref_s)
+
+
 # ------------------------------------------------------------------ workloads 1-4
 
 def _workload_inputs(idx, layout="packed"):

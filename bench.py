@@ -15,6 +15,19 @@ Prints one JSON line (rank 0).  Under torchrun each rank rotates its own pack (w
 scaling, no collective on the data path); the value is the tokens of all ranks over
 the slowest rank's time.  ``--impl reference`` times the CPU oracle on the host cores
 instead (bounded samples of the same workload).
+
+Other measurements of the same library:
+
+    --workload N                 another seeded workload (1-5)
+    --layout padded|padded-seq-used
+                                 the padded batch of workload 3, every row rotated or
+                                 the pad rows skipped (value = valid tokens per second)
+    --no-cache                   cos/sin evaluated per tile instead of read from a cache
+    --path rope-forms            the forward through every input form (fused QKV,
+                                 head-major, out of place, position ids, CP shards, no
+                                 cache, rescale), each checked bit for bit
+    --path glu                   SwiGLU / GeGLU forward + backward (--glu-workload,
+                                 --glu-kind)
 """
 from __future__ import annotations
 

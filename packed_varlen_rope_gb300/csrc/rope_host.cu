@@ -13,6 +13,9 @@
 
 #include "rope_qk.h"
 
+// rope_qk_apply with plain (not programmatically overlapped) launches (rope_qk.cu).
+int rope_qk_apply_plain_launch(const rope_qk_desc *desc, void *stream);
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -154,7 +157,7 @@ int rope_qk_host_impl(const rope_qk_desc *dp, void *workspace, int64_t workspace
         cd.total_tokens = n;
         if (p.position_ids != nullptr) cd.position_ids = ids_from(p, t0);
         else cd.token_offset = p.token_offset + t0;
-        rc = rope_qk_apply(&cd, stream);
+        rc = rope_qk_apply_plain_launch(&cd, stream);
         if (rc != ROPE_OK) {
             join();
             return rc;
@@ -259,7 +262,7 @@ extern "C" int rope_qk_host_static(const rope_qk_desc *desc, void *stream)
         cd.total_tokens = n;
         if (p.position_ids != nullptr) cd.position_ids = ids_from(p, t0);
         else cd.token_offset = p.token_offset + t0;
-        const int rc = rope_qk_apply(&cd, stream);
+        const int rc = rope_qk_apply_plain_launch(&cd, stream);
         if (rc != ROPE_OK) return rc;
         if (cudaMemcpyAsync(qo_host + t0 * q_row, dq, n * q_row, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
             cudaMemcpyAsync(ko_host + t0 * k_row, dk, n * k_row, cudaMemcpyDeviceToHost, s) != cudaSuccess)

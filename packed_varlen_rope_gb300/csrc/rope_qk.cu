@@ -184,6 +184,13 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
         }
     };
 
+    // Programmatic dependent launch: the grid may be scheduled while the kernel before
+    // it in the stream drains; nothing is read before that kernel has completed and its
+    // writes are visible, and the next launch may be scheduled from here on (a no-op
+    // for a plain launch).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     // 1. positions of the tile's tokens (one lane per token): from the caller's
     //    position ids, else by binary search of cu_seqlens in the global token stream
     if (threadIdx.x < kMaxTileTokens) {
@@ -372,21 +379,39 @@ int pick_tile_tokens(int h_tot, int head_dim)
     return tt;
 }
 
+// With `pdl`, the launch carries the programmatic-stream-serialisation attribute:
+// its CTAs may be scheduled while the previous kernel in the stream finishes (they wait
+// for it before reading anything), which hides the launch gap between back-to-back
+// rotations (measured: fwd+bwd step -0.7 % on 65,536 tokens, -4 % on 16,384, -9 % on
+// 7,714).
 template <int D, bool LONG>
-cudaError_t launch_tile(const RopeArgs &a, int grid, size_t smem, cudaStream_t stream)
+cudaError_t launch_tile(const RopeArgs &a, int grid, size_t smem, cudaStream_t stream, bool pdl)
 {
-    rope_qk_tile_kernel<D, LONG><<<grid, kThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    if (!pdl) {
+        rope_qk_tile_kernel<D, LONG><<<grid, kThreads, smem, stream>>>(a);
+        return cudaGetLastError();
+    }
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, rope_qk_tile_kernel<D, LONG>, a);
 }
 
 template <bool LONG>
-cudaError_t dispatch_dim(const RopeArgs &a, int grid, size_t smem, cudaStream_t stream)
+cudaError_t dispatch_dim(const RopeArgs &a, int grid, size_t smem, cudaStream_t stream, bool pdl)
 {
     switch (a.head_dim) {
-    case 64: return launch_tile<64, LONG>(a, grid, smem, stream);
-    case 128: return launch_tile<128, LONG>(a, grid, smem, stream);
-    case 256: return launch_tile<256, LONG>(a, grid, smem, stream);
-    default: return launch_tile<0, LONG>(a, grid, smem, stream);
+    case 64: return launch_tile<64, LONG>(a, grid, smem, stream, pdl);
+    case 128: return launch_tile<128, LONG>(a, grid, smem, stream, pdl);
+    case 256: return launch_tile<256, LONG>(a, grid, smem, stream, pdl);
+    default: return launch_tile<0, LONG>(a, grid, smem, stream, pdl);
     }
 }
 
@@ -448,7 +473,7 @@ int check_view(const View &v)
     return ROPE_OK;
 }
 
-int rope_qk_apply_impl(const rope_qk_desc *dp, void *stream)
+int rope_qk_apply_impl(const rope_qk_desc *dp, void *stream, bool pdl)
 {
     if (dp == nullptr) return ROPE_ERR_NULL;
     const rope_qk_desc &p = *dp;
@@ -523,8 +548,8 @@ int rope_qk_apply_impl(const rope_qk_desc *dp, void *stream)
     for (const View *v : {&q, &k, &qo, &ko})
         long_index = long_index || v->span_elems() > INT32_MAX;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const cudaError_t err = long_index ? dispatch_dim<true>(a, grid, smem, s)
-                                       : dispatch_dim<false>(a, grid, smem, s);
+    const cudaError_t err = long_index ? dispatch_dim<true>(a, grid, smem, s, pdl)
+                                       : dispatch_dim<false>(a, grid, smem, s, pdl);
     return err == cudaSuccess ? ROPE_OK : ROPE_ERR_LAUNCH;
 }
 
@@ -558,10 +583,17 @@ int rope_qk_run(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs, int
     p.position_scale = 1.0;
     p.cos_sin_cache = cache;
     p.cache_rows = cache_rows;
-    return rope_qk_apply_impl(&p, stream);
+    return rope_qk_apply_impl(&p, stream, true);
 }
 
 }  // namespace
+
+// rope_qk_apply with plain launches, for the host-buffer pipeline (its rotations follow
+// cross-stream event waits, where an overlapped launch has nothing to hide).
+int rope_qk_apply_plain_launch(const rope_qk_desc *desc, void *stream)
+{
+    return rope_qk_apply_impl(desc, stream, false);
+}
 
 extern "C" {
 
@@ -620,7 +652,7 @@ int rope_cos_sin_cache_build(float *cache, int64_t cache_rows, int32_t head_dim,
 
 int rope_qk_apply(const rope_qk_desc *desc, void *stream)
 {
-    return rope_qk_apply_impl(desc, stream);
+    return rope_qk_apply_impl(desc, stream, true);
 }
 
 int rope_qk_positions(const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_tokens,

@@ -542,3 +542,34 @@ def test_rotary_embedding_int64_position_ids(dev):
     assert np.array_equal(to_bits(yk), oracle.rope_rows(k0, p32, w.theta))
     assert np.array_equal(to_bits(qleaf.grad), oracle.rope_rows(g_q, p32, w.theta, bwd=True))
     assert np.array_equal(to_bits(kleaf.grad), oracle.rope_rows(g_k, p32, w.theta, bwd=True))
+
+
+def test_back_to_back_launches_see_previous_writes(dev):
+    """Rotations are launched so that they may be scheduled while the previous kernel in
+    the stream drains (programmatic dependent launch); they must still see everything
+    that kernel wrote.  Q and K are rewritten right before each rotation by a torch
+    conversion kernel, by a device copy, or by the previous rotation itself, 30 times in
+    a row, and every result equals the oracle."""
+    w, pack, q, k, dq, dk = _workload_inputs(2)
+    cu = torch.from_numpy(pack.cu_seqlens).to(dev)
+    cache = pr().new_cos_sin_cache(max(pack.lengths), w.head_dim, w.theta, device=dev)
+    q0, k0 = to_bits(q), to_bits(k)
+    once_q = oracle.rope_packed(q0, pack.cu_seqlens, w.theta)
+    once_k = oracle.rope_packed(k0, pack.cu_seqlens, w.theta)
+    twice_q = oracle.rope_packed(once_q, pack.cu_seqlens, w.theta)
+    twice_k = oracle.rope_packed(once_k, pack.cu_seqlens, w.theta)
+    qf, kf = q.float(), k.float()                    # exact: bf16 -> fp32 -> bf16
+    qa, ka = torch.empty_like(q), torch.empty_like(k)
+    for i in range(30):
+        if i % 3 == 0:
+            qa.copy_(qf)                             # conversion kernel
+            ka.copy_(kf)
+        else:
+            qa.copy_(q)                              # same-dtype device copy
+            ka.copy_(k)
+        pr().rope_qk_fwd(qa, ka, cu, w.theta, cos_sin_cache=cache)
+        if i % 2 == 1:
+            pr().rope_qk_fwd(qa, ka, cu, w.theta, cos_sin_cache=cache)    # reads the previous rotation
+        torch.cuda.synchronize()
+        want_q, want_k = (twice_q, twice_k) if i % 2 == 1 else (once_q, once_k)
+        assert np.array_equal(to_bits(qa), want_q) and np.array_equal(to_bits(ka), want_k), i

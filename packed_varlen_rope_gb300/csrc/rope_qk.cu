@@ -409,6 +409,7 @@ cudaError_t dispatch_dim(const RopeArgs &a, int grid, size_t smem, cudaStream_t 
 {
     switch (a.head_dim) {
     case 64: return launch_tile<64, LONG>(a, grid, smem, stream, pdl);
+    case 96: return launch_tile<96, LONG>(a, grid, smem, stream, pdl);
     case 128: return launch_tile<128, LONG>(a, grid, smem, stream, pdl);
     case 256: return launch_tile<256, LONG>(a, grid, smem, stream, pdl);
     default: return launch_tile<0, LONG>(a, grid, smem, stream, pdl);

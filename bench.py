@@ -574,11 +574,33 @@ def end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev, u
     torch.cuda.synchronize()
     steps_ms = [marks[i].elapsed_time(marks[i + 1]) for i in range(E)]
     ms = max_over_ranks(marks[0].elapsed_time(marks[E]) / E, world, dev)
+
+    # The same step captured once in a CUDA graph and replayed: whole steps are queued
+    # ahead, so a pause of the host thread (the host is shared) does not leave the GPU
+    # idle; every replay still copies the inputs in from and the results out to pinned
+    # host memory.
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    graph.replay()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    g0.record(stream)
+    for _ in range(E):
+        graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    gms = max_over_ranks(g0.elapsed_time(g1) / E, world, dev)
     return {"value": whole_job_tokens_per_s(world, pack.valid_tokens, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": h2d, "ms_per_step": ms, "steps": E,
             "step_ms_min": min(steps_ms), "step_ms_median": statistics.median(steps_ms),
             "step_ms_max": max(steps_ms), "step_ms_max_index": steps_ms.index(max(steps_ms)),
-            "path": "rope_qk_host: pinned host buffers streamed in %d-token chunks" % chunk}
+            "path": "rope_qk_host: pinned host buffers streamed in %d-token chunks" % chunk,
+            "graph_replay": {"value": whole_job_tokens_per_s(world, pack.valid_tokens, gms), "ms_per_step": gms,
+                             "steps": E, "path": "the same rope_qk_host calls captured in one CUDA graph"}}
 
 
 def run_glu(args, rank, world, local):

@@ -20,6 +20,11 @@
 // Every floating-point step is an explicit round-to-nearest intrinsic so that the
 // compiler cannot contract a multiply and an add; results are bit-identical to a plain
 // sequential evaluation of the same steps on a CPU.
+//
+// Launches use programmatic dependent launch: a grid may be scheduled while the
+// previous kernel in its stream drains, and its first instruction waits for that
+// kernel to complete, so back-to-back rotations lose no launch gap and nothing is read
+// early.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

@@ -288,12 +288,19 @@ def pin_position_scale(o) -> None:
 
     rng = np.random.Generator(np.random.PCG64(20))
     x = random_bf16_bits(rng, (4, 3, 128))
-    # TRL "training beyond 1M tokens", YaRN section: factor 4, 100,000 -> 25,000 and
-    # 163,840 -> 40,960 (power-of-two factor: identical bits)
+    # the page's worked example (tests/golden/position_rescale.txt: TRL "training
+    # beyond 1M tokens", YaRN section); a power-of-two factor gives identical bits
+    rows = [tuple(int(v) for v in line.split()) for line in
+            open(os.path.join(GOLDEN, "position_rescale.txt")) if line.strip() and not line.startswith("#")]
+    assert rows and all(f == 163840 // 40960 for f, _, _ in rows)
+    for factor, pos, rescaled in rows:
+        assert pos == rescaled * factor
+    positions = np.array([p for _, p, _ in rows] + [4, 0], np.int32)
+    expected = np.array([r for _, _, r in rows] + [1, 0], np.int32)
     for theta in (1.0e6, 1.0e4):
         for bwd in (False, True):
-            scaled = o.rope_rows(x, np.array([100000, 163840, 4, 0], np.int32), theta, bwd=bwd, scale=4.0)
-            plain = o.rope_rows(x, np.array([25000, 40960, 1, 0], np.int32), theta, bwd=bwd)
+            scaled = o.rope_rows(x, positions, theta, bwd=bwd, scale=float(rows[0][0]))
+            plain = o.rope_rows(x, expected, theta, bwd=bwd)
             assert np.array_equal(scaled, plain)
     # frequencies divided by the scale: exact for powers of two ...
     for d in (8, 64, 128):

@@ -125,11 +125,17 @@ class RotaryEmbedding:
             self._caches[device] = cur
         return cur
 
-    def __call__(self, q, k, cu_seqlens=None, position_ids=None, token_offset: int = 0):
+    def __call__(self, q, k, cu_seqlens=None, position_ids=None, token_offset: int = 0,
+                 max_position: int = 0):
+        """Rotate q and k in place (differentiable).  ``max_position``: an upper bound on
+        the position ids, for ids that exceed the row count (a context-parallel shard
+        of a long sequence carrying global ids); without it the cache covers ``T``
+        rows and larger ids are evaluated on the fly."""
         if q.shape[-1] != self.head_dim:
             raise ValueError("q and k must have head_dim %d" % self.head_dim)
         T = q.shape[0]
         rows = T if position_ids is not None else int(token_offset) + T
+        rows = max(rows, int(max_position) + 1 if max_position else 0)
         cache = self.cache(q.device, max(rows, 1))
         return apply_rope_qk(q, k, cu_seqlens, self.theta, cos_sin_cache=cache, position_ids=position_ids,
                              token_offset=token_offset, position_scale=self.position_scale)

@@ -542,6 +542,12 @@ def test_rotary_embedding_int64_position_ids(dev):
     assert np.array_equal(to_bits(yk), oracle.rope_rows(k0, p32, w.theta))
     assert np.array_equal(to_bits(qleaf.grad), oracle.rope_rows(g_q, p32, w.theta, bwd=True))
     assert np.array_equal(to_bits(kleaf.grad), oracle.rope_rows(g_k, p32, w.theta, bwd=True))
+    # global ids of a shard beyond its row count: the max_position hint sizes the cache
+    big = torch.from_numpy(pos + 100_000).to(dev)
+    qb = q.clone()
+    rope(qb, k.clone(), position_ids=big, max_position=100_000 + int(pos.max()))
+    assert rope.cache(dev, 1).shape[0] >= 100_000 + int(pos.max()) + 1
+    assert np.array_equal(to_bits(qb), oracle.rope_rows(q0, (pos + 100_000).astype(np.int32), w.theta))
 
 
 def test_back_to_back_launches_see_previous_writes(dev):

@@ -178,7 +178,8 @@ def test_glu_wide_row_stride(dev):
     assert torch.all(gap == 6.5) and torch.all(store[stride + 3 * cols:2 * stride] == 6.5)
 
 
-def test_glu_long_1m_by_9728(dev):
+@pytest.mark.parametrize("kind", KINDS)
+def test_glu_long_1m_by_9728(dev, kind):
     """1,048,576 tokens x 9,728 (the TRL page's MLP width at 1M tokens): every matrix
     spans 10.2e9 elements, so addresses pass 2^32 and 2^33 bytes.  Sampled rows, including
     those around element offset 2^31 and 2^32, against the oracle; canaries after the
@@ -203,10 +204,10 @@ def test_glu_long_1m_by_9728(dev):
                                                                  (1 << 32) // cols, (1 << 32) // cols + 1]]))
     pick_dev = torch.from_numpy(pick).to(dev)
     eb, gb, dhb = (to_bits(t[pick_dev]) for t in (e, g, dh))
-    pr().glu_fwd("swiglu", e, g, h)
-    pr().glu_bwd("swiglu", dh, e, g, de=e, dg=g)
+    pr().glu_fwd(kind, e, g, h)
+    pr().glu_bwd(kind, dh, e, g, de=e, dg=g)
     torch.cuda.synchronize()
-    _fwd_bwd_check("swiglu", eb, gb, dhb, h[pick_dev], e[pick_dev], g[pick_dev], "1M x 9728")
+    _fwd_bwd_check(kind, eb, gb, dhb, h[pick_dev], e[pick_dev], g[pick_dev], (kind, "1M x 9728"))
     for store in (es, gs, ds, hs):
         assert torch.all(store[n:] == 6.5)
 

@@ -311,12 +311,16 @@ def cpu_baseline(args, w, pack, q_sample, k_sample, dq_sample, dk_sample, skip_p
     n = int(max(cal, min(n_all, args.cpu_seconds / per_token)))
     t = time.perf_counter()
     outputs = run(n)
+    passes = 1
+    while time.perf_counter() - t < 0.9 * args.cpu_seconds:   # the whole sample is quick: repeat it
+        run(n)
+        passes += 1
     el = time.perf_counter() - t
     valid = n if pack.valid_mask is None else int(np.count_nonzero(pack.valid_mask[:n]))
-    return {"value": valid / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": "first %d rows (%d tokens) of the %s batch, fwd+bwd of Q and K, %.1f s on one host core"
-                      % (n, valid, w.name, el)}, outputs, cpu_all_cores(w, pos[:n], q_sample[:n], k_sample[:n],
-                                                                         dq_sample[:n], dk_sample[:n], valid=valid)
+    return {"value": passes * valid / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "first %d rows (%d tokens) of the %s batch, fwd+bwd of Q and K, %d pass(es) in %.1f s on "
+                      "one host core" % (n, valid, w.name, passes, el)}, outputs, \
+        cpu_all_cores(w, pos[:n], q_sample[:n], k_sample[:n], dq_sample[:n], dk_sample[:n], valid=valid)
 
 
 def cpu_all_cores(w, pos, q, k, dq, dk, seconds=2.0, valid=None):

@@ -1,0 +1,123 @@
+"""Seeded random combinations of the rotation's options against the oracle (needs a
+GB300): pack lengths with empty samples, head counts and head_dim, contiguous / fused
+QKV / head-major views, in place or out of place, forward or backward, linear rescale,
+and positions from cu_seqlens (with a shard offset and optionally seq_used) or from
+int32 / int64 position ids with out-of-range values.  Every case must equal the oracle
+bit for bit; rows without a position stay unchanged (copied when out of place)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from parity_util import from_bits, to_bits
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+N_CASES = 60
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from packed_varlen_rope_gb300 import build
+
+    build.build()
+    oracle.build()
+    return torch.device("cuda:0")
+
+
+def _bits(rng, shape):
+    f = torch.from_numpy(rng.standard_normal(size=shape).astype(np.float32))
+    return f.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _views(buf_kind, T, hq, hkv, d, dev):
+    """q and k views of the requested layout over fresh device memory."""
+    if buf_kind == "contiguous":
+        return (torch.empty((T, hq, d), dtype=torch.bfloat16, device=dev),
+                torch.empty((T, hkv, d), dtype=torch.bfloat16, device=dev), None)
+    if buf_kind == "fused":
+        buf = torch.full((T, hq + 2 * hkv, d), 2.5, dtype=torch.bfloat16, device=dev)
+        return buf[:, :hq], buf[:, hq:hq + hkv], buf
+    qh = torch.empty((hq, T, d), dtype=torch.bfloat16, device=dev)
+    kh = torch.empty((hkv, T, d), dtype=torch.bfloat16, device=dev)
+    return qh.transpose(0, 1), kh.transpose(0, 1), None
+
+
+@pytest.mark.parametrize("case", range(N_CASES))
+def test_random_options_match_oracle(dev, case):
+    import packed_varlen_rope_gb300 as pr
+
+    rng = np.random.Generator(np.random.PCG64(9000 + case))
+    d = int(rng.integers(1, 17)) * 16
+    hq = int(rng.integers(1, 9))
+    hkv = int(rng.integers(1, hq + 1))
+    n_seqs = int(rng.integers(1, 9))
+    lengths = rng.integers(0, 200, size=n_seqs)
+    lengths[rng.random(n_seqs) < 0.2] = 0                                 # empty samples
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    pack_tokens = int(cu[-1])
+    theta = float(rng.choice([1.0e4, 5.0e5, 1.0e6]))
+    scale = float(rng.choice([1.0, 1.0, 4.0, 2.5]))
+    bwd = bool(rng.integers(0, 2))
+    in_place = bool(rng.integers(0, 2))
+    layout = str(rng.choice(["contiguous", "fused", "head_major"]))
+    source = str(rng.choice(["cu", "cu_offset", "cu_seq_used", "ids32", "ids64"]))
+
+    # rows of this call and their expected positions (-1: row left as it is)
+    if source in ("cu", "cu_seq_used"):
+        offset, T = 0, pack_tokens + int(rng.integers(0, 5))          # a few rows past the pack
+    elif source == "cu_offset":
+        offset = int(rng.integers(0, max(1, pack_tokens)))
+        T = int(rng.integers(1, max(2, pack_tokens - offset + 4)))
+    else:
+        offset, T = 0, int(rng.integers(1, 400))
+    T = max(T, 1)
+    kw = {}
+    if source.startswith("cu"):
+        full = oracle.positions(cu, max(pack_tokens, offset + T))
+        pos = full[offset:offset + T].astype(np.int32)
+        kw = {"cu_seqlens": torch.from_numpy(cu).to(dev), "token_offset": offset}
+        if source == "cu_seq_used":
+            used = np.array([int(rng.integers(0, L + 1)) for L in lengths], np.int32)
+            starts = cu[:-1]
+            g = np.arange(offset, offset + T)
+            s = np.searchsorted(cu[1:], g, side="right")                # sample of each row (if inside)
+            inside = pos >= 0
+            pos = np.where(inside & (pos < used[np.minimum(s, n_seqs - 1)]), pos, -1).astype(np.int32)
+            assert np.all(starts[np.minimum(s, n_seqs - 1)][inside] <= g[inside])
+            kw["seq_used"] = torch.from_numpy(used).to(dev)
+    else:
+        ids = rng.integers(-5, 1 << 24, size=T).astype(np.int64)
+        ids[rng.random(T) < 0.05] = (1 << 24) + 3
+        if source == "ids64":
+            ids[rng.random(T) < 0.05] = (1 << 40) + 7
+            kw = {"position_ids": torch.from_numpy(ids).to(dev)}
+            pos = np.where((ids >= 0) & (ids < (1 << 24)), ids, -1).astype(np.int32)
+        else:
+            ids32 = ids.astype(np.int32)
+            kw = {"position_ids": torch.from_numpy(ids32).to(dev)}
+            pos = np.where((ids32 >= 0) & (ids32 < (1 << 24)), ids32, -1).astype(np.int32)
+
+    qb, kb = _bits(rng, (T, hq, d)), _bits(rng, (T, hkv, d))
+    q, k, fused = _views(layout, T, hq, hkv, d, dev)
+    q.copy_(from_bits(qb, dev))
+    k.copy_(from_bits(kb, dev))
+    if in_place:
+        pr.rope_qk_apply(q, k, theta, backward=bwd, position_scale=scale, **kw)
+        qo, ko = q, k
+    else:
+        qo = torch.full((T, hq, d), 7.0, dtype=torch.bfloat16, device=dev)
+        ko = torch.full((T, hkv, d), 7.0, dtype=torch.bfloat16, device=dev)
+        pr.rope_qk_apply(q, k, theta, backward=bwd, position_scale=scale, q_out=qo, k_out=ko, **kw)
+    torch.cuda.synchronize()
+    what = (case, d, hq, hkv, layout, source, in_place, bwd, scale)
+    assert np.array_equal(to_bits(qo.contiguous()), oracle.rope_rows(qb, pos, theta, bwd, scale)), what
+    assert np.array_equal(to_bits(ko.contiguous()), oracle.rope_rows(kb, pos, theta, bwd, scale)), what
+    if not in_place:
+        assert np.array_equal(to_bits(q.contiguous()), qb) and np.array_equal(to_bits(k.contiguous()), kb), what
+    if fused is not None:
+        assert torch.all(fused[:, hq + hkv:] == 2.5), what                 # V untouched

@@ -16,15 +16,16 @@
  * elements (1,048,576 tokens x 9,728, the intermediate width the TRL page uses, spans
  * 1.0e10), and every address is formed in 64 bits.
  *
- * Arithmetic.  bf16 inputs are widened exactly; act and act' are evaluated in binary32
- * in forms without cancellation (1 - sigmoid(x) = sigmoid(-x), Phi(x) = erfc(-x/sqrt2)/2,
- * (1 + tanh u)/2 = sigmoid(2u)).  Exponentials and reciprocals come from the
- * special-function unit, and erfc from a fitted approximation (relative error < 4e-6
- * for |x| < 6.4, < 2e-5 up to |x| = 12.5), wherever the results stay normal numbers;
- * further out the accurate expf / erfcf.  Every result is rounded once to bf16 (nearest
- * even).  Results agree with a binary64 evaluation rounded once to bf16 within one bf16
- * unit in the last place, plus a few binary32 units of the magnitude of the terms
- * summed in act'.
+ * Arithmetic.  bf16 inputs are widened exactly; act and act' are evaluated in forms
+ * without cancellation (1 - sigmoid(x) = sigmoid(-x), Phi(x) = erfc(-x/sqrt2)/2,
+ * (1 + tanh u)/2 = sigmoid(2u)).  Where every intermediate stays a normal binary32
+ * number (|x| < 86 for SiLU, 12.5 for the erf form, 9.5 for the tanh form) they run in
+ * binary32, exponentials and reciprocals from the special-function unit and erfc from a
+ * fitted approximation (relative error < 4e-6 for |x| < 6.4, < 2e-5 up to 12.5);
+ * farther out, and for NaN, the element's act, act' and products are evaluated in
+ * binary64.  Every result is rounded once to bf16 (nearest even).  Results agree with a
+ * binary64 evaluation rounded once to bf16 within one bf16 unit in the last place, plus
+ * a few binary32 units of the magnitude of the terms summed in act'.
  *
  * Layout.  Each matrix is bf16 [rows][cols] with cols contiguous and a row stride in
  * elements (a multiple of 8; when rows > 1, at least cols and below cols + 2^31); cols

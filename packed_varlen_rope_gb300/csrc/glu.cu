@@ -32,8 +32,6 @@ using pvr::make_fastdiv;
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
 constexpr float kSqrt2OverPi = 0.797884560802865355879892f;  // sqrt(2/pi)
-constexpr float kInvSqrt2Pi = 0.398942280401432677939946f;   // 1/sqrt(2 pi)
-constexpr float kInvSqrt2 = 0.707106781186547524400844f;     // 1/sqrt(2)
 constexpr float kGeluTanhC = 0.044715f;
 
 struct GluArgs {
@@ -76,31 +74,17 @@ __device__ __forceinline__ float rcp_approx(float x)
     return y;
 }
 
-// How act and act' pick between the special-function path and the accurate one.
-constexpr int kCareful = 0;   // accurate functions only
-constexpr int kFast = 1;      // special-function path; the caller has checked the range
-constexpr int kGuarded = 2;   // decided element by element
-
 // sigmoid(y) and sigmoid(-y) from one exponential that cannot overflow: with
 // t = exp(-|y|) in (0, 1], sigmoid(|y|) = 1 / (1 + t) and sigmoid(-|y|) = t / (1 + t),
-// so far in the tails the small one keeps its (possibly subnormal) value instead of
-// collapsing to zero.  While |y| < 86 (exp(-|y|) >= 2^-124 is normal) 2^x and 1/x come
-// from the special-function unit, a few binary32 units against the bf16 rounding of
-// every result; beyond, the accurate expf and IEEE reciprocal.  kFast: the caller has
-// checked the range; kCareful: always the accurate functions; kGuarded: decided here,
-// element by element.
-template <int MODE>
+// so in the tails the small one keeps its value instead of collapsing to zero.  2^x and
+// 1/x come from the special-function unit, a few binary32 units against the bf16
+// rounding of every result; callers keep |y| < 86, where exp(-|y|) >= 2^-124 is a
+// normal number (farther out careful_outputs takes over).
 __device__ __forceinline__ void sigmoid_pair(float y, float &sp, float &sm)
 {
     const float ay = fabsf(y);
-    float t, big;
-    if (MODE == kFast || (MODE == kGuarded && ay < 86.0f)) {
-        t = ex2_approx(ay * -1.44269504088896340736f);   // -log2(e)
-        big = rcp_approx(1.0f + t);
-    } else {
-        t = expf(-ay);
-        big = __frcp_rn(1.0f + t);
-    }
+    const float t = ex2_approx(ay * -1.44269504088896340736f);   // -log2(e)
+    const float big = rcp_approx(1.0f + t);
     const float small = t * big;
     sp = y >= 0.0f ? big : small;
     sm = y >= 0.0f ? small : big;
@@ -119,57 +103,45 @@ constexpr float kLog2e = 1.44269504088896340736f;
 constexpr float kHalfInvSqrt2 = 0.353553390593273762200f;      // 1 / (2 sqrt 2): z/2 = |x| / (2 sqrt 2)
 constexpr float kLog2InvSqrt2Pi = -1.32574806473615929f;       // log2(1 / sqrt(2 pi))
 
-// Inputs below these magnitudes take the fast path of activation<KIND, true>: all
-// special-function results stay normal (SiLU: |x| < 86; tanh form: |2u| < 86 up to
-// |x| = 9.9; erf form: z = |x|/sqrt2 < 8.84).
+// Inputs below these magnitudes take the binary32 path, where every special-function
+// result stays normal (SiLU: |x| < 86; tanh form: |2u| < 86 up to |x| = 9.9; erf form:
+// z = |x|/sqrt2 < 8.84).  Elements at or beyond them, and NaN, go to careful_outputs.
 template <int KIND>
 __device__ __forceinline__ float fast_limit()
 {
     return KIND == GLU_SWIGLU ? 86.0f : (KIND == GLU_GEGLU ? 12.5f : 9.5f);
 }
 
-// act(x) and act'(x), in forms without cancellation in the tails (MODE as above; kFast
-// means |x| is below fast_limit<KIND>()).
-template <int KIND, int MODE>
+// act(x) and act'(x) in binary32 for |x| < fast_limit<KIND>(), in forms without
+// cancellation in the tails.
+template <int KIND>
 __device__ __forceinline__ void activation(float x, float &a, float &da)
 {
     if (KIND == GLU_SWIGLU) {
         float sp, sm;
-        sigmoid_pair<MODE>(x, sp, sm);
-        a = x * sp;
-        da = sp * (1.0f + x * sm);
+        sigmoid_pair(x, sp, sm);
+        a = __fmul_rn(x, sp);
+        da = __fmul_rn(sp, __fmaf_rn(x, sm, 1.0f));
     } else if (KIND == GLU_GEGLU) {
         // Phi(x) = erfc(-x/sqrt2)/2 and phi(x) = exp(-x^2/2)/sqrt(2 pi)
-        float Phi, phi;
-        if (MODE == kFast || (MODE == kGuarded && fabsf(x) < fast_limit<KIND>())) {
-            const float t = rcp_approx(fmaf(fabsf(x), kHalfInvSqrt2, 1.0f));
-            float p = kErfcFit[0];
+        const float t = rcp_approx(fmaf(fabsf(x), kHalfInvSqrt2, 1.0f));
+        float p = kErfcFit[0];
 #pragma unroll
-            for (int i = 1; i < 10; ++i) p = fmaf(p, t, kErfcFit[i]);
-            const float xx = x * x;
-            // erfc(|x|/sqrt2)/2 = t * 2^(P(t) log2 e - (log2 e / 2) x^2 - 1)
-            const float half_erfc = t * ex2_approx(fmaf(p, kLog2e, fmaf(-0.5f * kLog2e, xx, -1.0f)));
-            Phi = x >= 0.0f ? 1.0f - half_erfc : half_erfc;
-            phi = ex2_approx(fmaf(-0.5f * kLog2e, xx, kLog2InvSqrt2Pi));
-        } else {
-            Phi = 0.5f * erfcf(-x * kInvSqrt2);
-            phi = expf(-0.5f * x * x) * kInvSqrt2Pi;
-        }
+        for (int i = 1; i < 10; ++i) p = fmaf(p, t, kErfcFit[i]);
+        const float xx = x * x;
+        // erfc(|x|/sqrt2)/2 = t * 2^(P(t) log2 e - (log2 e / 2) x^2 - 1)
+        const float half_erfc = t * ex2_approx(fmaf(p, kLog2e, fmaf(-0.5f * kLog2e, xx, -1.0f)));
+        const float Phi = x >= 0.0f ? 1.0f - half_erfc : half_erfc;
+        const float phi = ex2_approx(fmaf(-0.5f * kLog2e, xx, kLog2InvSqrt2Pi));
         a = x * Phi;
         da = fmaf(x, phi, Phi);
     } else {
         const float u = kSqrt2OverPi * (x + kGeluTanhC * x * x * x);
         float sp, sm;
-        sigmoid_pair<MODE>(2.0f * u, sp, sm);
+        sigmoid_pair(2.0f * u, sp, sm);
         a = x * sp;
         const float w = sp * sm;
-        if (MODE == kFast) {
-            da = sp + 2.0f * x * w * kSqrt2OverPi * (1.0f + 3.0f * kGeluTanhC * x * x);
-        } else {
-            // the second term vanishes with sp * sm; test it first so that a huge |x|
-            // (where 1 + 3c x^2 overflows) gives 0, not 0 * inf
-            da = w == 0.0f ? sp : sp + 2.0f * x * w * kSqrt2OverPi * (1.0f + 3.0f * kGeluTanhC * x * x);
-        }
+        da = sp + 2.0f * x * w * kSqrt2OverPi * (1.0f + 3.0f * kGeluTanhC * x * x);
     }
 }
 
@@ -178,10 +150,10 @@ __device__ __forceinline__ void activation(float x, float &a, float &da)
 // pair code below gives the scalar code's results bit for bit at half the issue cost.
 __device__ __forceinline__ float2 splat(float v) { return make_float2(v, v); }
 
-// Fast-path act and act' of two elements at once (MODE == kFast: the caller has checked
-// |x| < fast_limit<KIND>() for both).  The erf form runs the same operations as
-// activation<GLU_GEGLU, kFast>, and SiLU as sigmoid_pair<kFast> with a = x sp,
-// da = sp (1 + x sm); the tanh form evaluates each element with the scalar code.
+// act and act' of two elements at once, for |x| < fast_limit<KIND>() (other inputs give
+// values that the caller replaces).  The erf form runs the same operations as
+// activation<GLU_GEGLU>, and SiLU as sigmoid_pair with a = x sp, da = sp (1 + x sm);
+// the tanh form evaluates each element with the scalar code.
 template <int KIND>
 __device__ __forceinline__ void activation_pair_fast(float2 x, float2 &a, float2 &da)
 {
@@ -213,8 +185,8 @@ __device__ __forceinline__ void activation_pair_fast(float2 x, float2 &a, float2
         a = __fmul2_rn(x, sp);
         da = __fmul2_rn(sp, __ffma2_rn(x, sm, splat(1.0f)));
     } else {
-        activation<KIND, kFast>(x.x, a.x, da.x);
-        activation<KIND, kFast>(x.y, a.y, da.y);
+        activation<KIND>(x.x, a.x, da.x);
+        activation<KIND>(x.y, a.y, da.y);
     }
 }
 
@@ -240,46 +212,62 @@ __device__ __forceinline__ uint32_t pack(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// act and act' on the careful path, out of line: a scalar in, a pair out, so nothing
-// of the caller's unit goes through memory, and the rarely taken accurate functions keep
-// their registers off the fast path.
-template <int KIND>
-__device__ __noinline__ float2 activation_careful(float x)
-{
-    float a, da;
-    activation<KIND, kCareful>(x, a, da);
-    return make_float2(a, da);
-}
-
-// Where the range is checked, as measured on 1,048,576 x 9,728: once per unit of 8
-// elements (two code paths) for the forward kernels and the erf-form backward; element
-// by element (one path, fewer registers) for the SiLU and tanh-form backward.
+// One element with |x| >= fast_limit<KIND>() (or NaN): act, act' and the products in
+// binary64, each output rounded once to bf16.  In binary32 the far-tail
+// factors (e^x below e^-87, erfc far out) are subnormals with few significant bits, and
+// a large g or dh * g scales them back into the normal bf16 range, so the whole element
+// is evaluated in binary64.  Returns (h, 0) for the forward and (de, dg) for the
+// backward, as floats holding bf16 values.
 template <int KIND, bool BWD>
-__device__ __forceinline__ constexpr bool kUnitCheck()
+__device__ __forceinline__ float2 careful_outputs(float xf, float gf, float dhf)
 {
-    return !BWD || KIND == GLU_GEGLU;
+    constexpr double kSqrt2OverPiD = 0.797884560802865355879892;
+    constexpr double kInvSqrt2PiD = 0.398942280401432677939946;
+    constexpr double kInvSqrt2D = 0.707106781186547524400844;
+    constexpr double kGeluTanhCD = 0.044715;
+    const double x = xf;
+    double a, da;
+    if (KIND == GLU_GEGLU) {
+        const double Phi = 0.5 * erfc(-x * kInvSqrt2D);
+        const double phi = exp(-0.5 * x * x) * kInvSqrt2PiD;
+        a = x * Phi;
+        da = x * phi + Phi;
+    } else {
+        // SiLU: sigmoid(x); tanh form: sigmoid(2u), u = sqrt(2/pi) (x + c x^3)
+        const double y = KIND == GLU_SWIGLU ? x : 2.0 * kSqrt2OverPiD * (x + kGeluTanhCD * x * x * x);
+        const double t = exp(-fabs(y));
+        const double big = 1.0 / (1.0 + t);
+        const double small = t * big;
+        const double sp = y >= 0.0 ? big : small;
+        const double sm = y >= 0.0 ? small : big;
+        a = x * sp;
+        if (KIND == GLU_SWIGLU) {
+            da = sp * (1.0 + x * sm);
+        } else {
+            // the second term vanishes with sp * sm; test it first so that a huge |x|
+            // gives sp, not 0 * inf
+            const double w = sp * sm;
+            da = w == 0.0 ? sp : sp + 2.0 * x * w * kSqrt2OverPiD * (1.0 + 3.0 * kGeluTanhCD * x * x);
+        }
+    }
+    const double g = gf;
+    if (!BWD) return make_float2(__bfloat162float(__double2bfloat16(a * g)), 0.0f);
+    const double dh = dhf;
+    return make_float2(__bfloat162float(__double2bfloat16(dh * g * da)),
+                       __bfloat162float(__double2bfloat16(dh * a)));
 }
 
-// The 8 elements of one unit: 4 bf16 pairs of e (already widened in x), g and dh.
-template <int KIND, bool BWD, int MODE>
-__device__ __forceinline__ void glu_unit(const float2 (&x)[4], const uint32_t *wg, const uint32_t *wd,
-                                         uint32_t *p0, uint32_t *p1)
+// The 8 elements of one unit in range: 4 bf16 pairs of e (widened in x), g and dh, two
+// elements per binary32 instruction.
+template <int KIND, bool BWD>
+__device__ __forceinline__ void glu_unit_fast(const float2 (&x)[4], const uint32_t *wg, const uint32_t *wd,
+                                              uint32_t *p0, uint32_t *p1)
 {
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
         const float2 gg = unpack(wg[w]);
         float2 av, dv;
-        if (MODE == kFast) {
-            activation_pair_fast<KIND>(x[w], av, dv);
-        } else if (MODE == kGuarded) {
-            activation<KIND, MODE>(x[w].x, av.x, dv.x);
-            activation<KIND, MODE>(x[w].y, av.y, dv.y);
-        } else {
-            const float2 r0 = activation_careful<KIND>(x[w].x);
-            const float2 r1 = activation_careful<KIND>(x[w].y);
-            av = make_float2(r0.x, r1.x);
-            dv = make_float2(r0.y, r1.y);
-        }
+        activation_pair_fast<KIND>(x[w], av, dv);
         if (!BWD) {
             const float2 h = __fmul2_rn(av, gg);
             p0[w] = pack(h.x, h.y);
@@ -291,6 +279,47 @@ __device__ __forceinline__ void glu_unit(const float2 (&x)[4], const uint32_t *w
             p1[w] = pack(dg.x, dg.y);
         }
     }
+}
+
+struct UnitOut {
+    uint4 o0, o1;
+};
+
+// A unit with some element out of range (rare), out of line so that the fast path keeps
+// its registers: elements in range take the same binary32 operations as glu_unit_fast
+// (identical bits), the others careful_outputs, so each output depends on its own
+// element only.  The unit's words come by value (registers, no local arrays).
+template <int KIND, bool BWD>
+__device__ __noinline__ UnitOut glu_unit_careful(uint4 ve, uint4 vg, uint4 vd)
+{
+    const uint32_t *we = &ve.x, *wg = &vg.x, *wd = &vd.x;
+    UnitOut r;
+    uint32_t *p0 = &r.o0.x, *p1 = &r.o1.x;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const float2 xe = unpack(we[w]);
+        const float2 gg = unpack(wg[w]);
+        const float2 dh = BWD ? unpack(wd[w]) : make_float2(0.0f, 0.0f);
+        float o0[2], o1[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float x = i ? xe.y : xe.x, g = i ? gg.y : gg.x, d = i ? dh.y : dh.x;
+            if (fabsf(x) < fast_limit<KIND>()) {
+                float a, da;
+                activation<KIND>(x, a, da);
+                o0[i] = BWD ? __fmul_rn(__fmul_rn(d, g), da) : __fmul_rn(a, g);
+                o1[i] = __fmul_rn(d, a);
+            } else {
+                const float2 c = careful_outputs<KIND, BWD>(x, g, d);
+                o0[i] = c.x;
+                o1[i] = c.y;
+            }
+        }
+        p0[w] = pack(o0[0], o0[1]);
+        p1[w] = BWD ? pack(o1[0], o1[1]) : 0u;
+    }
+    if (!BWD) r.o1 = make_uint4(0u, 0u, 0u, 0u);
+    return r;
 }
 
 // Blocks per SM the register allocation must leave room for, as measured on 65,536 x
@@ -336,35 +365,20 @@ glu_kernel(const __grid_constant__ GluArgs a)
         const uint32_t *we = &ve[k].x, *wg = &vg[k].x, *wd = &vd[k].x;
         uint4 o0, o1;
         uint32_t *p0 = &o0.x, *p1 = &o1.x;
-        if (kUnitCheck<KIND, BWD>()) {
-            float2 x[4];
-            float amax = 0.0f;
+        float2 x[4];
+        float amax = 0.0f;
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                x[w] = unpack(we[w]);
-                amax = fmaxf(amax, fmaxf(fabsf(x[w].x), fabsf(x[w].y)));
-            }
-            // one range check per unit (NaN fails it and takes the careful path)
-            if (amax < fast_limit<KIND>())
-                glu_unit<KIND, BWD, kFast>(x, wg, wd, p0, p1);
-            else
-                glu_unit<KIND, BWD, kCareful>(x, wg, wd, p0, p1);
+        for (int w = 0; w < 4; ++w) {
+            x[w] = unpack(we[w]);
+            amax = fmaxf(amax, fmaxf(fabsf(x[w].x), fabsf(x[w].y)));
+        }
+        // one range check per unit (NaN fails it)
+        if (amax < fast_limit<KIND>()) {
+            glu_unit_fast<KIND, BWD>(x, wg, wd, p0, p1);
         } else {
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const float2 xe = unpack(we[w]);
-                const float2 gg = unpack(wg[w]);
-                float a0, d0, a1, d1;
-                activation<KIND, kGuarded>(xe.x, a0, d0);
-                activation<KIND, kGuarded>(xe.y, a1, d1);
-                if (!BWD) {
-                    p0[w] = pack(a0 * gg.x, a1 * gg.y);
-                } else {
-                    const float2 dh = unpack(wd[w]);
-                    p0[w] = pack(dh.x * gg.x * d0, dh.y * gg.y * d1);   // de
-                    p1[w] = pack(dh.x * a0, dh.y * a1);                 // dg
-                }
-            }
+            const UnitOut r = glu_unit_careful<KIND, BWD>(ve[k], vg[k], BWD ? vd[k] : ve[k]);
+            o0 = r.o0;
+            o1 = r.o1;
         }
         const uint32_t u = base + k * kThreads;
         store_stream(unit_ptr(a.out0, u, row[k], a.pad_out0), o0);

@@ -121,3 +121,43 @@ def test_random_options_match_oracle(dev, case):
         assert np.array_equal(to_bits(q.contiguous()), qb) and np.array_equal(to_bits(k.contiguous()), kb), what
     if fused is not None:
         assert torch.all(fused[:, hq + hkv:] == 2.5), what                 # V untouched
+
+
+@pytest.mark.parametrize("case", range(40))
+def test_random_glu_options_match_oracle(dev, case):
+    """SwiGLU / GeGLU with random shapes, per-matrix row padding, in-place aliasing and
+    value scales that reach the careful (far-tail) path, within the bar of
+    tests/test_gpu_glu.py."""
+    import packed_varlen_rope_gb300 as pr
+    from test_gpu_glu import KINDS, _fwd_bwd_check
+
+    rng = np.random.Generator(np.random.PCG64(9500 + case))
+    kind = str(rng.choice(KINDS))
+    rows = int(rng.integers(1, 300))
+    cols = int(rng.integers(1, 65)) * 8
+    scale = float(rng.choice([1.0, 3.0, 12.0, 40.0]))
+
+    def bits():
+        f = torch.from_numpy((rng.standard_normal(size=(rows, cols)) * scale).astype(np.float32))
+        return f.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+    def mat(b=None):
+        pad = int(rng.choice([0, 0, 8, 40]))
+        buf = torch.full((rows * (cols + pad),), 6.5, dtype=torch.bfloat16, device=dev)
+        t = buf.as_strided((rows, cols), (cols + pad, 1))
+        if b is not None:
+            t.copy_(from_bits(b, dev))
+        return t
+
+    eb, gb, dhb = bits(), bits(), bits()
+    e, g, dh = mat(eb), mat(gb), mat(dhb)
+    in_place = bool(rng.integers(0, 2))
+    h = g if in_place else mat()
+    pr.glu_fwd(kind, e, g, h)
+    torch.cuda.synchronize()
+    h_res = h.clone()
+    g.copy_(from_bits(gb, dev))                               # restore g if h overwrote it
+    de, dg = (e, g) if in_place else (mat(), mat())
+    pr.glu_bwd(kind, dh, e, g, de, dg)
+    torch.cuda.synchronize()
+    _fwd_bwd_check(kind, eb, gb, dhb, h_res, de.clone(), dg.clone(), (case, kind, rows, cols, scale, in_place))

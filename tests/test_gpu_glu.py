@@ -1,7 +1,8 @@
 """SwiGLU / GeGLU kernels against the binary64 oracle (needs a GB300).
 
-Bar (derived from the arithmetic, the kernels evaluate in binary32 with the accurate
-CUDA math functions, the oracle in binary64, both round once to bf16):
+Bar (derived from the arithmetic: the kernels evaluate in binary32 -- special-function
+exponentials and reciprocals and a fitted erfc where results stay normal, the accurate
+CUDA functions beyond -- the oracle in binary64, both round once to bf16):
 
     |gpu - ref| <= ulp_bf16(max(|gpu|, |ref|)) + 2^-18 * M
 

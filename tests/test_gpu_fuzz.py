@@ -29,8 +29,8 @@ def dev():
     return torch.device("cuda:0")
 
 
-def _bits(rng, shape):
-    f = torch.from_numpy(rng.standard_normal(size=shape).astype(np.float32))
+def _bits(rng, shape, scale=1.0):
+    f = torch.from_numpy((rng.standard_normal(size=shape) * scale).astype(np.float32))
     return f.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
 
@@ -102,7 +102,8 @@ def test_random_options_match_oracle(dev, case):
             kw = {"position_ids": torch.from_numpy(ids32).to(dev)}
             pos = np.where((ids32 >= 0) & (ids32 < (1 << 24)), ids32, -1).astype(np.int32)
 
-    qb, kb = _bits(rng, (T, hq, d)), _bits(rng, (T, hkv, d))
+    vscale = float(rng.choice([1.0, 1.0, 1e-35, 1e35]))              # subnormal products / overflow
+    qb, kb = _bits(rng, (T, hq, d), vscale), _bits(rng, (T, hkv, d), vscale)
     q, k, fused = _views(layout, T, hq, hkv, d, dev)
     q.copy_(from_bits(qb, dev))
     k.copy_(from_bits(kb, dev))
@@ -114,7 +115,7 @@ def test_random_options_match_oracle(dev, case):
         ko = torch.full((T, hkv, d), 7.0, dtype=torch.bfloat16, device=dev)
         pr.rope_qk_apply(q, k, theta, backward=bwd, position_scale=scale, q_out=qo, k_out=ko, **kw)
     torch.cuda.synchronize()
-    what = (case, d, hq, hkv, layout, source, in_place, bwd, scale)
+    what = (case, d, hq, hkv, layout, source, in_place, bwd, scale, vscale)
     assert np.array_equal(to_bits(qo.contiguous()), oracle.rope_rows(qb, pos, theta, bwd, scale)), what
     assert np.array_equal(to_bits(ko.contiguous()), oracle.rope_rows(kb, pos, theta, bwd, scale)), what
     if not in_place:

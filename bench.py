@@ -441,6 +441,8 @@ def run_ours(args, rank, world, local):
 
     rows_moved = T if args.layout == "padded" else pack.valid_tokens     # rows one launch reads and writes
     bytes_per_pass = 4 * (w.n_q_heads + w.n_kv_heads) * w.head_dim * rows_moved
+    # the kernel instance the library dispatches for this call (head_dim template, 64-bit offsets)
+    launch = pr.rope_qk_launch_info(q, k, w.theta, cu_seqlens=cu, cos_sin_cache=cache, seq_used=used)
 
     def step():
         fwd(q, k)
@@ -525,7 +527,8 @@ def run_ours(args, rank, world, local):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
                      "traffic": profiled_traffic(w.name) if cache is not None and args.layout == "packed" else None,
-                     "kernel": "rope_qk_tile_kernel<128,false>",
+                     "kernel": launch.kernel_name(),
+                     "grid": {"ctas": launch.grid, "threads": launch.threads, "tile_tokens": launch.tile_tokens},
                      "algorithmic_bytes_per_launch": bytes_per_pass,
                      "avg_launch_us": avg_launch_s * 1e6, "peak_kind": peak_kind + " (hbm_gbs)"},
         "clocks": clocks,
@@ -761,10 +764,11 @@ def run_rope_forms(args, rank, world, local):
 
     forms = {}
 
-    def record(name, fn, check, launches=1):
+    def record(name, fn, check, launches=1, nbytes_form=None):
         sec = timed(fn)
-        forms[name] = {"us": sec * 1e6, "gbs": nbytes / sec / 1e9, "frac": nbytes / sec / 1e9 / peak,
-                       "launches": launches, "check": check}
+        nb = nbytes if nbytes_form is None else nbytes_form
+        forms[name] = {"us": sec * 1e6, "gbs": nb / sec / 1e9, "frac": nb / sec / 1e9 / peak,
+                       "launches": launches, "bytes": nb, "check": check}
 
     # contiguous [T, H, d]
     q, k = q0.clone(), k0.clone()
@@ -803,18 +807,53 @@ def run_rope_forms(args, rank, world, local):
     pr.rope_qk_apply(q, k, w.theta, position_ids=pos, cos_sin_cache=cache)
     record("position_ids int32 [T], rope_qk_apply",
            lambda: pr.rope_qk_apply(q, k, w.theta, position_ids=pos, cos_sin_cache=cache), same(q, k))
-    # context-parallel shards: 2 contiguous halves, and the load-balanced 2*cp chunks (cp = 2)
-    for name, bounds in (("2 contiguous CP shards (token_offset)", [(0, T // 2), (T // 2, T)]),
-                         ("cp=2 load-balanced chunks 0,3 | 1,2 (token_offset)",
-                          [(0, T // 4), (3 * T // 4, T), (T // 4, T // 2), (T // 2, 3 * T // 4)])):
-        q, k = q0.clone(), k0.clone()
+    # context-parallel shards, cp = 2.  Contiguous: rank r holds tokens [r T/2, (r+1) T/2)
+    # of the one pack buffer (a token offset per launch).  Load-balanced: rank r holds
+    # chunks r and 3 - r of 4, one after the other in its own buffer, rotated in one
+    # launch through the segment list; each rank's launch is timed alone (what a rank of
+    # a real context-parallel group runs) and the two ranks back to back.
+    q, k = q0.clone(), k0.clone()
+    halves = [(0, T // 2), (T // 2, T)]
 
-        def shards():
-            for a, b in bounds:
-                pr.rope_qk_apply(q[a:b], k[a:b], w.theta, cu_seqlens=cu, token_offset=a, cos_sin_cache=cache)
+    def contiguous_shards():
+        for a, b in halves:
+            pr.rope_qk_apply(q[a:b], k[a:b], w.theta, cu_seqlens=cu, token_offset=a, cos_sin_cache=cache)
 
-        shards()
-        record(name, shards, same(q, k), launches=len(bounds))
+    contiguous_shards()
+    record("cp=2 contiguous shards, both ranks (token_offset, 2 launches)", contiguous_shards, same(q, k),
+           launches=2)
+    cp = 2
+    ranks = []
+    for r in range(cp):
+        shards = pr.cp_shards(T, cp, r, load_balanced=True)
+        rows_r = torch.tensor(pr.shard_rows(shards), device=dev)
+        inside = rows_r < T                                   # rows past the pack's end are padding
+        ql = torch.zeros((rows_r.numel(), Hq, d), dtype=torch.bfloat16, device=dev)
+        kl = torch.zeros((rows_r.numel(), Hkv, d), dtype=torch.bfloat16, device=dev)
+        ql[inside], kl[inside] = q0[rows_r[inside]], k0[rows_r[inside]]
+        ranks.append((ql, kl, pr.shard_segments(shards), rows_r, inside))
+
+    def rank_launch(r):
+        ql, kl, segs, _, _ = ranks[r]
+        pr.rope_qk_apply(ql, kl, w.theta, cu_seqlens=cu, segments=segs, cos_sin_cache=cache)
+
+    def lb_check():
+        ok = True
+        for ql, kl, _, rows_r, inside in ranks:
+            ok = ok and torch.equal(ql[inside], q_ref[rows_r[inside]]) and torch.equal(kl[inside], k_ref[rows_r[inside]])
+        return "bit-identical to contiguous" if ok else "MISMATCH"
+
+    for r in range(cp):
+        rank_launch(r)
+    check = lb_check()
+    rank_bytes = [4 * (Hq + Hkv) * d * int(x[4].sum()) for x in ranks]
+    record("cp=2 load-balanced, rank 0 alone: chunks 0,3 (segments, 1 launch)", lambda: rank_launch(0), check,
+           nbytes_form=rank_bytes[0])
+    record("cp=2 load-balanced, rank 1 alone: chunks 1,2 (segments, 1 launch)", lambda: rank_launch(1), check,
+           nbytes_form=rank_bytes[1])
+    record("cp=2 load-balanced, both ranks (segments, 2 launches)", lambda: [rank_launch(r) for r in range(cp)],
+           check, launches=2)
+    del ranks
     # binary64 cos/sin on the fly (no cache)
     q, k = q0.clone(), k0.clone()
     pr.rope_qk_fwd(q, k, cu, w.theta)

@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define ROPE_QK_ABI_VERSION 4
+#define ROPE_QK_ABI_VERSION 5
 
 typedef enum rope_status {
     ROPE_OK = 0,
@@ -66,7 +66,10 @@ typedef enum rope_status {
     ROPE_ERR_LAUNCH = -7,       /* the CUDA runtime refused a launch or copy */
     ROPE_ERR_THETA = -8,        /* theta or position_scale not finite and > 0 */
     ROPE_ERR_KIND = -9,         /* unknown activation kind (glu.h) */
-    ROPE_ERR_WORKSPACE = -10    /* one token's Q and K rows do not fit the static staging */
+    ROPE_ERR_WORKSPACE = -10,   /* one token's Q and K rows do not fit the static staging */
+    ROPE_ERR_CACHE = -11        /* the cos/sin cache was built for another theta, head_dim,
+                                   position_scale or device, or its descriptor was not
+                                   written by rope_cos_sin_cache_build */
 } rope_status;
 
 /* Bits of rope_qk_desc.flags. */
@@ -77,6 +80,34 @@ typedef enum rope_status {
 #define ROPE_CU_DECREASING       0x2   /* cu_seqlens[s+1] < cu_seqlens[s] for some s */
 #define ROPE_CU_PAST_END         0x4   /* cu_seqlens[n_seqs] > total_tokens */
 #define ROPE_CU_NONZERO_START    0x8   /* cu_seqlens[0] != 0 (allowed; tokens before it are outside) */
+
+/*
+ * A cos/sin cache: the (c, s) pairs of every position below `rows`, evaluated once by
+ * rope_cos_sin_cache_build for one (theta, head_dim, position_scale), so that the
+ * rotations read them instead of evaluating them (the pages take cos and sin as
+ * precomputed inputs; unsloth.ai page, section "Kernel Triton QK RoPE fusionné avec
+ * packing").  The rows are a function of theta alone (TRL "training beyond 1M
+ * tokens", YaRN section: `rope_theta` must match the model), so the descriptor records
+ * what they were built for and every call that reads them checks it.
+ *
+ * Only rope_cos_sin_cache_build writes this struct; treat it as read-only.  A call
+ * rejects (ROPE_ERR_CACHE) a cache whose theta, head_dim or position_scale differs
+ * from the call's, that was built on another device, or whose fields were changed
+ * after the build (the `check` word no longer matches them).  The struct is host
+ * memory owned by the caller and read during the call only; `data` is the device
+ * table, owned by the caller, 16-byte aligned, float[rows][4][head_dim/16][4]: entry
+ * [p][q][c] holds (c_j, s_j, c_{j+1}, s_{j+1}) of position p for j = 8c + 2q (chunk c
+ * covers frequencies 8c..8c+7, the order in which the rotation kernel consumes them).
+ */
+typedef struct rope_cos_sin_cache {
+    const float *data;             /* device table, rows * head_dim floats             */
+    int64_t rows;                  /* positions 0 .. rows-1 (at most 2^24)             */
+    int32_t head_dim;
+    int32_t device;                /* CUDA device ordinal current at the build         */
+    double theta;
+    double position_scale;
+    uint64_t check;                /* written by the build from the fields above       */
+} rope_cos_sin_cache;
 
 /*
  * Forward: rotate Q and K of every token of the pack (unsloth.ai page, section "Kernel
@@ -95,17 +126,16 @@ typedef enum rope_status {
  *   in_place        nonzero: write the result over q and k (q_out/k_out ignored);
  *                   zero: write to q_out/k_out (same shapes, 16-byte aligned, disjoint
  *                   from q and k); q and k are then only read.
- *   cos_sin_cache   optional device cache of (c, s) per position, as
- *                   rope_cos_sin_cache_build writes it for the same theta and head_dim;
- *                   16-byte aligned.  Positions >= cache_rows, and every position when
- *                   the cache is NULL, are evaluated on the fly with identical results.
- *   cache_rows      rows of the cache (>= 0).
+ *   cos_sin_cache   optional (NULL: none) cache built for the same theta and head_dim
+ *                   with position_scale 1, on the current device.  Positions >= its
+ *                   rows, and every position without a cache, are evaluated on the fly
+ *                   with identical results.
  *   stream          cudaStream_t or NULL.
  */
 int rope_qk_fwd(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs,
                 int64_t total_tokens, int32_t n_q_heads, int32_t n_kv_heads,
                 int32_t head_dim, double theta, int32_t in_place,
-                void *q_out, void *k_out, const float *cos_sin_cache, int64_t cache_rows,
+                void *q_out, void *k_out, const rope_cos_sin_cache *cos_sin_cache,
                 void *stream);
 
 /*
@@ -116,7 +146,7 @@ int rope_qk_fwd(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs,
 int rope_qk_bwd(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs,
                 int64_t total_tokens, int32_t n_q_heads, int32_t n_kv_heads,
                 int32_t head_dim, double theta, int32_t in_place,
-                void *q_out, void *k_out, const float *cos_sin_cache, int64_t cache_rows,
+                void *q_out, void *k_out, const rope_cos_sin_cache *cos_sin_cache,
                 void *stream);
 
 /*
@@ -149,15 +179,33 @@ int rope_qk_bwd(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs,
  * tokens [a, b) of a pack pass the whole pack's cu_seqlens with token_offset = a
  * (token_offset + total_tokens <= 2^24).
  *
+ * Segments.  A context-parallel rank of the load-balanced layout (TRL "training beyond
+ * 1M tokens", context-parallel section: the sequence cut into 2 * cp_size chunks, rank
+ * r holding chunks r and 2 * cp_size - 1 - r) keeps rows that are not consecutive in
+ * the pack.  With n_segments > 0 (at most ROPE_MAX_SEGMENTS), segments[i] says that
+ * rows row_start[i] .. row_start[i+1] - 1 (the last segment: up to total_tokens - 1)
+ * are tokens token_start[i], token_start[i] + 1, ... of cu_seqlens' stream, so one call
+ * rotates all of a rank's shards.  segments is a HOST array read during the call;
+ * segments[0].row_start == 0, row_start strictly increasing and below total_tokens,
+ * token_start >= 0 and every segment's last token below 2^24 (else ROPE_ERR_SHAPE or
+ * ROPE_ERR_UNSUPPORTED).  It needs cu_seqlens (not position_ids) and token_offset 0.
+ *
  * seq_used.  Optional, with cu_seqlens: sample s uses only its first seq_used[s]
  * tokens; the rest of its rows (the padding of a padded batch laid out with uniform
  * cu_seqlens) are left out like tokens outside the pack.  Ignored with position_ids.
  *
  * position_scale.  Linear position rescale (> 0; 1.0 = none): every frequency is
  * divided by it in binary64 before the rounding to binary32, i.e. position p acts as
- * p / position_scale.  A cos/sin cache must come from rope_cos_sin_cache_build_scaled
- * with the same theta, head_dim and position_scale.
+ * p / position_scale.  A cos/sin cache must have been built with the same theta,
+ * head_dim and position_scale (else ROPE_ERR_CACHE).
  */
+#define ROPE_MAX_SEGMENTS 16
+
+typedef struct rope_qk_segment {
+    int64_t row_start;             /* first row (of q and k) of the segment           */
+    int64_t token_start;           /* its token index in cu_seqlens' stream           */
+} rope_qk_segment;
+
 typedef struct rope_qk_desc {
     void *q;                       /* bf16 view [total_tokens, n_q_heads, head_dim]  */
     int64_t q_stride_token;        /* elements between consecutive tokens             */
@@ -181,16 +229,38 @@ typedef struct rope_qk_desc {
     int64_t token_offset;          /* >= 0; global index of row 0 in cu_seqlens' stream */
     double theta;
     double position_scale;         /* 1.0 = plain rotation                            */
-    const float *cos_sin_cache;    /* optional, as for rope_qk_fwd                    */
-    int64_t cache_rows;
+    const rope_cos_sin_cache *cos_sin_cache;   /* optional (NULL: none)               */
     int32_t backward;              /* 0: rotation; nonzero: transpose (sin negated)   */
     int32_t flags;                 /* ROPE_FLAG_* bits, 0 for none; an unknown bit is
                                       ROPE_ERR_UNSUPPORTED                             */
     const int32_t *seq_used;       /* optional device int32 [n_seqs], with cu_seqlens */
+    const rope_qk_segment *segments;   /* optional HOST array [n_segments]            */
+    int32_t n_segments;            /* 0: no segments (row r is token token_offset + r) */
+    int32_t reserved;              /* 0 */
 } rope_qk_desc;
 
 /* Apply the rotation a descriptor describes (asynchronous on `stream`). */
 int rope_qk_apply(const rope_qk_desc *desc, void *stream);
+
+/*
+ * What rope_qk_apply would launch for `desc`, without launching it and without any
+ * CUDA call: the rotation kernel's compile-time instance (head_dim 64, 96, 128 or 256,
+ * or 0 for the generic one), whether it uses 64-bit element offsets (some view spans
+ * 2^31 elements or more; unsloth.ai page, section "Indexage int64 pour les kernels
+ * Triton"), and its grid: one CTA of `threads` threads per tile of `tile_tokens`
+ * consecutive tokens.  Returns the status rope_qk_apply's argument checks give (the
+ * cache's device is not checked); grid == 0 when there is nothing to launch.
+ */
+typedef struct rope_qk_launch {
+    int32_t head_dim_instance;
+    int32_t long_index;
+    int32_t grid;
+    int32_t tile_tokens;
+    int32_t threads;
+    int32_t smem_bytes;            /* dynamic shared memory per CTA (cos/sin rows)    */
+} rope_qk_launch;
+
+int rope_qk_launch_info(const rope_qk_desc *desc, rope_qk_launch *info);
 
 /*
  * Host-buffer form of rope_qk_apply, for Q and K that live in host memory.  desc->q,
@@ -207,13 +277,16 @@ int rope_qk_apply(const rope_qk_desc *desc, void *stream);
  * the host-to-device copy of one chunk, the rotation of the previous one and the
  * device-to-host copy of the one before overlap, the copies on two streams the library
  * creates per device on first use and keeps.  Each chunk is rotated with its global
- * token offset (or its slice of position_ids), so the result is that of one rotation
- * of the whole pack.
+ * token offset (or its slice of position_ids, or of the segment list), so the result
+ * is that of one rotation of the whole pack.
  *
  * `stream` runs the rotations and then waits for the last copy to the host: once it
  * reaches that point, the host outputs are complete.  The host buffers and the
- * workspace must stay untouched until then.  Enqueueing is serialised by a lock.  On an
- * error return after copies were queued, `stream` is still ordered after all of them.
+ * workspace must stay untouched until then.  Enqueueing is serialised by a lock.
+ * Every argument is checked for the whole pack before the first copy is queued, so a
+ * rejected call copies and launches nothing; only a failure of the CUDA runtime itself
+ * (ROPE_ERR_LAUNCH) can come after copies were queued, and `stream` is then still
+ * ordered after all of them.
  */
 int rope_qk_host(const rope_qk_desc *desc, void *workspace, int64_t workspace_bytes, void *stream);
 
@@ -230,7 +303,9 @@ int rope_qk_host(const rope_qk_desc *desc, void *workspace, int64_t workspace_by
  * Same descriptor and results as rope_qk_host.  Chunks of up to
  * 32 MiB / ((n_q_heads + n_kv_heads) * head_dim * 2) tokens are copied in, rotated and
  * copied out one after the other, all on `stream` (no overlap of copies and rotation).
- * A shape whose single token does not fit is rejected with ROPE_ERR_WORKSPACE.
+ * A shape whose single token does not fit is rejected with ROPE_ERR_WORKSPACE.  As for
+ * rope_qk_host, every argument is checked for the whole pack before the first copy: a
+ * rejected call leaves the host buffers untouched.
  *
  * The first call on a device looks up the array's device address (once per device,
  * that device current); make that first call before any stream capture.  Every call
@@ -242,27 +317,21 @@ int rope_qk_host(const rope_qk_desc *desc, void *workspace, int64_t workspace_by
 int rope_qk_host_static(const rope_qk_desc *desc, void *stream);
 
 /*
- * Fill a cos/sin cache with (c, s) of every position p < cache_rows and frequency
- * j < head_dim/2, by the arithmetic above (binary64 cos/sin on the device, rounded to
- * binary32).  cache: device float[cache_rows][4][head_dim/16][4], 16-byte aligned,
- * owned by the caller (cache_rows * head_dim floats).  Entry [p][q][c] holds
- * (c_j, s_j, c_{j+1}, s_{j+1}) for j = 8c + 2q: chunk c covers frequencies
- * 8c..8c+7, the order in which the rotation kernel consumes them.  Build it once per
- * (theta, head_dim) with cache_rows >= the longest sample (at most 2^24); every layer
- * and step can reuse it.
+ * Build a cos/sin cache: fill `data` with (c, s) of every position p < rows and
+ * frequency j < head_dim/2 by the arithmetic above, the frequencies divided by
+ * position_scale (> 0, finite; 1.0 for the plain rotation) before their rounding to
+ * binary32 (the linear rescale of TRL "training beyond 1M tokens", YaRN section: with
+ * factor 4, position 100,000 is read as 25,000), and write the descriptor `cache` that
+ * the rotations take.  data: device float[rows * head_dim], 16-byte aligned, owned by
+ * the caller (rope_cos_sin_cache_bytes).  rows <= 2^24; build it once per (theta,
+ * head_dim, position_scale) with rows >= the longest sample, on the device that runs
+ * the rotations (the current device); every layer and step can reuse it.  The
+ * descriptor is written only when the fill was queued (ROPE_OK); it is usable on
+ * `stream`, or after it, once the fill has run.
  */
-int rope_cos_sin_cache_build(float *cache, int64_t cache_rows, int32_t head_dim,
-                             double theta, void *stream);
-
-/*
- * rope_cos_sin_cache_build for a linearly rescaled position (TRL "training beyond 1M
- * tokens", YaRN section: with factor 4, position 100,000 is read as 25,000).  Every
- * frequency is divided by position_scale (> 0, finite) before the one rounding to
- * binary32, as the `position_scale` field of rope_qk_desc does.  A cache serves only
- * calls with the same theta, head_dim and position_scale.
- */
-int rope_cos_sin_cache_build_scaled(float *cache, int64_t cache_rows, int32_t head_dim,
-                                    double theta, double position_scale, void *stream);
+int rope_cos_sin_cache_build(rope_cos_sin_cache *cache, float *data, int64_t rows,
+                             int32_t head_dim, double theta, double position_scale,
+                             void *stream);
 
 /* Bytes a cache of `cache_rows` rows takes (cache_rows * head_dim * 4), or -1. */
 int64_t rope_cos_sin_cache_bytes(int64_t cache_rows, int32_t head_dim);

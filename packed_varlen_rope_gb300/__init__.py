@@ -19,8 +19,13 @@ from ._binding import (  # noqa: F401
     ROPE_CU_NONZERO_START,
     ROPE_CU_PAST_END,
     ROPE_FLAG_POSITION_IDS_INT64,
+    ROPE_MAX_SEGMENTS,
+    CosSinCache,
+    RopeCosSinCacheDesc,
     RopeError,
     RopeQKDesc,
+    RopeQKLaunch,
+    RopeQKSegment,
     glu_bwd,
     glu_fwd,
     load_library,
@@ -32,10 +37,12 @@ from ._binding import (  # noqa: F401
     rope_qk_fwd,
     rope_qk_host,
     rope_qk_inv_freq,
+    rope_qk_launch_info,
     rope_qk_positions,
     rope_strerror,
     rope_validate_cu_seqlens,
 )
+from .shards import cp_shards, shard_rows, shard_segments  # noqa: F401
 
 
 def _autograd_function():
@@ -46,25 +53,27 @@ def _autograd_function():
         backward applies the transpose rotation to the incoming gradients."""
 
         @staticmethod
-        def forward(ctx, q, k, theta, cu_seqlens, position_ids, token_offset, position_scale, cos_sin_cache):
+        def forward(ctx, q, k, theta, cu_seqlens, position_ids, token_offset, position_scale, cos_sin_cache,
+                    segments):
             rope_qk_apply(q, k, theta, cu_seqlens=cu_seqlens, position_ids=position_ids,
-                          token_offset=token_offset, position_scale=position_scale, cos_sin_cache=cos_sin_cache)
+                          token_offset=token_offset, position_scale=position_scale, cos_sin_cache=cos_sin_cache,
+                          segments=segments)
             ctx.mark_dirty(q, k)
-            ctx.save_for_backward(cu_seqlens, position_ids, cos_sin_cache)
-            ctx.args = (theta, token_offset, position_scale)
+            ctx.save_for_backward(cu_seqlens, position_ids)
+            ctx.args = (theta, token_offset, position_scale, cos_sin_cache, segments)
             return q, k
 
         @staticmethod
         def backward(ctx, dq, dk):
-            cu_seqlens, position_ids, cache = ctx.saved_tensors
-            theta, token_offset, position_scale = ctx.args
+            cu_seqlens, position_ids = ctx.saved_tensors
+            theta, token_offset, position_scale, cache, segments = ctx.args
             dq, dk = dq.contiguous(), dk.contiguous()      # e.g. broadcast (stride 0) gradients
             dq_out = torch.empty(dq.shape, dtype=dq.dtype, device=dq.device)
             dk_out = torch.empty(dk.shape, dtype=dk.dtype, device=dk.device)
             rope_qk_apply(dq, dk, theta, cu_seqlens=cu_seqlens, position_ids=position_ids, backward=True,
                           q_out=dq_out, k_out=dk_out, token_offset=token_offset,
-                          position_scale=position_scale, cos_sin_cache=cache)
-            return dq_out, dk_out, None, None, None, None, None, None
+                          position_scale=position_scale, cos_sin_cache=cache, segments=segments)
+            return dq_out, dk_out, None, None, None, None, None, None, None
 
     return RopeQK
 
@@ -73,15 +82,16 @@ _RopeQK = None
 
 
 def apply_rope_qk(q, k, cu_seqlens, theta: float, cos_sin_cache=None, position_ids=None, token_offset: int = 0,
-                  position_scale: float = 1.0):
+                  position_scale: float = 1.0, segments=None):
     """Differentiable in-place RoPE of packed q [T, Hq, d] and k [T, Hkv, d] (any
     token/head strides).  Positions from ``position_ids`` if given, else from
-    ``cu_seqlens`` (row r is token ``token_offset + r``)."""
+    ``cu_seqlens`` (row r is token ``token_offset + r``, or as ``segments`` map it)."""
     global _RopeQK
     if _RopeQK is None:
         _RopeQK = _autograd_function()
+    segs = None if segments is None else tuple((int(a), int(b)) for a, b in segments)
     return _RopeQK.apply(q, k, theta, cu_seqlens, position_ids, int(token_offset), float(position_scale),
-                         cos_sin_cache)
+                         cos_sin_cache, segs)
 
 
 def cache_rows_for(needed: int, current: int) -> int:
@@ -118,24 +128,32 @@ class RotaryEmbedding:
 
         device = torch.device(device)
         cur = self._caches.get(device)
-        want = cache_rows_for(rows, 0 if cur is None else cur.shape[0])
-        if cur is None or want != cur.shape[0]:
+        want = cache_rows_for(rows, 0 if cur is None else cur.rows)
+        if cur is None or want != cur.rows:
             cur = new_cos_sin_cache(want, self.head_dim, self.theta, device=device,
                                     position_scale=self.position_scale)
             self._caches[device] = cur
         return cur
 
     def __call__(self, q, k, cu_seqlens=None, position_ids=None, token_offset: int = 0,
-                 max_position: int = 0):
+                 max_position: int = 0, segments=None):
         """Rotate q and k in place (differentiable).  ``max_position``: an upper bound on
         the position ids, for ids that exceed the row count (a context-parallel shard
         of a long sequence carrying global ids); without it the cache covers ``T``
-        rows and larger ids are evaluated on the fly."""
+        rows and larger ids are evaluated on the fly.  ``segments``: a context-parallel
+        rank's (row_start, token_start) list (``shard_segments``)."""
         if q.shape[-1] != self.head_dim:
             raise ValueError("q and k must have head_dim %d" % self.head_dim)
         T = q.shape[0]
-        rows = T if position_ids is not None else int(token_offset) + T
+        if position_ids is not None:
+            rows = T
+        elif segments is not None:
+            segs = list(segments)
+            ends = [segs[i + 1][0] if i + 1 < len(segs) else T for i in range(len(segs))]
+            rows = max(b + (e - a) for (a, b), e in zip(segs, ends))
+        else:
+            rows = int(token_offset) + T
         rows = max(rows, int(max_position) + 1 if max_position else 0)
         cache = self.cache(q.device, max(rows, 1))
         return apply_rope_qk(q, k, cu_seqlens, self.theta, cos_sin_cache=cache, position_ids=position_ids,
-                             token_offset=token_offset, position_scale=self.position_scale)
+                             token_offset=token_offset, position_scale=self.position_scale, segments=segments)

@@ -16,9 +16,9 @@ LIB_PATH = os.path.join(HERE, "librope_qk.so")
 
 EXPORTS = (
     "rope_qk_fwd", "rope_qk_bwd", "rope_qk_apply", "rope_cos_sin_cache_build",
-    "rope_cos_sin_cache_build_scaled", "rope_cos_sin_cache_bytes", "rope_qk_positions",
+    "rope_cos_sin_cache_bytes", "rope_qk_positions",
     "rope_validate_cu_seqlens", "rope_qk_inv_freq", "rope_strerror", "rope_qk_abi_version",
-    "glu_fwd", "glu_bwd", "rope_qk_host", "rope_qk_host_static",
+    "glu_fwd", "glu_bwd", "rope_qk_host", "rope_qk_host_static", "rope_qk_launch_info",
 )
 
 GLU_KINDS = {"swiglu": 0, "geglu": 1, "geglu_tanh": 2}
@@ -28,8 +28,27 @@ ROPE_CU_DECREASING = 0x2
 ROPE_CU_PAST_END = 0x4
 ROPE_CU_NONZERO_START = 0x8
 ROPE_FLAG_POSITION_IDS_INT64 = 0x1
+ROPE_MAX_SEGMENTS = 16
 
 _lib = None
+
+
+class RopeCosSinCacheDesc(ctypes.Structure):
+    """Mirror of ``rope_cos_sin_cache`` in include/rope_qk.h (written by the library's
+    cache build only)."""
+
+    _fields_ = [
+        ("data", ctypes.c_void_p), ("rows", ctypes.c_int64), ("head_dim", ctypes.c_int32),
+        ("device", ctypes.c_int32), ("theta", ctypes.c_double), ("position_scale", ctypes.c_double),
+        ("check", ctypes.c_uint64),
+    ]
+
+
+class RopeQKSegment(ctypes.Structure):
+    """Mirror of ``rope_qk_segment``: rows from ``row_start`` on are tokens
+    ``token_start``, ``token_start + 1``, ... of cu_seqlens' stream."""
+
+    _fields_ = [("row_start", ctypes.c_int64), ("token_start", ctypes.c_int64)]
 
 
 class RopeQKDesc(ctypes.Structure):
@@ -44,10 +63,58 @@ class RopeQKDesc(ctypes.Structure):
         ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
         ("position_ids", ctypes.c_void_p), ("total_tokens", ctypes.c_int64), ("token_offset", ctypes.c_int64),
         ("theta", ctypes.c_double), ("position_scale", ctypes.c_double),
-        ("cos_sin_cache", ctypes.c_void_p), ("cache_rows", ctypes.c_int64),
+        ("cos_sin_cache", ctypes.POINTER(RopeCosSinCacheDesc)),
         ("backward", ctypes.c_int32), ("flags", ctypes.c_int32),
         ("seq_used", ctypes.c_void_p),
+        ("segments", ctypes.POINTER(RopeQKSegment)), ("n_segments", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
     ]
+
+
+class RopeQKLaunch(ctypes.Structure):
+    """Mirror of ``rope_qk_launch``: what rope_qk_apply launches for a descriptor."""
+
+    _fields_ = [("head_dim_instance", ctypes.c_int32), ("long_index", ctypes.c_int32), ("grid", ctypes.c_int32),
+                ("tile_tokens", ctypes.c_int32), ("threads", ctypes.c_int32), ("smem_bytes", ctypes.c_int32)]
+
+    def kernel_name(self) -> str:
+        """The rotation kernel's instance as its template reads: rope_qk_tile_kernel<D, LONG>."""
+        return "rope_qk_tile_kernel<%d,%s>" % (self.head_dim_instance, "true" if self.long_index else "false")
+
+
+class CosSinCache:
+    """A cos/sin cache: the device table ``data`` (float32 [rows, 4, head_dim/16, 4])
+    and the descriptor the library's build wrote for it, which records the theta,
+    head_dim, position_scale and device it serves.  Passed as ``cos_sin_cache=`` to the
+    rotations; the library rejects it for any other theta, head_dim, scale or device."""
+
+    def __init__(self, data, desc: RopeCosSinCacheDesc):
+        self.data = data
+        self.desc = desc
+
+    @property
+    def rows(self) -> int:
+        return int(self.desc.rows)
+
+    @property
+    def head_dim(self) -> int:
+        return int(self.desc.head_dim)
+
+    @property
+    def theta(self) -> float:
+        return float(self.desc.theta)
+
+    @property
+    def position_scale(self) -> float:
+        return float(self.desc.position_scale)
+
+    @property
+    def device(self):
+        return self.data.device
+
+    def ref(self):
+        """``rope_cos_sin_cache *`` for a C call."""
+        return ctypes.pointer(self.desc)
 
 
 class RopeError(RuntimeError):
@@ -67,20 +134,21 @@ def load_library(path: Optional[str] = None):
         raise OSError("librope_qk.so is not built (%s); run packed_varlen_rope_gb300.build.build()" % p)
     lib = ctypes.CDLL(p)
     vp, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double
-    rope_args = [vp, vp, vp, i32, i64, i32, i32, i32, dbl, i32, vp, vp, vp, i64, vp]
+    cache_p = ctypes.POINTER(RopeCosSinCacheDesc)
+    rope_args = [vp, vp, vp, i32, i64, i32, i32, i32, dbl, i32, vp, vp, cache_p, vp]
     for name in ("rope_qk_fwd", "rope_qk_bwd"):
         getattr(lib, name).argtypes = rope_args
         getattr(lib, name).restype = ctypes.c_int
     lib.rope_qk_apply.argtypes = [ctypes.POINTER(RopeQKDesc), vp]
     lib.rope_qk_apply.restype = ctypes.c_int
+    lib.rope_qk_launch_info.argtypes = [ctypes.POINTER(RopeQKDesc), ctypes.POINTER(RopeQKLaunch)]
+    lib.rope_qk_launch_info.restype = ctypes.c_int
     lib.rope_qk_host.argtypes = [ctypes.POINTER(RopeQKDesc), vp, i64, vp]
     lib.rope_qk_host.restype = ctypes.c_int
     lib.rope_qk_host_static.argtypes = [ctypes.POINTER(RopeQKDesc), vp]
     lib.rope_qk_host_static.restype = ctypes.c_int
-    lib.rope_cos_sin_cache_build.argtypes = [vp, i64, i32, dbl, vp]
+    lib.rope_cos_sin_cache_build.argtypes = [cache_p, vp, i64, i32, dbl, dbl, vp]
     lib.rope_cos_sin_cache_build.restype = ctypes.c_int
-    lib.rope_cos_sin_cache_build_scaled.argtypes = [vp, i64, i32, dbl, dbl, vp]
-    lib.rope_cos_sin_cache_build_scaled.restype = ctypes.c_int
     lib.rope_cos_sin_cache_bytes.argtypes = [i64, i32]
     lib.rope_cos_sin_cache_bytes.restype = ctypes.c_int64
     lib.rope_qk_positions.argtypes = [vp, i32, i64, vp, vp]
@@ -159,6 +227,30 @@ def _check_cu(cu_seqlens, device):
         raise ValueError("cu_seqlens must be a contiguous int32 tensor on the device of q")
 
 
+def _cache_arg(cache, head_dim: int, device):
+    """``rope_cos_sin_cache *`` of a ``CosSinCache`` (None: a NULL pointer) after the
+    checks the C side cannot make on a tensor: type, dtype, layout and device.  theta,
+    head_dim and position_scale are checked by the library against its descriptor."""
+    import torch
+
+    if cache is None:
+        return None
+    if not isinstance(cache, CosSinCache):
+        raise ValueError("cos_sin_cache must be a CosSinCache (new_cos_sin_cache / rope_cos_sin_cache_build)")
+    t = cache.data
+    if t.dtype != torch.float32:
+        raise ValueError("cos_sin_cache must hold float32 values, not %s" % t.dtype)
+    if t.dim() != 4 or tuple(t.shape[1:]) != (4, head_dim // 16, 4) or t.shape[0] != cache.rows or \
+            not t.is_contiguous():
+        raise ValueError("cos_sin_cache must hold a contiguous [rows, 4, head_dim/16, 4] table for head_dim %d, "
+                         "got %s" % (head_dim, tuple(t.shape)))
+    if not t.is_cuda or t.device != device:
+        raise ValueError("cos_sin_cache is on %s, the rotation runs on %s" % (t.device, device))
+    if cache.rows and cache.desc.data != t.data_ptr():
+        raise ValueError("cos_sin_cache's descriptor does not describe its tensor")
+    return cache.ref()
+
+
 def _rope(fn_name, q, k, cu_seqlens, theta, in_place, q_out, k_out, cos_sin_cache, stream):
     _check_qk(q, k)
     _check_cu(cu_seqlens, q.device)
@@ -170,17 +262,11 @@ def _rope(fn_name, q, k, cu_seqlens, theta, in_place, q_out, k_out, cos_sin_cach
         _check_qk(q_out, k_out)
         if q_out.shape != q.shape or k_out.shape != k.shape or q_out.device != q.device:
             raise ValueError("q_out/k_out must have the shapes and device of q/k")
-    rows = 0
-    if cos_sin_cache is not None:
-        if cos_sin_cache.dim() != 4 or tuple(cos_sin_cache.shape[1:]) != (4, d // 16, 4) or \
-                not cos_sin_cache.is_contiguous() or cos_sin_cache.device != q.device:
-            raise ValueError("cos_sin_cache must be a contiguous float32 [rows, 4, head_dim/16, 4] tensor")
-        rows = cos_sin_cache.shape[0]
+    cache = _cache_arg(cos_sin_cache, d, q.device)
     fn = getattr(load_library(), fn_name)
     st = _on(q.device, fn, _ptr(q), _ptr(k), _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, hq, hkv, d,
              float(theta), 1 if in_place else 0, _ptr(q_out) if not in_place else None,
-             _ptr(k_out) if not in_place else None, _ptr(cos_sin_cache), rows,
-             _stream(stream, q.device))
+             _ptr(k_out) if not in_place else None, cache, _stream(stream, q.device))
     _check(fn_name, st)
     return (q, k) if in_place else (q_out, k_out)
 
@@ -188,6 +274,7 @@ def _rope(fn_name, q, k, cu_seqlens, theta, in_place, q_out, k_out, cos_sin_cach
 def rope_qk_fwd(q, k, cu_seqlens, theta: float, in_place: bool = True, q_out=None, k_out=None,
                 cos_sin_cache=None, stream=None):
     """Rotate Q [T, Hq, d] and K [T, Hkv, d] (bf16, CUDA) by their packed positions.
+    ``cos_sin_cache``: an optional ``CosSinCache`` built for the same theta and head_dim.
     Returns (q, k) in place, else (q_out, k_out)."""
     return _rope("rope_qk_fwd", q, k, cu_seqlens, theta, in_place, q_out, k_out, cos_sin_cache, stream)
 
@@ -199,39 +286,34 @@ def rope_qk_bwd(q, k, cu_seqlens, theta: float, in_place: bool = True, q_out=Non
     return _rope("rope_qk_bwd", q, k, cu_seqlens, theta, in_place, q_out, k_out, cos_sin_cache, stream)
 
 
-def rope_cos_sin_cache_build(cache, theta: float, stream=None, position_scale: float = 1.0):
+def rope_cos_sin_cache_build(data, theta: float, stream=None, position_scale: float = 1.0) -> CosSinCache:
     """Fill a float32 [rows, 4, head_dim/16, 4] CUDA tensor with (cos, sin) per position
-    (entry [p, q, c] = c_j, s_j, c_j+1, s_j+1 for j = 8c + 2q).  A position_scale other
-    than 1 builds the cache of the linearly rescaled rotation."""
+    (entry [p, q, c] = c_j, s_j, c_j+1, s_j+1 for j = 8c + 2q) for one theta and linear
+    position_scale, and return it as a ``CosSinCache`` with the library's descriptor."""
     import torch
 
-    if cache.dtype != torch.float32 or not cache.is_cuda or not cache.is_contiguous() or \
-            cache.dim() != 4 or cache.shape[1] != 4 or cache.shape[3] != 4:
+    if data.dtype != torch.float32 or not data.is_cuda or not data.is_contiguous() or \
+            data.dim() != 4 or data.shape[1] != 4 or data.shape[3] != 4:
         raise ValueError("cache must be a contiguous CUDA float32 [rows, 4, head_dim/16, 4] tensor")
-    lib = load_library()
-    st_ = _stream(stream, cache.device)
-    if position_scale == 1.0:
-        st = _on(cache.device, lib.rope_cos_sin_cache_build, _ptr(cache), cache.shape[0], 16 * cache.shape[2],
-                 float(theta), st_)
-        _check("rope_cos_sin_cache_build", st)
-    else:
-        st = _on(cache.device, lib.rope_cos_sin_cache_build_scaled, _ptr(cache), cache.shape[0],
-                 16 * cache.shape[2], float(theta), float(position_scale), st_)
-        _check("rope_cos_sin_cache_build_scaled", st)
-    return cache
+    desc = RopeCosSinCacheDesc()
+    st = _on(data.device, load_library().rope_cos_sin_cache_build, ctypes.byref(desc), _ptr(data), data.shape[0],
+             16 * data.shape[2], float(theta), float(position_scale), _stream(stream, data.device))
+    _check("rope_cos_sin_cache_build", st)
+    return CosSinCache(data, desc)
 
 
 def new_cos_sin_cache(rows: int, head_dim: int, theta: float, device="cuda", stream=None,
-                      position_scale: float = 1.0):
-    """Allocate (through torch) and fill a cos/sin cache of ``rows`` positions."""
+                      position_scale: float = 1.0) -> CosSinCache:
+    """Allocate (through torch) and build a cos/sin cache of ``rows`` positions."""
     import torch
 
-    cache = torch.empty((rows, 4, head_dim // 16, 4), dtype=torch.float32, device=device)
-    return rope_cos_sin_cache_build(cache, theta, stream, position_scale)
+    data = torch.empty((rows, 4, head_dim // 16, 4), dtype=torch.float32, device=device)
+    return rope_cos_sin_cache_build(data, theta, stream, position_scale)
 
 
 def cache_as_cos_sin(cache_np):
-    """View a cache copied to the host (numpy [rows, 4, d/16, 4]) as [rows, d/2, 2] (c, s)."""
+    """View a cache table copied to the host (numpy [rows, 4, d/16, 4]) as [rows, d/2, 2]
+    (c, s)."""
     rows, _, cph, _ = cache_np.shape
     return cache_np.transpose(0, 2, 1, 3).reshape(rows, 8 * cph, 2)
 
@@ -280,18 +362,21 @@ def _view_args(t, name):
     return _ptr(t), t.stride(0), t.stride(1)
 
 
-def rope_qk_apply(q, k, theta: float, cu_seqlens=None, position_ids=None, backward: bool = False,
-                  q_out=None, k_out=None, token_offset: int = 0, position_scale: float = 1.0,
-                  cos_sin_cache=None, stream=None, seq_used=None):
-    """General form of the rotation (C entry point ``rope_qk_apply``).
+def _segments_arg(segments, T: int):
+    """(ctypes array, count) of a list of (row_start, token_start) pairs."""
+    if segments is None:
+        return None, 0
+    segs = [(int(a), int(b)) for a, b in segments]
+    if not 1 <= len(segs) <= ROPE_MAX_SEGMENTS:
+        raise ValueError("give 1 to %d segments" % ROPE_MAX_SEGMENTS)
+    arr = (RopeQKSegment * len(segs))(*[RopeQKSegment(a, b) for a, b in segs])
+    return arr, len(segs)
 
-    q, k: bf16 CUDA views [T, Hq, d] and [T, Hkv, d] with any token/head strides
-    (head_dim contiguous) -- e.g. the Q and K slices of one fused QKV output, rotated in
-    place.  Positions come from ``position_ids`` (int32 or int64 [T]) if given, else from
-    ``cu_seqlens`` with row r read as token ``token_offset + r`` (and, with
-    ``seq_used``, only the first seq_used[s] tokens of sample s rotated).
-    ``position_scale`` is the linear position rescale (1 = none).  Returns (q, k) in place, else (q_out,
-    k_out)."""
+
+def _apply_desc(q, k, theta, cu_seqlens, position_ids, backward, q_out, k_out, token_offset, position_scale,
+                cos_sin_cache, seq_used, segments):
+    """The descriptor of a rope_qk_apply call (and the objects it points into, which must
+    outlive the call)."""
     qp, q_ts, q_hs = _view_args(q, "q")
     kp, k_ts, k_hs = _view_args(k, "k")
     if q.shape[0] != k.shape[0] or q.shape[2] != k.shape[2] or q.device != k.device:
@@ -308,41 +393,81 @@ def rope_qk_apply(q, k, theta: float, cu_seqlens=None, position_ids=None, backwa
             raise ValueError("q_out/k_out must have the shapes and device of q/k")
         desc.q_out, desc.q_out_stride_token, desc.q_out_stride_head = _view_args(q_out, "q_out")
         desc.k_out, desc.k_out_stride_token, desc.k_out_stride_head = _view_args(k_out, "k_out")
-    if position_ids is not None:
-        import torch
-
-        if position_ids.dtype not in (torch.int32, torch.int64) or position_ids.device != q.device or \
-                not position_ids.is_contiguous() or position_ids.numel() != T:
-            raise ValueError("position_ids must be a contiguous int32 or int64 [tokens] tensor on the device of q")
-        desc.position_ids = _ptr(position_ids)
-        if position_ids.dtype == torch.int64:
-            desc.flags |= ROPE_FLAG_POSITION_IDS_INT64
-    elif cu_seqlens is not None:
-        _check_cu(cu_seqlens, q.device)
-        desc.cu_seqlens = _ptr(cu_seqlens)
-        desc.n_seqs = cu_seqlens.numel() - 1
-        if seq_used is not None:
-            _check_cu(seq_used, q.device)
-            if seq_used.numel() != desc.n_seqs:
-                raise ValueError("seq_used must hold one int32 per sample")
-            desc.seq_used = _ptr(seq_used)
-    else:
-        raise ValueError("give cu_seqlens or position_ids")
+    _positions_args(desc, T, q.device, cu_seqlens, position_ids, seq_used)
+    seg_arr, desc.n_segments = _segments_arg(segments, T)
+    if seg_arr is not None:
+        desc.segments = seg_arr
     desc.n_q_heads, desc.n_kv_heads, desc.head_dim = hq, k.shape[1], d
     desc.total_tokens = T
     desc.token_offset = int(token_offset)
     desc.theta = float(theta)
     desc.position_scale = float(position_scale)
-    if cos_sin_cache is not None:
-        if cos_sin_cache.dim() != 4 or tuple(cos_sin_cache.shape[1:]) != (4, d // 16, 4) or \
-                not cos_sin_cache.is_contiguous() or cos_sin_cache.device != q.device:
-            raise ValueError("cos_sin_cache must be a contiguous float32 [rows, 4, head_dim/16, 4] tensor")
-        desc.cos_sin_cache = _ptr(cos_sin_cache)
-        desc.cache_rows = cos_sin_cache.shape[0]
+    cache = _cache_arg(cos_sin_cache, d, q.device)
+    if cache is not None:
+        desc.cos_sin_cache = cache
     desc.backward = 1 if backward else 0
+    return desc, (seg_arr, cache)
+
+
+def rope_qk_apply(q, k, theta: float, cu_seqlens=None, position_ids=None, backward: bool = False,
+                  q_out=None, k_out=None, token_offset: int = 0, position_scale: float = 1.0,
+                  cos_sin_cache=None, stream=None, seq_used=None, segments=None):
+    """General form of the rotation (C entry point ``rope_qk_apply``).
+
+    q, k: bf16 CUDA views [T, Hq, d] and [T, Hkv, d] with any token/head strides
+    (head_dim contiguous) -- e.g. the Q and K slices of one fused QKV output, rotated in
+    place.  Positions come from ``position_ids`` (int32 or int64 [T]) if given, else from
+    ``cu_seqlens`` with row r read as token ``token_offset + r`` (and, with
+    ``seq_used``, only the first seq_used[s] tokens of sample s rotated).  ``segments``:
+    a list of (row_start, token_start) pairs, rows from row_start on being tokens
+    token_start, token_start + 1, ... (a context-parallel rank's non-adjacent shards in
+    one call; see ``cp_shards``).  ``position_scale`` is the linear position rescale
+    (1 = none).  Returns (q, k) in place, else (q_out, k_out)."""
+    desc, keep = _apply_desc(q, k, theta, cu_seqlens, position_ids, backward, q_out, k_out, token_offset,
+                             position_scale, cos_sin_cache, seq_used, segments)
     st = _on(q.device, load_library().rope_qk_apply, ctypes.byref(desc), _stream(stream, q.device))
+    del keep
     _check("rope_qk_apply", st)
     return (q, k) if q_out is None else (q_out, k_out)
+
+
+def rope_qk_launch_info(q, k, theta: float, cu_seqlens=None, position_ids=None, backward: bool = False,
+                        q_out=None, k_out=None, token_offset: int = 0, position_scale: float = 1.0,
+                        cos_sin_cache=None, seq_used=None, segments=None) -> RopeQKLaunch:
+    """What ``rope_qk_apply`` with the same arguments would launch (C entry point
+    ``rope_qk_launch_info``; no launch, no CUDA call): ``.kernel_name()``, grid, tile."""
+    desc, keep = _apply_desc(q, k, theta, cu_seqlens, position_ids, backward, q_out, k_out, token_offset,
+                             position_scale, cos_sin_cache, seq_used, segments)
+    info = RopeQKLaunch()
+    st = load_library().rope_qk_launch_info(ctypes.byref(desc), ctypes.byref(info))
+    del keep
+    _check("rope_qk_launch_info", st)
+    return info
+
+
+def _positions_args(desc, T: int, device, cu_seqlens, position_ids, seq_used):
+    """Fill the position source of a descriptor: int32/int64 position ids, or cu_seqlens
+    (with seq_used), all contiguous tensors on ``device``."""
+    import torch
+
+    if position_ids is not None:
+        if position_ids.dtype not in (torch.int32, torch.int64) or position_ids.device != device or \
+                not position_ids.is_contiguous() or position_ids.numel() != T:
+            raise ValueError("position_ids must be a contiguous int32 or int64 [tokens] tensor on %s" % device)
+        desc.position_ids = _ptr(position_ids)
+        if position_ids.dtype == torch.int64:
+            desc.flags |= ROPE_FLAG_POSITION_IDS_INT64
+    elif cu_seqlens is not None:
+        _check_cu(cu_seqlens, device)
+        desc.cu_seqlens = _ptr(cu_seqlens)
+        desc.n_seqs = cu_seqlens.numel() - 1
+        if seq_used is not None:
+            _check_cu(seq_used, device)
+            if seq_used.numel() != desc.n_seqs:
+                raise ValueError("seq_used must hold one int32 per sample")
+            desc.seq_used = _ptr(seq_used)
+    else:
+        raise ValueError("give cu_seqlens or position_ids")
 
 
 def rope_qk_abi_version() -> int:
@@ -400,15 +525,17 @@ def glu_bwd(kind: str, dh, e, g, de=None, dg=None, stream=None):
 
 def rope_qk_host(q, k, theta: float, workspace=None, cu_seqlens=None, position_ids=None, backward: bool = False,
                  q_out=None, k_out=None, token_offset: int = 0, position_scale: float = 1.0,
-                 cos_sin_cache=None, stream=None, device=None, seq_used=None):
+                 cos_sin_cache=None, stream=None, device=None, seq_used=None, segments=None):
     """Rotate Q [T, Hq, d] and K [T, Hkv, d] that live in HOST memory (contiguous bf16 CPU
     tensors, pinned for overlapped copies), streaming them through ``workspace`` (a
     CUDA tensor of any dtype used as raw staging memory).  Without a workspace the
     library's built-in 32 MiB staging array is used and nothing is allocated
     (``rope_qk_host_static``; ``device`` then names the GPU).  cu_seqlens /
-    position_ids / cos_sin_cache / seq_used (with cu_seqlens: the used tokens of each
-    sample of a padded batch) are CUDA tensors.  Asynchronous on ``stream``:
-    synchronise it before reading the results.  Returns (q, k) or (q_out, k_out)."""
+    position_ids / seq_used (with cu_seqlens: the used tokens of each sample of a
+    padded batch) are CUDA tensors; cos_sin_cache a ``CosSinCache`` on the same GPU;
+    segments as for ``rope_qk_apply``.  q_out and k_out, if given, are host tensors of
+    exactly q's and k's shapes.  Asynchronous on ``stream``: synchronise it before
+    reading the results.  Returns (q, k) or (q_out, k_out)."""
     import torch
 
     for name, t in (("q", q), ("k", k), ("q_out", q_out), ("k_out", k_out)):
@@ -420,6 +547,8 @@ def rope_qk_host(q, k, theta: float, workspace=None, cu_seqlens=None, position_i
         raise ValueError("q and k must share tokens and head_dim")
     if (q_out is None) != (k_out is None):
         raise ValueError("give both q_out and k_out, or neither")
+    if q_out is not None and (q_out.shape != q.shape or k_out.shape != k.shape):
+        raise ValueError("q_out and k_out must have exactly the shapes of q and k")
     if workspace is not None and (not workspace.is_cuda or not workspace.is_contiguous()):
         raise ValueError("workspace must be a contiguous CUDA tensor")
     T, hq, d = q.shape
@@ -429,35 +558,26 @@ def rope_qk_host(q, k, theta: float, workspace=None, cu_seqlens=None, position_i
         dev = torch.device(device)
     else:
         dev = torch.device("cuda", torch.cuda.current_device())
+    if dev.type != "cuda":
+        raise ValueError("the staging device must be a CUDA device")
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    cache = _cache_arg(cos_sin_cache, d, dev)
     desc = RopeQKDesc()
     desc.q, desc.q_stride_token, desc.q_stride_head = _ptr(q), hq * d, d
     desc.k, desc.k_stride_token, desc.k_stride_head = _ptr(k), k.shape[1] * d, d
     if q_out is not None:
         desc.q_out, desc.q_out_stride_token, desc.q_out_stride_head = _ptr(q_out), hq * d, d
         desc.k_out, desc.k_out_stride_token, desc.k_out_stride_head = _ptr(k_out), k.shape[1] * d, d
-    if position_ids is not None:
-        if position_ids.dtype not in (torch.int32, torch.int64) or position_ids.device != dev or \
-                not position_ids.is_contiguous() or position_ids.numel() != T:
-            raise ValueError("position_ids must be a contiguous int32 or int64 [tokens] tensor on the "
-                             "workspace's device")
-        desc.position_ids = _ptr(position_ids)
-        if position_ids.dtype == torch.int64:
-            desc.flags |= ROPE_FLAG_POSITION_IDS_INT64
-    elif cu_seqlens is not None:
-        _check_cu(cu_seqlens, dev)
-        desc.cu_seqlens, desc.n_seqs = _ptr(cu_seqlens), cu_seqlens.numel() - 1
-        if seq_used is not None:
-            _check_cu(seq_used, dev)
-            if seq_used.numel() != desc.n_seqs:
-                raise ValueError("seq_used must hold one int32 per sample")
-            desc.seq_used = _ptr(seq_used)
-    else:
-        raise ValueError("give cu_seqlens or position_ids")
+    _positions_args(desc, T, dev, cu_seqlens, position_ids, seq_used)
+    seg_arr, desc.n_segments = _segments_arg(segments, T)
+    if seg_arr is not None:
+        desc.segments = seg_arr
     desc.n_q_heads, desc.n_kv_heads, desc.head_dim = hq, k.shape[1], d
     desc.total_tokens, desc.token_offset = T, int(token_offset)
     desc.theta, desc.position_scale = float(theta), float(position_scale)
-    if cos_sin_cache is not None:
-        desc.cos_sin_cache, desc.cache_rows = _ptr(cos_sin_cache), cos_sin_cache.shape[0]
+    if cache is not None:
+        desc.cos_sin_cache = cache
     desc.backward = 1 if backward else 0
     if workspace is None:
         # no workspace: the library's own static staging array (rope_qk_host_static)

@@ -7,6 +7,7 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -15,6 +16,8 @@
 
 // rope_qk_apply with plain (not programmatically overlapped) launches (rope_qk.cu).
 int rope_qk_apply_plain_launch(const rope_qk_desc *desc, void *stream);
+// rope_qk_apply's checks that do not depend on where Q and K live (rope_qk.cu).
+int rope_qk_check_pack(const rope_qk_desc *desc);
 
 namespace {
 
@@ -60,6 +63,36 @@ bool contiguous(const void *p, int64_t ts, int64_t hs, int32_t heads, int32_t d)
     return p == nullptr || (hs == d && ts == static_cast<int64_t>(heads) * d);
 }
 
+// Everything a host-buffer call can be rejected for, checked on the whole pack before
+// the first copy: the checks of rope_qk_apply that do not depend on where Q and K live
+// (sizes, flags, theta and scale, positions, segments, the cache), the host buffers'
+// layout, and the cache's device.  Every chunk's rotation then takes a descriptor that
+// passes rope_qk_apply's checks (its views are slices of the staging memory, its
+// positions a slice of the pack's), so no error other than one of the CUDA runtime can
+// come after a copy.  Returns ROPE_OK for a call with work to do.
+int check_host_call(const rope_qk_desc *dp)
+{
+    int rc = rope_qk_check_pack(dp);
+    if (rc != ROPE_OK) return rc;
+    const rope_qk_desc &p = *dp;
+    if (p.total_tokens == 0) return ROPE_OK;
+    if (p.q == nullptr || p.k == nullptr) return ROPE_ERR_NULL;
+    if ((p.q_out == nullptr) != (p.k_out == nullptr)) return ROPE_ERR_NULL;
+    const int32_t d = p.head_dim;
+    if (!contiguous(p.q, p.q_stride_token, p.q_stride_head, p.n_q_heads, d) ||
+        !contiguous(p.k, p.k_stride_token, p.k_stride_head, p.n_kv_heads, d) ||
+        !contiguous(p.q_out, p.q_out_stride_token, p.q_out_stride_head, p.n_q_heads, d) ||
+        !contiguous(p.k_out, p.k_out_stride_token, p.k_out_stride_head, p.n_kv_heads, d))
+        return ROPE_ERR_SHAPE;
+    const rope_cos_sin_cache *c = p.cos_sin_cache;
+    if (c != nullptr && c->rows > 0) {
+        int dev = -1;
+        if (cudaGetDevice(&dev) != cudaSuccess) return ROPE_ERR_LAUNCH;
+        if (dev != c->device) return ROPE_ERR_CACHE;
+    }
+    return ROPE_OK;
+}
+
 // The position ids of rows [t0, ...) of a chunk: int32 or, with the flag, int64 values.
 const int32_t *ids_from(const rope_qk_desc &p, int64_t t0)
 {
@@ -68,39 +101,61 @@ const int32_t *ids_from(const rope_qk_desc &p, int64_t t0)
     return p.position_ids + t0;
 }
 
+// Descriptor of the rotation of rows [t0, t0 + n) of the pack, staged in place at dq
+// (Q rows) and dk (K rows): the pack's descriptor with contiguous device views, its
+// position ids, token offset or segment list moved to the chunk's first row.  `segs`
+// receives the chunk's segments (the pack's, cut to the chunk and re-based).
+rope_qk_desc chunk_desc(const rope_qk_desc &p, int64_t t0, int64_t n, void *dq, void *dk, rope_qk_segment *segs)
+{
+    rope_qk_desc cd = p;
+    const int64_t d = p.head_dim;
+    cd.q = dq;
+    cd.k = dk;
+    cd.q_stride_token = p.n_q_heads * d;
+    cd.q_stride_head = d;
+    cd.k_stride_token = p.n_kv_heads * d;
+    cd.k_stride_head = d;
+    cd.q_out = nullptr;
+    cd.k_out = nullptr;
+    cd.total_tokens = n;
+    if (p.position_ids != nullptr) {
+        cd.position_ids = ids_from(p, t0);
+    } else if (p.n_segments == 0) {
+        cd.token_offset = p.token_offset + t0;
+    } else {
+        int m = 0;
+        for (int i = 0; i < p.n_segments; ++i) {
+            const int64_t s0 = p.segments[i].row_start;
+            const int64_t s1 = i + 1 < p.n_segments ? p.segments[i + 1].row_start : p.total_tokens;
+            const int64_t lo = std::max(s0, t0), hi = std::min(s1, t0 + n);
+            if (lo >= hi) continue;
+            segs[m].row_start = lo - t0;
+            segs[m].token_start = p.segments[i].token_start + (lo - s0);
+            ++m;
+        }
+        cd.segments = segs;
+        cd.n_segments = m;
+    }
+    return cd;
+}
+
 }  // namespace
 
 // Shared by rope_qk_host and its static-workspace variant: stream the pack through
 // `workspace` (device, workspace_bytes) on `stream`.
 int rope_qk_host_impl(const rope_qk_desc *dp, void *workspace, int64_t workspace_bytes, void *stream)
 {
-    if (dp == nullptr) return ROPE_ERR_NULL;
+    int rc = check_host_call(dp);
+    if (rc != ROPE_OK) return rc;
     const rope_qk_desc &p = *dp;
     const int64_t T = p.total_tokens;
-    if (T < 0 || p.n_q_heads < 1 || p.n_kv_heads < 1 || p.token_offset < 0 || workspace_bytes < 0)
-        return ROPE_ERR_SHAPE;
-    if ((p.flags & ~ROPE_FLAG_POSITION_IDS_INT64) != 0) return ROPE_ERR_UNSUPPORTED;
-    if (p.head_dim < 16 || p.head_dim > 256 || p.head_dim % 16 != 0) return ROPE_ERR_HEAD_DIM;
+    if (workspace_bytes < 0) return ROPE_ERR_SHAPE;
     if (T == 0) return ROPE_OK;
-    if (p.q == nullptr || p.k == nullptr || workspace == nullptr) return ROPE_ERR_NULL;
-    if ((p.q_out == nullptr) != (p.k_out == nullptr)) return ROPE_ERR_NULL;
-    const int32_t d = p.head_dim;
-    if (!contiguous(p.q, p.q_stride_token, p.q_stride_head, p.n_q_heads, d) ||
-        !contiguous(p.k, p.k_stride_token, p.k_stride_head, p.n_kv_heads, d) ||
-        !contiguous(p.q_out, p.q_out_stride_token, p.q_out_stride_head, p.n_q_heads, d) ||
-        !contiguous(p.k_out, p.k_out_stride_token, p.k_out_stride_head, p.n_kv_heads, d))
-        return ROPE_ERR_SHAPE;
+    if (workspace == nullptr) return ROPE_ERR_NULL;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ROPE_ERR_ALIGN;
-    // what rope_qk_apply would reject for the whole pack is rejected before any copy
-    if (!(p.theta > 0.0) || p.theta > 1.7e308 || !(p.position_scale > 0.0) || p.position_scale > 1.7e308)
-        return ROPE_ERR_THETA;
-    if (p.position_ids == nullptr && p.cu_seqlens == nullptr) return ROPE_ERR_NULL;
-    if (p.position_ids == nullptr && (p.n_seqs < 0 || p.token_offset + T > (int64_t(1) << 24)))
-        return p.n_seqs < 0 ? ROPE_ERR_SHAPE : ROPE_ERR_UNSUPPORTED;
-    if (p.cos_sin_cache != nullptr && (reinterpret_cast<uintptr_t>(p.cos_sin_cache) & 15u) != 0) return ROPE_ERR_ALIGN;
-    if (p.cache_rows < 0) return ROPE_ERR_SHAPE;
 
     // chunk geometry: two slots, each holding the Q and K rows of `chunk` tokens
+    const int32_t d = p.head_dim;
     const int64_t q_row = static_cast<int64_t>(p.n_q_heads) * d * 2;
     const int64_t k_row = static_cast<int64_t>(p.n_kv_heads) * d * 2;
     const int64_t per_token = q_row + k_row;
@@ -108,16 +163,17 @@ int rope_qk_host_impl(const rope_qk_desc *dp, void *workspace, int64_t workspace
     chunk -= chunk % 8;                       // keep every slot's K part 16-byte aligned
     if (chunk < 8) return ROPE_ERR_UNSUPPORTED;
     if (chunk > T) chunk = T;
+    if (chunk > (int64_t(1) << 24)) chunk = int64_t(1) << 24;
     const int64_t slot_bytes = ((chunk * per_token) + 255) / 256 * 256;
 
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceQueues *qs = nullptr;
-    int rc = queues_for_current_device(&qs);
+    rc = queues_for_current_device(&qs);
     if (rc != ROPE_OK) return rc;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // On an early return the caller's stream still waits for every copy already queued,
-    // so that freeing or reusing the workspace or the host buffers after the error is
-    // ordered after them.
+    // After a failure of the CUDA runtime the caller's stream still waits for every copy
+    // already queued, so that freeing or reusing the workspace or the host buffers after
+    // the error is ordered after them.
     auto join = [&]() {
         if (cudaEventRecord(qs->loaded[0], qs->h2d) == cudaSuccess) cudaStreamWaitEvent(s, qs->loaded[0], 0);
         if (cudaEventRecord(qs->drained[0], qs->d2h) == cudaSuccess) cudaStreamWaitEvent(s, qs->drained[0], 0);
@@ -145,18 +201,8 @@ int rope_qk_host_impl(const rope_qk_desc *dp, void *workspace, int64_t workspace
         // 2. rotate the chunk in place in the slot, on the caller's stream
         ok = ok && cudaStreamWaitEvent(s, qs->loaded[slot], 0) == cudaSuccess;
         if (!ok) break;
-        rope_qk_desc cd = p;
-        cd.q = dq;
-        cd.k = dk;
-        cd.q_stride_token = p.n_q_heads * static_cast<int64_t>(d);
-        cd.q_stride_head = d;
-        cd.k_stride_token = p.n_kv_heads * static_cast<int64_t>(d);
-        cd.k_stride_head = d;
-        cd.q_out = nullptr;
-        cd.k_out = nullptr;
-        cd.total_tokens = n;
-        if (p.position_ids != nullptr) cd.position_ids = ids_from(p, t0);
-        else cd.token_offset = p.token_offset + t0;
+        rope_qk_segment segs[ROPE_MAX_SEGMENTS];
+        const rope_qk_desc cd = chunk_desc(p, t0, n, dq, dk, segs);
         rc = rope_qk_apply_plain_launch(&cd, stream);
         if (rc != ROPE_OK) {
             join();
@@ -200,12 +246,11 @@ static __device__ __align__(256) unsigned char g_static_staging[kStaticStagingBy
 
 extern "C" int rope_qk_host_static(const rope_qk_desc *desc, void *stream)
 {
-    if (desc == nullptr) return ROPE_ERR_NULL;
+    int rc = check_host_call(desc);
+    if (rc != ROPE_OK) return rc;
     const rope_qk_desc &p = *desc;
-    if (p.total_tokens < 0 || p.n_q_heads < 1 || p.n_kv_heads < 1) return ROPE_ERR_SHAPE;
-    if ((p.flags & ~ROPE_FLAG_POSITION_IDS_INT64) != 0) return ROPE_ERR_UNSUPPORTED;
-    if (p.head_dim < 16 || p.head_dim > 256 || p.head_dim % 16 != 0) return ROPE_ERR_HEAD_DIM;
-    if (p.total_tokens == 0) return ROPE_OK;
+    const int64_t T = p.total_tokens;
+    if (T == 0) return ROPE_OK;
     const int64_t q_row = static_cast<int64_t>(p.n_q_heads) * p.head_dim * 2;
     const int64_t k_row = static_cast<int64_t>(p.n_kv_heads) * p.head_dim * 2;
     // one chunk must hold at least one token's Q and K rows
@@ -224,18 +269,9 @@ extern "C" int rope_qk_host_static(const rope_qk_desc *desc, void *stream)
         }
         staging = g_static_staging_addr[dev];
     }
-    if (p.q == nullptr || p.k == nullptr) return ROPE_ERR_NULL;
-    if ((p.q_out == nullptr) != (p.k_out == nullptr)) return ROPE_ERR_NULL;
-    const int32_t d = p.head_dim;
-    if (!contiguous(p.q, p.q_stride_token, p.q_stride_head, p.n_q_heads, d) ||
-        !contiguous(p.k, p.k_stride_token, p.k_stride_head, p.n_kv_heads, d) ||
-        !contiguous(p.q_out, p.q_out_stride_token, p.q_out_stride_head, p.n_q_heads, d) ||
-        !contiguous(p.k_out, p.k_out_stride_token, p.k_out_stride_head, p.n_kv_heads, d))
-        return ROPE_ERR_SHAPE;
 
     // one slot, everything in order on the caller's stream: copy a chunk in, rotate it,
     // copy it out, next chunk
-    const int64_t T = p.total_tokens;
     int64_t chunk = kStaticStagingBytes / (q_row + k_row);
     if (chunk > T) chunk = T;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -250,19 +286,9 @@ extern "C" int rope_qk_host_static(const rope_qk_desc *desc, void *stream)
         if (cudaMemcpyAsync(dq, q_host + t0 * q_row, n * q_row, cudaMemcpyHostToDevice, s) != cudaSuccess ||
             cudaMemcpyAsync(dk, k_host + t0 * k_row, n * k_row, cudaMemcpyHostToDevice, s) != cudaSuccess)
             return ROPE_ERR_LAUNCH;
-        rope_qk_desc cd = p;
-        cd.q = dq;
-        cd.k = dk;
-        cd.q_stride_token = q_row / 2;
-        cd.q_stride_head = d;
-        cd.k_stride_token = k_row / 2;
-        cd.k_stride_head = d;
-        cd.q_out = nullptr;
-        cd.k_out = nullptr;
-        cd.total_tokens = n;
-        if (p.position_ids != nullptr) cd.position_ids = ids_from(p, t0);
-        else cd.token_offset = p.token_offset + t0;
-        const int rc = rope_qk_apply_plain_launch(&cd, stream);
+        rope_qk_segment segs[ROPE_MAX_SEGMENTS];
+        const rope_qk_desc cd = chunk_desc(p, t0, n, dq, dk, segs);
+        rc = rope_qk_apply_plain_launch(&cd, stream);
         if (rc != ROPE_OK) return rc;
         if (cudaMemcpyAsync(qo_host + t0 * q_row, dq, n * q_row, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
             cudaMemcpyAsync(ko_host + t0 * k_row, dk, n * k_row, cudaMemcpyDeviceToHost, s) != cudaSuccess)

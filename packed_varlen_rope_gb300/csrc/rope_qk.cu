@@ -43,6 +43,7 @@ constexpr int kThreads = 128;           // threads per CTA (10 CTAs per SM at 48
 constexpr int kUnroll = 2;              // pair units in flight per thread (4 x 16-byte loads)
 constexpr int kMaxHalf = 128;           // head_dim <= 256
 constexpr int kMaxTileTokens = 32;      // one warp resolves the tile's positions
+constexpr int kMaxSegments = ROPE_MAX_SEGMENTS;
 constexpr int64_t kMaxTokens = int64_t(1) << 24;   // positions < 2^24 are exact in fp32
 
 using pvr::FastDiv;
@@ -63,7 +64,9 @@ struct RopeArgs {
     const float4 *cache;
     int32_t n_seqs;
     int32_t n_tokens;
-    int32_t token_offset;                    // row r is token token_offset + r of cu's stream
+    int32_t n_seg;                           // >= 1 row segments (cu_seqlens positions)
+    int32_t seg_row[kMaxSegments];           // first row of segment i (seg_row[0] == 0)
+    int32_t seg_delta[kMaxSegments];         // row r of segment i is token r + seg_delta[i]
     int32_t hq;
     int32_t hkv;
     int32_t h_tot;
@@ -209,7 +212,10 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
                 const long long p = __ldg(a.pos_ids64 + r);
                 pos = (p >= 0 && p < static_cast<long long>(kMaxTokens)) ? static_cast<int>(p) : -1;
             } else {
-                pos = token_position(a.cu, a.n_seqs, a.token_offset + r, a.seq_used);
+                int seg = 0;
+                for (int i = 1; i < a.n_seg; ++i)
+                    if (r >= a.seg_row[i]) seg = i;
+                pos = token_position(a.cu, a.n_seqs, r + a.seg_delta[seg], a.seq_used);
             }
         }
         s_pos[threadIdx.x] = pos;
@@ -479,29 +485,128 @@ int check_view(const View &v)
     return ROPE_OK;
 }
 
-int rope_qk_apply_impl(const rope_qk_desc *dp, void *stream, bool pdl)
+// Check word of a cache descriptor: FNV-1a (64-bit) over the bytes of every other
+// field, so that a descriptor not written by the build, or changed after it, is caught.
+uint64_t cache_check_word(const rope_cos_sin_cache &c)
+{
+    uint64_t h = 1469598103934665603ull;
+    auto mix = [&h](const void *p, size_t n) {
+        const unsigned char *b = static_cast<const unsigned char *>(p);
+        for (size_t i = 0; i < n; ++i) {
+            h ^= b[i];
+            h *= 1099511628211ull;
+        }
+    };
+    const uintptr_t data = reinterpret_cast<uintptr_t>(c.data);
+    mix(&data, sizeof data);
+    mix(&c.rows, sizeof c.rows);
+    mix(&c.head_dim, sizeof c.head_dim);
+    mix(&c.device, sizeof c.device);
+    mix(&c.theta, sizeof c.theta);
+    mix(&c.position_scale, sizeof c.position_scale);
+    return h;
+}
+
+// The cache serves this rotation: written by the build, for the same head_dim, theta
+// and position_scale, with a table inside the limits the build enforces.
+int check_cache(const rope_cos_sin_cache *c, int32_t head_dim, double theta, double scale)
+{
+    if (c == nullptr) return ROPE_OK;
+    if (c->check != cache_check_word(*c)) return ROPE_ERR_CACHE;
+    if (c->head_dim != head_dim || !(c->theta == theta) || !(c->position_scale == scale)) return ROPE_ERR_CACHE;
+    if (c->rows < 0 || c->rows > kMaxTokens || (c->rows > 0 && c->data == nullptr)) return ROPE_ERR_CACHE;
+    if (c->data != nullptr && !aligned(c->data, 16)) return ROPE_ERR_ALIGN;
+    return ROPE_OK;
+}
+
+// A cache with rows is read by kernels of the current device only.
+int check_cache_device(const rope_cos_sin_cache *c)
+{
+    if (c == nullptr || c->rows == 0) return ROPE_OK;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ROPE_ERR_LAUNCH;
+    return dev == c->device ? ROPE_OK : ROPE_ERR_CACHE;
+}
+
+}  // namespace
+
+// Every check of a descriptor that does not depend on where Q and K live: sizes, flags,
+// theta and scale, the position source (cu_seqlens with an offset or segments, or
+// position ids) and the cache.  Shared by rope_qk_apply and the host-buffer entry
+// points, which run it on the whole pack before they copy anything.  No CUDA call.
+int rope_qk_check_pack(const rope_qk_desc *dp)
 {
     if (dp == nullptr) return ROPE_ERR_NULL;
     const rope_qk_desc &p = *dp;
     const int64_t T = p.total_tokens;
-    if (T < 0 || p.n_seqs < 0 || p.n_q_heads < 1 || p.n_kv_heads < 1 || p.cache_rows < 0 ||
-        p.token_offset < 0)
+    if (T < 0 || p.n_seqs < 0 || p.n_q_heads < 1 || p.n_kv_heads < 1 || p.token_offset < 0 ||
+        p.n_segments < 0 || p.n_segments > kMaxSegments)
         return ROPE_ERR_SHAPE;
     if (p.n_q_heads > (1 << 20) || p.n_kv_heads > (1 << 20)) return ROPE_ERR_SHAPE;
-    if ((p.flags & ~ROPE_FLAG_POSITION_IDS_INT64) != 0) return ROPE_ERR_UNSUPPORTED;
-    const bool ids64 = (p.flags & ROPE_FLAG_POSITION_IDS_INT64) != 0;
+    if ((p.flags & ~ROPE_FLAG_POSITION_IDS_INT64) != 0 || p.reserved != 0) return ROPE_ERR_UNSUPPORTED;
     int rc = check_head_dim(p.head_dim);
     if (rc != ROPE_OK) return rc;
     if ((rc = check_theta(p.theta)) != ROPE_OK) return rc;
     if ((rc = check_scale(p.position_scale)) != ROPE_OK) return rc;
-    // positions must stay exact in binary32: global token indices (cu_seqlens) below
-    // 2^24; explicit position ids outside [0, 2^24) are skipped by the kernel
-    if (p.position_ids == nullptr && p.token_offset + T > kMaxTokens) return ROPE_ERR_UNSUPPORTED;
-    if (T > INT32_MAX / 2) return ROPE_ERR_UNSUPPORTED;
     if (T == 0) return ROPE_OK;     // nothing is read or written; pointers may be NULL
-    if (p.position_ids == nullptr && p.cu_seqlens == nullptr) return ROPE_ERR_NULL;
-    if (p.cos_sin_cache != nullptr && !aligned(p.cos_sin_cache, 16)) return ROPE_ERR_ALIGN;
-    if (ids64 && p.position_ids != nullptr && !aligned(p.position_ids, 8)) return ROPE_ERR_ALIGN;
+    const bool ids64 = (p.flags & ROPE_FLAG_POSITION_IDS_INT64) != 0;
+    if (p.position_ids != nullptr) {
+        if (p.n_segments > 0) return ROPE_ERR_UNSUPPORTED;
+        if (ids64 && !aligned(p.position_ids, 8)) return ROPE_ERR_ALIGN;
+    } else {
+        // positions must stay exact in binary32: global token indices below 2^24
+        // (explicit position ids outside [0, 2^24) are skipped by the kernel instead)
+        if (p.cu_seqlens == nullptr) return ROPE_ERR_NULL;
+        if (p.n_segments == 0) {
+            if (p.token_offset + T > kMaxTokens) return ROPE_ERR_UNSUPPORTED;
+        } else {
+            if (p.segments == nullptr) return ROPE_ERR_NULL;
+            if (p.token_offset != 0 || p.segments[0].row_start != 0) return ROPE_ERR_SHAPE;
+            for (int i = 0; i < p.n_segments; ++i) {
+                const rope_qk_segment &g = p.segments[i];
+                const int64_t end = i + 1 < p.n_segments ? p.segments[i + 1].row_start : T;
+                if (g.row_start >= end || end > T || g.token_start < 0) return ROPE_ERR_SHAPE;
+                if (g.token_start > kMaxTokens || end - g.row_start > kMaxTokens - g.token_start)
+                    return ROPE_ERR_UNSUPPORTED;
+            }
+        }
+    }
+    return check_cache(p.cos_sin_cache, p.head_dim, p.theta, p.position_scale);
+}
+
+namespace {
+
+// What rope_qk_apply launches for a descriptor: the kernel's arguments, grid, shared
+// memory and instance (head_dim template, 0 = generic; 64-bit offsets or not).
+struct Launch {
+    RopeArgs a;
+    int grid = 0;
+    size_t smem = 0;
+    int d_instance = 0;
+    bool long_index = false;
+};
+
+int instance_for(int head_dim)
+{
+    switch (head_dim) {
+    case 64: case 96: case 128: case 256: return head_dim;
+    default: return 0;
+    }
+}
+
+// Every argument check of rope_qk_apply, then the launch plan.  With `check_device`,
+// also the cache's device (the one CUDA runtime call of the checks).  For T == 0
+// returns ROPE_OK with L->grid == 0 (nothing to launch).
+int plan_rotation(const rope_qk_desc *dp, Launch *L, bool check_device)
+{
+    int rc = rope_qk_check_pack(dp);
+    if (rc != ROPE_OK) return rc;
+    const rope_qk_desc &p = *dp;
+    const int64_t T = p.total_tokens;
+    L->grid = 0;
+    if (T == 0) return ROPE_OK;
+    if (T > INT32_MAX / 2) return ROPE_ERR_UNSUPPORTED;
+    const bool ids64 = (p.flags & ROPE_FLAG_POSITION_IDS_INT64) != 0;
 
     const int64_t d = p.head_dim;
     const View q{p.q, T, p.n_q_heads, p.q_stride_token, p.q_stride_head, d};
@@ -519,27 +624,42 @@ int rope_qk_apply_impl(const rope_qk_desc *dp, void *stream, bool pdl)
             for (const View *i : {&q, &k})
                 if (overlap(o->base, o->bytes(), i->base, i->bytes())) return ROPE_ERR_OVERLAP;
     }
+    if (check_device && (rc = check_cache_device(p.cos_sin_cache)) != ROPE_OK) return rc;
 
-    RopeArgs a{};
+    RopeArgs &a = L->a;
+    a = RopeArgs{};
     a.q_in = static_cast<const __nv_bfloat16 *>(p.q);
     a.k_in = static_cast<const __nv_bfloat16 *>(p.k);
     a.q_out = static_cast<__nv_bfloat16 *>(const_cast<void *>(qo.base));
     a.k_out = static_cast<__nv_bfloat16 *>(const_cast<void *>(ko.base));
     a.q_ts = q.ts;  a.q_hs = q.hs;  a.k_ts = k.ts;  a.k_hs = k.hs;
     a.qo_ts = qo.ts; a.qo_hs = qo.hs; a.ko_ts = ko.ts; a.ko_hs = ko.hs;
+    const bool ids = p.position_ids != nullptr;
     a.cu = p.cu_seqlens;
-    a.pos_ids = ids64 ? nullptr : p.position_ids;
-    a.pos_ids64 = ids64 ? reinterpret_cast<const long long *>(p.position_ids) : nullptr;
-    a.seq_used = p.position_ids != nullptr ? nullptr : p.seq_used;
-    a.cache = reinterpret_cast<const float4 *>(p.cos_sin_cache);
-    a.n_seqs = p.position_ids != nullptr ? 0 : p.n_seqs;
+    a.pos_ids = ids && !ids64 ? p.position_ids : nullptr;
+    a.pos_ids64 = ids && ids64 ? reinterpret_cast<const long long *>(p.position_ids) : nullptr;
+    a.seq_used = ids ? nullptr : p.seq_used;
+    const rope_cos_sin_cache *cache = p.cos_sin_cache;
+    a.cache = cache != nullptr && cache->rows > 0 ? reinterpret_cast<const float4 *>(cache->data) : nullptr;
+    a.cache_rows = a.cache != nullptr ? static_cast<int32_t>(cache->rows) : 0;
+    a.n_seqs = ids ? 0 : p.n_seqs;
     a.n_tokens = static_cast<int32_t>(T);
-    a.token_offset = static_cast<int32_t>(p.position_ids != nullptr ? 0 : p.token_offset);
+    // row r of segment i is token r + seg_delta[i] of cu_seqlens' stream (all below 2^24)
+    if (ids || p.n_segments == 0) {
+        a.n_seg = 1;
+        a.seg_row[0] = 0;
+        a.seg_delta[0] = ids ? 0 : static_cast<int32_t>(p.token_offset);
+    } else {
+        a.n_seg = p.n_segments;
+        for (int i = 0; i < p.n_segments; ++i) {
+            a.seg_row[i] = static_cast<int32_t>(p.segments[i].row_start);
+            a.seg_delta[i] = static_cast<int32_t>(p.segments[i].token_start - p.segments[i].row_start);
+        }
+    }
     a.hq = p.n_q_heads;
     a.hkv = p.n_kv_heads;
     a.h_tot = p.n_q_heads + p.n_kv_heads;
     a.head_dim = p.head_dim;
-    a.cache_rows = static_cast<int32_t>(p.cache_rows < kMaxTokens ? p.cache_rows : kMaxTokens);
     a.tile_tokens = pick_tile_tokens(a.h_tot, p.head_dim);
     a.in_place = in_place ? 1 : 0;
     a.bwd = p.backward ? 1 : 0;
@@ -547,26 +667,34 @@ int rope_qk_apply_impl(const rope_qk_desc *dp, void *stream, bool pdl)
     a.div_cph = make_fastdiv(static_cast<uint32_t>(p.head_dim / 16));
     host_inv_freq(p.theta, p.head_dim, p.position_scale, a.w);
 
-    const int grid = static_cast<int>((T + a.tile_tokens - 1) / a.tile_tokens);
-    const size_t smem = static_cast<size_t>(a.tile_tokens) * (p.head_dim / 2) * sizeof(float2);  // 4*cph float4 per token
+    L->grid = static_cast<int>((T + a.tile_tokens - 1) / a.tile_tokens);
+    L->smem = static_cast<size_t>(a.tile_tokens) * (p.head_dim / 2) * sizeof(float2);  // 4*cph float4 per token
     // 64-bit offsets only when some element offset of a view reaches 2^31
-    bool long_index = false;
+    L->long_index = false;
     for (const View *v : {&q, &k, &qo, &ko})
-        long_index = long_index || v->span_elems() > INT32_MAX;
+        L->long_index = L->long_index || v->span_elems() > INT32_MAX;
+    L->d_instance = instance_for(p.head_dim);
+    return ROPE_OK;
+}
+
+int rope_qk_apply_impl(const rope_qk_desc *dp, void *stream, bool pdl)
+{
+    Launch L;
+    const int rc = plan_rotation(dp, &L, true);
+    if (rc != ROPE_OK || L.grid == 0) return rc;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const cudaError_t err = long_index ? dispatch_dim<true>(a, grid, smem, s, pdl)
-                                       : dispatch_dim<false>(a, grid, smem, s, pdl);
+    const cudaError_t err = L.long_index ? dispatch_dim<true>(L.a, L.grid, L.smem, s, pdl)
+                                         : dispatch_dim<false>(L.a, L.grid, L.smem, s, pdl);
     return err == cudaSuccess ? ROPE_OK : ROPE_ERR_LAUNCH;
 }
 
 // The contiguous [T, H, d] form of the two simple entry points.
 int rope_qk_run(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_tokens,
                 int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, double theta,
-                int32_t in_place, void *q_out, void *k_out, const float *cache, int64_t cache_rows,
+                int32_t in_place, void *q_out, void *k_out, const rope_cos_sin_cache *cache,
                 void *stream, int bwd)
 {
-    if (total_tokens < 0 || n_seqs < 0 || n_q_heads < 1 || n_kv_heads < 1 || cache_rows < 0)
-        return ROPE_ERR_SHAPE;
+    if (total_tokens < 0 || n_seqs < 0 || n_q_heads < 1 || n_kv_heads < 1) return ROPE_ERR_SHAPE;
     // out of place needs both outputs (a desc with no outputs would mean in place)
     if (total_tokens > 0 && !in_place && (q_out == nullptr || k_out == nullptr)) return ROPE_ERR_NULL;
     rope_qk_desc p{};
@@ -588,7 +716,6 @@ int rope_qk_run(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs, int
     p.theta = theta;
     p.position_scale = 1.0;
     p.cos_sin_cache = cache;
-    p.cache_rows = cache_rows;
     return rope_qk_apply_impl(&p, stream, true);
 }
 
@@ -605,20 +732,20 @@ extern "C" {
 
 int rope_qk_fwd(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_tokens,
                 int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, double theta,
-                int32_t in_place, void *q_out, void *k_out, const float *cos_sin_cache,
-                int64_t cache_rows, void *stream)
+                int32_t in_place, void *q_out, void *k_out, const rope_cos_sin_cache *cos_sin_cache,
+                void *stream)
 {
     return rope_qk_run(q, k, cu_seqlens, n_seqs, total_tokens, n_q_heads, n_kv_heads, head_dim,
-                       theta, in_place, q_out, k_out, cos_sin_cache, cache_rows, stream, 0);
+                       theta, in_place, q_out, k_out, cos_sin_cache, stream, 0);
 }
 
 int rope_qk_bwd(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_tokens,
                 int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, double theta,
-                int32_t in_place, void *q_out, void *k_out, const float *cos_sin_cache,
-                int64_t cache_rows, void *stream)
+                int32_t in_place, void *q_out, void *k_out, const rope_cos_sin_cache *cos_sin_cache,
+                void *stream)
 {
     return rope_qk_run(q, k, cu_seqlens, n_seqs, total_tokens, n_q_heads, n_kv_heads, head_dim,
-                       theta, in_place, q_out, k_out, cos_sin_cache, cache_rows, stream, 1);
+                       theta, in_place, q_out, k_out, cos_sin_cache, stream, 1);
 }
 
 int64_t rope_cos_sin_cache_bytes(int64_t cache_rows, int32_t head_dim)
@@ -627,38 +754,60 @@ int64_t rope_cos_sin_cache_bytes(int64_t cache_rows, int32_t head_dim)
     return cache_rows * head_dim * static_cast<int64_t>(sizeof(float));
 }
 
-int rope_cos_sin_cache_build_scaled(float *cache, int64_t cache_rows, int32_t head_dim, double theta,
-                                    double position_scale, void *stream)
+int rope_cos_sin_cache_build(rope_cos_sin_cache *cache, float *data, int64_t rows, int32_t head_dim,
+                             double theta, double position_scale, void *stream)
 {
-    if (cache_rows < 0) return ROPE_ERR_SHAPE;
+    if (cache == nullptr) return ROPE_ERR_NULL;
+    if (rows < 0) return ROPE_ERR_SHAPE;
     int rc = check_head_dim(head_dim);
     if (rc != ROPE_OK) return rc;
     if ((rc = check_theta(theta)) != ROPE_OK) return rc;
     if ((rc = check_scale(position_scale)) != ROPE_OK) return rc;
-    if (cache_rows > kMaxTokens) return ROPE_ERR_UNSUPPORTED;
-    if (cache_rows == 0) return ROPE_OK;
-    if (cache == nullptr) return ROPE_ERR_NULL;
-    if (!aligned(cache, 16)) return ROPE_ERR_ALIGN;
-    CacheArgs a{};
-    host_inv_freq(theta, head_dim, position_scale, a.w);
-    const int cph = head_dim / 16;
-    const int64_t n = cache_rows * 4 * cph;
-    const int64_t blocks64 = (n + 255) / 256;
-    const int blocks = static_cast<int>(blocks64 < 152 * 64 ? blocks64 : 152 * 64);
-    cos_sin_cache_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        reinterpret_cast<float4 *>(cache), cache_rows, cph, a);
-    return cudaGetLastError() == cudaSuccess ? ROPE_OK : ROPE_ERR_LAUNCH;
-}
-
-int rope_cos_sin_cache_build(float *cache, int64_t cache_rows, int32_t head_dim, double theta,
-                             void *stream)
-{
-    return rope_cos_sin_cache_build_scaled(cache, cache_rows, head_dim, theta, 1.0, stream);
+    if (rows > kMaxTokens) return ROPE_ERR_UNSUPPORTED;
+    rope_cos_sin_cache c{};
+    c.data = data;
+    c.rows = rows;
+    c.head_dim = head_dim;
+    c.device = -1;                  // no rows: no table to read, valid on every device
+    c.theta = theta;
+    c.position_scale = position_scale;
+    if (rows > 0) {
+        if (data == nullptr) return ROPE_ERR_NULL;
+        if (!aligned(data, 16)) return ROPE_ERR_ALIGN;
+        if (cudaGetDevice(&c.device) != cudaSuccess) return ROPE_ERR_LAUNCH;
+        CacheArgs a{};
+        host_inv_freq(theta, head_dim, position_scale, a.w);
+        const int cph = head_dim / 16;
+        const int64_t n = rows * 4 * cph;
+        const int64_t blocks64 = (n + 255) / 256;
+        const int blocks = static_cast<int>(blocks64 < 152 * 64 ? blocks64 : 152 * 64);
+        cos_sin_cache_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+            reinterpret_cast<float4 *>(data), rows, cph, a);
+        if (cudaGetLastError() != cudaSuccess) return ROPE_ERR_LAUNCH;
+    }
+    c.check = cache_check_word(c);
+    *cache = c;
+    return ROPE_OK;
 }
 
 int rope_qk_apply(const rope_qk_desc *desc, void *stream)
 {
     return rope_qk_apply_impl(desc, stream, true);
+}
+
+int rope_qk_launch_info(const rope_qk_desc *desc, rope_qk_launch *info)
+{
+    if (info == nullptr) return ROPE_ERR_NULL;
+    Launch L;
+    const int rc = plan_rotation(desc, &L, false);
+    if (rc != ROPE_OK) return rc;
+    info->head_dim_instance = L.grid > 0 ? L.d_instance : 0;
+    info->long_index = L.grid > 0 && L.long_index ? 1 : 0;
+    info->grid = L.grid;
+    info->tile_tokens = L.grid > 0 ? L.a.tile_tokens : 0;
+    info->threads = L.grid > 0 ? kThreads : 0;
+    info->smem_bytes = static_cast<int32_t>(L.smem);
+    return ROPE_OK;
 }
 
 int rope_qk_positions(const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_tokens,
@@ -703,15 +852,19 @@ const char *rope_strerror(int status)
     switch (status) {
     case ROPE_OK: return "ok";
     case ROPE_ERR_NULL: return "a required pointer is NULL";
-    case ROPE_ERR_SHAPE: return "invalid size or stride: negative count/stride/offset or head count < 1";
+    case ROPE_ERR_SHAPE: return "invalid size, stride or segment list: negative count/stride/offset, head count < 1, "
+                                "segments not starting at row 0 or not increasing";
     case ROPE_ERR_HEAD_DIM: return "head_dim must be a multiple of 16 in [16, 256]";
-    case ROPE_ERR_ALIGN: return "Q/K/outputs and the cos/sin cache must be 16-byte aligned, strides multiples of 8 elements";
+    case ROPE_ERR_ALIGN: return "Q/K/outputs and the cos/sin cache must be 16-byte aligned (int64 position ids 8-byte), "
+                                "strides multiples of 8 elements";
     case ROPE_ERR_OVERLAP: return "Q and K overlap, a view overlaps itself, or an output overlaps an input";
     case ROPE_ERR_UNSUPPORTED: return "global token indices and cache rows must stay within 2^24 (exact fp32 positions)";
     case ROPE_ERR_LAUNCH: return "the CUDA runtime rejected a launch";
     case ROPE_ERR_THETA: return "theta and position_scale must be finite and > 0";
     case ROPE_ERR_KIND: return "unknown activation kind";
     case ROPE_ERR_WORKSPACE: return "one token's Q and K rows exceed the 32 MiB static staging array";
+    case ROPE_ERR_CACHE: return "the cos/sin cache was built for another theta, head_dim, position_scale or device, "
+                                "or its descriptor was not written by rope_cos_sin_cache_build";
     default: return "unknown rope status";
     }
 }

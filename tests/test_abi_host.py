@@ -18,6 +18,7 @@ HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.jo
 
 OK, ERR_NULL, ERR_SHAPE, ERR_HEAD_DIM, ERR_ALIGN, ERR_OVERLAP, ERR_UNSUPPORTED, ERR_LAUNCH, ERR_THETA = \
     0, -1, -2, -3, -4, -5, -6, -7, -8
+ERR_WORKSPACE, ERR_CACHE = -10, -11
 
 
 @pytest.fixture(scope="module")
@@ -54,15 +55,16 @@ def test_library_exports_every_declared_symbol(lib):
 def test_header_is_plain_c(tmp_path):
     src = tmp_path / "use_header.c"
     src.write_text('#include "rope_qk.h"\n#include "glu.h"\n'
-                   'int main(void) { return ROPE_QK_ABI_VERSION == 4 && GLU_GEGLU_TANH == 2 && ROPE_FLAG_POSITION_IDS_INT64 == 1 ? 0 : 1; }\n')
+                   'int main(void) { return ROPE_QK_ABI_VERSION == 5 && GLU_GEGLU_TANH == 2 && ROPE_FLAG_POSITION_IDS_INT64 == 1 &&\n'
+                   '    ROPE_MAX_SEGMENTS == 16 && ROPE_ERR_CACHE == -11 ? 0 : 1; }\n')
     subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Werror", "-pedantic", "-I", os.path.dirname(HEADER),
                            "-c", str(src), "-o", str(tmp_path / "use_header.o")])
 
 
 def test_abi_version_and_strerror(lib):
-    assert lib.rope_qk_abi_version() == 4
+    assert lib.rope_qk_abi_version() == 5
     for code in (OK, ERR_NULL, ERR_SHAPE, ERR_HEAD_DIM, ERR_ALIGN, ERR_OVERLAP, ERR_UNSUPPORTED,
-                 ERR_LAUNCH, ERR_THETA, -9, -10):
+                 ERR_LAUNCH, ERR_THETA, -9, ERR_WORKSPACE, ERR_CACHE):
         assert lib.rope_strerror(code)
     assert lib.rope_strerror(-99) == b"unknown rope status"
 
@@ -77,19 +79,22 @@ def test_inv_freq_matches_oracle_bits(lib, oracle_mod):
                                       oracle_mod.inv_freq(theta, d, scale)), (theta, d, scale)
 
 
-def test_desc_layout_matches_header(tmp_path):
-    """The ctypes mirror of rope_qk_desc has the C struct's offsets and size."""
-    from packed_varlen_rope_gb300 import RopeQKDesc
+@pytest.mark.parametrize("struct", ["rope_qk_desc", "rope_cos_sin_cache", "rope_qk_segment"])
+def test_desc_layout_matches_header(tmp_path, struct):
+    """The ctypes mirrors of the C structs have the C compiler's offsets and sizes."""
+    from packed_varlen_rope_gb300 import RopeCosSinCacheDesc, RopeQKDesc, RopeQKSegment
 
-    names = [f[0] for f in RopeQKDesc._fields_]
-    body = "".join('printf("%%zu\\n", offsetof(rope_qk_desc, %s));' % n for n in names)
+    cls = {"rope_qk_desc": RopeQKDesc, "rope_cos_sin_cache": RopeCosSinCacheDesc,
+           "rope_qk_segment": RopeQKSegment}[struct]
+    names = [f[0] for f in cls._fields_]
+    body = "".join('printf("%%zu\\n", offsetof(%s, %s));' % (struct, n) for n in names)
     src = tmp_path / "layout.c"
     src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "rope_qk.h"\n'
-                   'int main(void) { %s printf("%%zu\\n", sizeof(rope_qk_desc)); return 0; }\n' % body)
+                   'int main(void) { %s printf("%%zu\\n", sizeof(%s)); return 0; }\n' % (body, struct))
     exe = tmp_path / "layout"
     subprocess.check_call(["gcc", "-std=c99", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)])
     got = [int(v) for v in subprocess.check_output([str(exe)]).split()]
-    want = [getattr(RopeQKDesc, n).offset for n in names] + [ctypes.sizeof(RopeQKDesc)]
+    want = [getattr(cls, n).offset for n in names] + [ctypes.sizeof(cls)]
     assert got == want
 
 
@@ -103,9 +108,34 @@ def test_cache_bytes(lib):
 Q, K, QO, KO, CU, CACHE = 0x10000000, 0x20000000, 0x30000000, 0x40000000, 0x50000000, 0x60000000
 
 
+def cache_desc(lib, rows=0, d=64, theta=1e4, scale=1.0, data=None):
+    """A cache descriptor written by the library's build.  rows == 0 makes no CUDA call
+    (no table to fill); rows > 0 is forged from a 0-row build and resealed by the
+    test's own copy of the check word, to exercise the host checks without a GPU."""
+    from packed_varlen_rope_gb300 import RopeCosSinCacheDesc
+
+    c = RopeCosSinCacheDesc()
+    assert lib.rope_cos_sin_cache_build(ctypes.byref(c), data, 0, d, theta, scale, None) == OK
+    if rows:
+        c.rows, c.data, c.device = rows, data, 0
+        c.check = _fnv_check(c)
+    return c
+
+
+def _fnv_check(c):
+    import struct
+
+    h = 1469598103934665603
+    raw = struct.pack("<Qqiidd", c.data or 0, c.rows, c.head_dim, c.device, c.theta, c.position_scale)
+    for b in raw:
+        h = ((h ^ b) * 1099511628211) & 0xFFFFFFFFFFFFFFFF
+    return h
+
+
 def call(lib, fn="rope_qk_fwd", q=Q, k=K, cu=CU, n=4, T=0, hq=4, hkv=2, d=64, theta=1e4, in_place=1,
-         qo=None, ko=None, cache=None, rows=0):
-    return getattr(lib, fn)(q, k, cu, n, T, hq, hkv, d, theta, in_place, qo, ko, cache, rows, None)
+         qo=None, ko=None, cache=None):
+    return getattr(lib, fn)(q, k, cu, n, T, hq, hkv, d, theta, in_place, qo, ko,
+                            None if cache is None else ctypes.pointer(cache), None)
 
 
 @pytest.mark.parametrize("fn", ["rope_qk_fwd", "rope_qk_bwd"])
@@ -118,7 +148,6 @@ def test_argument_checks(lib, fn):
     assert c(n=-1) == ERR_SHAPE
     assert c(hq=0) == ERR_SHAPE
     assert c(hkv=0) == ERR_SHAPE
-    assert c(rows=-5) == ERR_SHAPE
     for d in (0, 8, 24, 65, 72, 272, 512):
         assert c(d=d) == ERR_HEAD_DIM, d
     for th in (0.0, -1.0, float("nan"), float("inf")):
@@ -132,8 +161,8 @@ def test_argument_checks(lib, fn):
     assert c(q=Q + 8) == ERR_ALIGN
     assert c(k=K + 2) == ERR_ALIGN
     assert c(in_place=0, qo=QO + 4, ko=KO) == ERR_ALIGN
-    assert c(cache=CACHE + 4, rows=16) == ERR_ALIGN
-    assert c(cache=CACHE + 8, rows=16) == ERR_ALIGN
+    assert c(cache=cache_desc(lib, rows=16, data=CACHE + 4)) == ERR_ALIGN
+    assert c(cache=cache_desc(lib, rows=16, data=CACHE + 8)) == ERR_ALIGN
     assert c(T=0, in_place=0, qo=QO, ko=KO) == OK
     T = 16
     qbytes = T * 4 * 64 * 2
@@ -144,13 +173,21 @@ def test_argument_checks(lib, fn):
 
 
 def test_other_entry_points_argument_checks(lib):
-    assert lib.rope_cos_sin_cache_build(CACHE, 0, 128, 1e6, None) == OK
-    assert lib.rope_cos_sin_cache_build(CACHE, -1, 128, 1e6, None) == ERR_SHAPE
-    assert lib.rope_cos_sin_cache_build(CACHE, 8, 100, 1e6, None) == ERR_HEAD_DIM
-    assert lib.rope_cos_sin_cache_build(CACHE, 8, 128, 0.0, None) == ERR_THETA
-    assert lib.rope_cos_sin_cache_build(CACHE, (1 << 24) + 1, 128, 1e6, None) == ERR_UNSUPPORTED
-    assert lib.rope_cos_sin_cache_build(None, 8, 128, 1e6, None) == ERR_NULL
-    assert lib.rope_cos_sin_cache_build(CACHE + 8, 8, 128, 1e6, None) == ERR_ALIGN
+    from packed_varlen_rope_gb300 import RopeCosSinCacheDesc
+
+    c = RopeCosSinCacheDesc()
+    b = lambda data=CACHE, rows=8, d=128, theta=1e6, scale=1.0, out=ctypes.byref(c): \
+        lib.rope_cos_sin_cache_build(out, data, rows, d, theta, scale, None)  # noqa: E731
+    assert b(rows=0) == OK
+    assert b(rows=-1) == ERR_SHAPE
+    assert b(d=100) == ERR_HEAD_DIM
+    assert b(theta=0.0) == ERR_THETA
+    assert b(scale=-2.0) == ERR_THETA and b(scale=float("inf")) == ERR_THETA
+    assert b(rows=(1 << 24) + 1) == ERR_UNSUPPORTED
+    assert b(data=None) == ERR_NULL
+    assert b(data=CACHE + 8) == ERR_ALIGN
+    assert b(out=None) == ERR_NULL
+    assert b(rows=0, scale=4.0) == OK
     assert lib.rope_qk_positions(CU, 3, 0, Q, None) == OK
     assert lib.rope_qk_positions(CU, -1, 8, Q, None) == ERR_SHAPE
     assert lib.rope_qk_positions(None, 3, 8, Q, None) == ERR_NULL
@@ -163,8 +200,40 @@ def test_other_entry_points_argument_checks(lib):
     assert lib.rope_qk_inv_freq(1e4, 100, 1.0, w) == ERR_HEAD_DIM
     assert lib.rope_qk_inv_freq(1e4, 128, 1.0, None) == ERR_NULL
     assert lib.rope_qk_inv_freq(1e4, 128, 0.0, w) == ERR_THETA
-    assert lib.rope_cos_sin_cache_build_scaled(CACHE, 8, 128, 1e6, -2.0, None) == ERR_THETA
-    assert lib.rope_cos_sin_cache_build_scaled(CACHE, 0, 128, 1e6, 4.0, None) == OK
+
+
+def test_cache_descriptor_must_match_the_call(lib):
+    """A cache serves only the (theta, head_dim, position_scale) it was built for, and
+    only as the build wrote it: every mismatch is ROPE_ERR_CACHE, found on the host."""
+    from packed_varlen_rope_gb300 import RopeCosSinCacheDesc
+
+    c = RopeCosSinCacheDesc()
+    assert lib.rope_cos_sin_cache_build(ctypes.byref(c), None, 0, 64, 1e4, 1.0, None) == OK
+    assert (c.rows, c.head_dim, c.theta, c.position_scale, c.device) == (0, 64, 1e4, 1.0, -1)
+    assert c.check == _fnv_check(c)          # the test's copy of the check word agrees
+    f = lambda cache, **kw: call(lib, T=16, cache=cache, **kw)  # noqa: E731
+    assert f(cache_desc(lib, rows=0)) != ERR_CACHE      # matching (and empty): accepted by the checks
+    assert f(cache_desc(lib, theta=1e6)) == ERR_CACHE
+    assert f(cache_desc(lib, d=128)) == ERR_CACHE
+    assert f(cache_desc(lib, scale=4.0)) == ERR_CACHE               # the plain entry points use scale 1
+    forged = cache_desc(lib)
+    forged.rows = 1 << 20                                           # changed after the build
+    assert f(forged) == ERR_CACHE
+    forged = cache_desc(lib)
+    forged.theta = 1e6                                              # ... to match another call
+    assert call(lib, T=16, theta=1e6, cache=forged) == ERR_CACHE
+    assert f(RopeCosSinCacheDesc()) == ERR_CACHE                    # never built (all zero)
+    # the descriptor form checks position_scale against the cache as well
+    a = lambda **kw: lib.rope_qk_apply(ctypes.byref(_desc(**kw)), None)  # noqa: E731
+    scaled = cache_desc(lib, scale=4.0)
+    assert a(position_scale=4.0, cos_sin_cache=ctypes.pointer(scaled)) != ERR_CACHE
+    assert a(position_scale=2.0, cos_sin_cache=ctypes.pointer(scaled)) == ERR_CACHE
+    assert a(position_scale=4.0, theta=1e5, cos_sin_cache=ctypes.pointer(scaled)) == ERR_CACHE
+    # host-buffer entries reject it before any copy
+    for entry in ("rope_qk_host", "rope_qk_host_static"):
+        d = _desc(cos_sin_cache=ctypes.pointer(cache_desc(lib, theta=7.0)))
+        args = (ctypes.byref(d),) + ((Q, 1 << 20) if entry == "rope_qk_host" else ()) + (None,)
+        assert getattr(lib, entry)(*args) == ERR_CACHE
 
 
 def _desc(T=16, hq=4, hkv=2, d=64, **kw):
@@ -259,3 +328,167 @@ def test_rotary_cache_growth_rule():
     assert cache_rows_for(1025, 1024) == 2048 and cache_rows_for(16384, 0) == 16384
     assert cache_rows_for(20000, 16384) == 32768 and cache_rows_for(500, 32768) == 32768
     assert cache_rows_for((1 << 20) + 1, 1 << 20) == 1 << 21
+
+
+def test_segment_list_checks(lib):
+    """rope_qk_apply's segment list: starts at row 0, rows strictly increasing and inside
+    the call, tokens non-negative and below 2^24; it needs cu_seqlens and offset 0."""
+    from packed_varlen_rope_gb300 import RopeQKSegment
+
+    def a(segs, **kw):
+        arr = (RopeQKSegment * max(1, len(segs)))(*[RopeQKSegment(r, t) for r, t in segs])
+        p = _desc(**kw)
+        p.segments, p.n_segments = arr, len(segs)
+        return lib.rope_qk_apply(ctypes.byref(p), None)
+
+    assert a([(1, 0)]) == ERR_SHAPE                        # does not start at row 0
+    assert a([(0, 0), (8, 100), (8, 200)]) == ERR_SHAPE    # row_start not increasing
+    assert a([(0, 0), (16, 100)]) == ERR_SHAPE             # a segment starting past the rows
+    assert a([(0, -1)]) == ERR_SHAPE
+    assert a([(0, 0), (8, (1 << 24) - 4)]) == ERR_UNSUPPORTED   # last token of segment 2 past 2^24
+    assert a([(0, 0)], token_offset=4) == ERR_SHAPE
+    assert a([(0, 0)], position_ids=CU) == ERR_UNSUPPORTED
+    p = _desc()
+    p.n_segments = 17
+    assert lib.rope_qk_apply(ctypes.byref(p), None) == ERR_SHAPE
+    p.n_segments = 2                                       # segments pointer left NULL
+    assert lib.rope_qk_apply(ctypes.byref(p), None) == ERR_NULL
+    p.n_segments, p.reserved = 0, 1
+    assert lib.rope_qk_apply(ctypes.byref(p), None) == ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("entry", ["rope_qk_host", "rope_qk_host_static"])
+def test_host_entries_check_the_whole_pack_first(lib, entry):
+    """A host-buffer call whose pack crosses 2^24 global tokens only in a late chunk is
+    rejected before any copy: the status is the argument error (a CUDA call on this
+    machine, which has no GPU, would have failed with ROPE_ERR_LAUNCH), and the host
+    buffers are untouched."""
+    from packed_varlen_rope_gb300 import RopeQKDesc, RopeQKSegment
+
+    T, hq, hkv, d = 4096, 2, 1, 64
+    q = np.arange(T * hq * d, dtype=np.uint16).reshape(T, hq, d)
+    k = np.arange(T * hkv * d, dtype=np.uint16).reshape(T, hkv, d) ^ 0x5555
+    q0, k0 = q.copy(), k.copy()
+    p = RopeQKDesc()
+    p.q, p.q_stride_token, p.q_stride_head = q.ctypes.data, hq * d, d
+    p.k, p.k_stride_token, p.k_stride_head = k.ctypes.data, hkv * d, d
+    p.cu_seqlens, p.n_seqs = CU, 1
+    p.n_q_heads, p.n_kv_heads, p.head_dim = hq, hkv, d
+    p.total_tokens, p.theta, p.position_scale = T, 1e4, 1.0
+    extra = (Q, 64 * 1024) if entry == "rope_qk_host" else ()      # a workspace of many chunks
+    run = lambda: getattr(lib, entry)(ctypes.byref(p), *extra, None)  # noqa: E731
+    p.token_offset = (1 << 24) - T + 1                              # only the last token is past 2^24
+    assert run() == ERR_UNSUPPORTED
+    p.token_offset = 0
+    segs = (RopeQKSegment * 2)(RopeQKSegment(0, 0), RopeQKSegment(T - 8, (1 << 24) - 4))
+    p.segments, p.n_segments = segs, 2                              # the second segment crosses it
+    assert run() == ERR_UNSUPPORTED
+    p.segments, p.n_segments = None, 0
+    p.theta = -1.0
+    assert run() == ERR_THETA
+    p.theta, p.q_stride_head = 1e4, d + 8                           # host buffers must be contiguous
+    assert run() == ERR_SHAPE
+    assert np.array_equal(q, q0) and np.array_equal(k, k0)
+
+
+def test_host_binding_checks_outputs_and_cache():
+    """rope_qk_host rejects output buffers of another shape and a cache of the wrong
+    type, dtype, shape or device with ValueError before any C call."""
+    import torch
+
+    import packed_varlen_rope_gb300 as pr
+    from packed_varlen_rope_gb300 import CosSinCache, RopeCosSinCacheDesc
+
+    T, hq, hkv, d = 32, 4, 2, 64
+    q = torch.zeros(T, hq, d, dtype=torch.bfloat16)
+    k = torch.zeros(T, hkv, d, dtype=torch.bfloat16)
+    cu = torch.tensor([0, T], dtype=torch.int32)
+    for qo, ko in ((torch.zeros(T - 1, hq, d, dtype=torch.bfloat16), torch.zeros(T, hkv, d, dtype=torch.bfloat16)),
+                   (torch.zeros(T, hq, d, dtype=torch.bfloat16), torch.zeros(T, hkv, d // 2, dtype=torch.bfloat16)),
+                   (torch.zeros(T, hq, d, dtype=torch.bfloat16), torch.zeros(T, hkv + 1, d, dtype=torch.bfloat16))):
+        with pytest.raises(ValueError, match="shapes"):
+            pr.rope_qk_host(q, k, 1e4, cu_seqlens=cu, q_out=qo, k_out=ko, device="cuda:0")
+
+    def cache(t, rows=None):
+        desc = RopeCosSinCacheDesc()
+        desc.rows = t.shape[0] if rows is None else rows
+        return CosSinCache(t, desc)
+
+    bad = [
+        (torch.zeros(8, 4, d // 16, 4, dtype=torch.float32), "cos_sin_cache must be a CosSinCache"),
+        (cache(torch.zeros(8, 4, d // 16, 4, dtype=torch.bfloat16)), "float32"),
+        (cache(torch.zeros(8, 4, d // 16, 4, dtype=torch.float16)), "float32"),
+        (cache(torch.zeros(8, 4, d // 32, 4, dtype=torch.float32)), "head_dim 64"),       # built for d = 32
+        (cache(torch.zeros(8, 4, d // 16, 4, dtype=torch.float32), rows=16), "rows"),     # table shorter than claimed
+        (cache(torch.zeros(8, 4, 2 * d // 16, 4, dtype=torch.float32)[:, :, ::2]), "contiguous"),
+        (cache(torch.zeros(8, 4, d // 16, 4, dtype=torch.float32)), "is on cpu"),          # host memory
+    ]
+    for c, why in bad:
+        with pytest.raises(ValueError, match=why if why != "rows" else "table"):
+            pr.rope_qk_host(q, k, 1e4, cu_seqlens=cu, cos_sin_cache=c, device="cuda:0")
+
+
+def test_cp_shard_plan():
+    """Contiguous and load-balanced context-parallel shards cover every token of the
+    padded pack exactly once; rank r of the load-balanced plan holds chunks r and
+    2 cp - 1 - r; the segments map local rows to those tokens."""
+    from packed_varlen_rope_gb300 import cp_shards, shard_rows, shard_segments
+
+    for T in (0, 1, 7, 64, 1000, 65536, 65537):
+        for cp in (1, 2, 3, 4, 8):
+            for lb in (False, True):
+                rows = [shard_rows(cp_shards(T, cp, r, lb)) for r in range(cp)]
+                flat = sorted(t for rr in rows for t in rr)
+                n_chunks = 2 * cp if lb else cp
+                padded = -(-T // n_chunks) * n_chunks
+                assert flat == list(range(padded)), (T, cp, lb)
+                assert len({len(rr) for rr in rows}) == 1          # equal shards (padding included)
+                for r in range(cp):
+                    sh = cp_shards(T, cp, r, lb)
+                    segs = shard_segments(sh)
+                    local = shard_rows(sh)
+                    for i, (row0, tok0) in enumerate(segs):
+                        row1 = segs[i + 1][0] if i + 1 < len(segs) else len(local)
+                        assert local[row0:row1] == list(range(tok0, tok0 + row1 - row0))
+    c = -(-1000 // 8)
+    assert cp_shards(1000, 4, 1) == [(c, c), (6 * c, c)]
+    assert shard_segments(cp_shards(1000, 4, 1)) == [(0, c), (c, 6 * c)]
+    with pytest.raises(ValueError):
+        cp_shards(10, 2, 2)
+
+
+def test_launch_info_names_the_dispatched_instance(lib):
+    """rope_qk_launch_info reports the kernel instance rope_qk_apply picks: the head_dim
+    template (64, 96, 128, 256, else the generic 0) and 64-bit offsets exactly when a
+    view spans 2^31 elements or more -- the 1M-token pack (32 Q heads of 128) needs
+    them, the 65,536-token Qwen3-32B pack does not."""
+    from packed_varlen_rope_gb300 import RopeQKDesc, RopeQKLaunch
+
+    def info(T, hq, hkv, d, **kw):
+        p = RopeQKDesc()
+        p.q, p.q_stride_token, p.q_stride_head = 1 << 40, hq * d, d
+        p.k, p.k_stride_token, p.k_stride_head = 1 << 44, hkv * d, d
+        p.cu_seqlens, p.n_seqs = CU, 1
+        p.n_q_heads, p.n_kv_heads, p.head_dim = hq, hkv, d
+        p.total_tokens, p.theta, p.position_scale = T, 1e6, 1.0
+        for key, v in kw.items():
+            setattr(p, key, v)
+        out = RopeQKLaunch()
+        assert lib.rope_qk_launch_info(ctypes.byref(p), ctypes.byref(out)) == OK
+        return out
+
+    w4 = info(65536, 64, 8, 128)
+    assert w4.kernel_name() == "rope_qk_tile_kernel<128,false>"
+    assert (w4.tile_tokens, w4.threads, w4.grid) == (1, 128, 65536)
+    w5 = info(1 << 20, 32, 8, 128)
+    assert w5.kernel_name() == "rope_qk_tile_kernel<128,true>" and w5.grid == (1 << 20) // w5.tile_tokens
+    assert info(4096, 4, 2, 80).kernel_name() == "rope_qk_tile_kernel<0,false>"
+    assert info(64, 4, 2, 64).kernel_name() == "rope_qk_tile_kernel<64,false>"
+    # head-major views of 2^19 tokens x 32 heads: the head stride makes the span pass 2^31
+    hm = info(1 << 19, 32, 8, 128, q_stride_token=128, q_stride_head=(1 << 19) * 128)
+    assert hm.long_index == 1
+    empty = info(0, 4, 2, 64)
+    assert empty.grid == 0
+    assert lib.rope_qk_launch_info(None, ctypes.byref(RopeQKLaunch())) == ERR_NULL
+    p = RopeQKDesc()
+    assert lib.rope_qk_launch_info(ctypes.byref(p), None) == ERR_NULL

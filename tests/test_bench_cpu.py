@@ -19,10 +19,19 @@ def test_kernel_hash_ignores_comments_and_spacing():
     assert bench._code_only(code) != bench._code_only(same.replace("+ 1", "+ 2"))
 
 
-def test_committed_profile_matches_kernel():
-    """The traffic figure in profiles/ was taken on the kernel as it is now."""
-    assert bench.profiled_traffic("qwen3-32b-64k") is not None
-    assert bench.profiled_traffic("qwen3-4b-16k") is None          # no capture of that workload
+def test_profile_traffic_only_for_the_current_kernel(tmp_path, monkeypatch):
+    """The bench reports ncu traffic only from a summary taken on the kernel source as
+    it is now (its recorded hash equals the current one); any other summary, or none,
+    gives null."""
+    summary = tmp_path / "rope_qk_tile_kernel_%s.md"
+    monkeypatch.setattr(bench, "PROFILE_SUMMARY", str(summary))
+    (tmp_path / "rope_qk_tile_kernel_now.md").write_text(
+        "kernel_source_sha256: %s\ntraffic_bytes_per_launch: 123\n" % bench.kernel_source_hash())
+    (tmp_path / "rope_qk_tile_kernel_old.md").write_text(
+        "kernel_source_sha256: %s\ntraffic_bytes_per_launch: 456\n" % ("0" * 64))
+    assert bench.profiled_traffic("now") == 123
+    assert bench.profiled_traffic("old") is None
+    assert bench.profiled_traffic("missing") is None
 
 
 def test_whole_job_value_is_weak_scaling():

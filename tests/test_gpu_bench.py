@@ -29,7 +29,7 @@ def _bench(*args, timeout=600):
 
 def test_rope_forms_on_qwen3_4b_16k():
     d = _bench("--path", "rope-forms", "--workload", "2")
-    assert d["workload"] == "qwen3-4b-16k" and len(d["forms"]) == 9
+    assert d["workload"] == "qwen3-4b-16k" and len(d["forms"]) == 11
     for name, f in d["forms"].items():
         assert f["us"] > 0 and f["gbs"] > 0, name
         assert f["check"].startswith("bit-identical") or f["check"].endswith(" 0 differ"), (name, f["check"])
@@ -51,6 +51,8 @@ def test_rope_bench_line_small():
                 "cpu_baseline", "cpu_baseline_all_cores", "e2e", "clocks", "gpu_launches", "parity"):
         assert key in d, key
     assert d["parity"]["bit_mismatch"] == 0 and d["gpu_launches"] == 40
+    assert d["roofline"]["kernel"] == "rope_qk_tile_kernel<128,false>"
+    assert d["roofline"]["grid"]["ctas"] * d["roofline"]["grid"]["tile_tokens"] >= 16384
     assert d["e2e"]["h2d_bytes_per_step"] == d["e2e"]["d2h_bytes_per_step"] > 0
 
 

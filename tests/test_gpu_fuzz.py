@@ -1,8 +1,8 @@
 """Seeded random combinations of the rotation's options against the oracle (needs a
 GB300): pack lengths with empty samples, head counts and head_dim, contiguous / fused
 QKV / head-major views, in place or out of place, forward or backward, linear rescale,
-and positions from cu_seqlens (with a shard offset and optionally seq_used) or from
-int32 / int64 position ids with out-of-range values.  Every case must equal the oracle
+and positions from cu_seqlens (with a shard offset, a segment list, or seq_used) or
+from int32 / int64 position ids with out-of-range values.  Every case must equal the oracle
 bit for bit; rows without a position stay unchanged (copied when out of place)."""
 from __future__ import annotations
 
@@ -15,7 +15,7 @@ from parity_util import from_bits, to_bits
 pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
-N_CASES = 60
+N_CASES = 80
 
 
 @pytest.fixture(scope="module")
@@ -65,7 +65,7 @@ def test_random_options_match_oracle(dev, case):
     bwd = bool(rng.integers(0, 2))
     in_place = bool(rng.integers(0, 2))
     layout = str(rng.choice(["contiguous", "fused", "head_major"]))
-    source = str(rng.choice(["cu", "cu_offset", "cu_seq_used", "ids32", "ids64"]))
+    source = str(rng.choice(["cu", "cu_offset", "cu_seq_used", "cu_segments", "ids32", "ids64"]))
 
     # rows of this call and their expected positions (-1: row left as it is)
     if source in ("cu", "cu_seq_used"):
@@ -73,11 +73,25 @@ def test_random_options_match_oracle(dev, case):
     elif source == "cu_offset":
         offset = int(rng.integers(0, max(1, pack_tokens)))
         T = int(rng.integers(1, max(2, pack_tokens - offset + 4)))
+    elif source == "cu_segments":
+        offset, T = 0, int(rng.integers(1, max(2, pack_tokens + 4)))
     else:
         offset, T = 0, int(rng.integers(1, 400))
     T = max(T, 1)
     kw = {}
-    if source.startswith("cu"):
+    if source == "cu_segments":
+        # rows cut into 1 to 4 segments, each mapped to its own run of tokens (anywhere in
+        # the pack, a few past its end)
+        n_seg = int(rng.integers(1, min(4, T) + 1))
+        starts = np.sort(rng.choice(np.arange(1, T), size=n_seg - 1, replace=False)) if n_seg > 1 else []
+        row_starts = [0] + [int(x) for x in starts]
+        token_starts = [int(rng.integers(0, pack_tokens + 4)) for _ in row_starts]
+        ends = row_starts[1:] + [T]
+        tokens = np.concatenate([np.arange(t0, t0 + (e - r0)) for r0, t0, e in zip(row_starts, token_starts, ends)])
+        full = oracle.positions(cu, max(pack_tokens, int(tokens.max()) + 1))
+        pos = full[tokens].astype(np.int32)
+        kw = {"cu_seqlens": torch.from_numpy(cu).to(dev), "segments": list(zip(row_starts, token_starts))}
+    elif source.startswith("cu"):
         full = oracle.positions(cu, max(pack_tokens, offset + T))
         pos = full[offset:offset + T].astype(np.int32)
         kw = {"cu_seqlens": torch.from_numpy(cu).to(dev), "token_offset": offset}

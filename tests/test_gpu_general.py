@@ -208,6 +208,48 @@ def test_context_parallel_shards(dev, cp):
     _check(to_bits(ref_k), _expect(k0, pos, w.theta), k0, "cp ref k")
 
 
+@pytest.mark.parametrize("idx,cp", [(2, 2), (2, 4), (3, 3)])
+@pytest.mark.parametrize("bwd", [False, True])
+def test_cp_ranks_one_launch_each(dev, idx, cp, bwd):
+    """Load-balanced context parallelism with the package's shard plan: each rank's
+    buffer holds its two chunks (padding included) and is rotated in ONE launch through
+    the segment list; put back in pack order, the ranks' rows equal the oracle over the
+    whole pack bit for bit, and the padding rows are untouched."""
+    from packed_varlen_rope_gb300 import workloads as wl
+
+    w = wl.WORKLOADS[idx]
+    pack = wl.make_pack(w)
+    T = pack.total_tokens
+    cu = torch.from_numpy(pack.cu_seqlens).to(dev)
+    q = wl.normal_bf16((T, w.n_q_heads, w.head_dim), 18, device="cuda")
+    k = wl.normal_bf16((T, w.n_kv_heads, w.head_dim), 19, device="cuda")
+    q0, k0 = to_bits(q), to_bits(k)
+    cache = pr().new_cos_sin_cache(max(pack.lengths), w.head_dim, w.theta, device=dev)
+    got_q, got_k = np.zeros_like(q0), np.zeros_like(k0)
+    seen = np.zeros(T, dtype=np.int32)
+    for r in range(cp):
+        shards = pr().cp_shards(T, cp, r, load_balanced=True)
+        rows = np.array(pr().shard_rows(shards))
+        inside = rows < T
+        lq = np.full((rows.size,) + q0.shape[1:], 0x4040, np.uint16)        # padding rows: 3.0
+        lk = np.full((rows.size,) + k0.shape[1:], 0x4040, np.uint16)
+        lq[inside], lk[inside] = q0[rows[inside]], k0[rows[inside]]
+        dq, dk = from_bits(lq, dev), from_bits(lk, dev)
+        info = pr().rope_qk_launch_info(dq, dk, w.theta, cu_seqlens=cu, segments=pr().shard_segments(shards),
+                                        cos_sin_cache=cache, backward=bwd)
+        assert info.grid == -(-rows.size // info.tile_tokens)              # one launch covers the rank
+        pr().rope_qk_apply(dq, dk, w.theta, cu_seqlens=cu, segments=pr().shard_segments(shards),
+                           cos_sin_cache=cache, backward=bwd)
+        torch.cuda.synchronize()
+        oq, ok = to_bits(dq), to_bits(dk)
+        assert np.all(oq[~inside] == 0x4040) and np.all(ok[~inside] == 0x4040)
+        got_q[rows[inside]], got_k[rows[inside]] = oq[inside], ok[inside]
+        seen[rows[inside]] += 1
+    assert np.all(seen == 1)
+    _check(got_q, oracle.rope_packed(q0, pack.cu_seqlens, w.theta, bwd=bwd), q0, ("cp q", idx, cp))
+    _check(got_k, oracle.rope_packed(k0, pack.cu_seqlens, w.theta, bwd=bwd), k0, ("cp k", idx, cp))
+
+
 def test_position_scale_page_example(dev):
     """TRL YaRN section: with factor 4, position 100,000 reads as 25,000 (and 163,840
     as 40,960) -- bit-identical rows, with and without a cos/sin cache."""
@@ -246,7 +288,7 @@ def test_position_scale_parity(dev, scale):
     _check(to_bits(q), _expect(q0, pos, w.theta, scale=scale), q0, "scaled q")
     _check(to_bits(k), _expect(k0, pos, w.theta, scale=scale), k0, "scaled k")
     # the scaled cache holds the oracle's scaled cos/sin
-    host = pr()._binding.cache_as_cos_sin(cache[:64].cpu().numpy())
+    host = pr()._binding.cache_as_cos_sin(cache.data[:64].cpu().numpy())
     for p in range(64):
         c, s = oracle.cos_sin(p, w.theta, w.head_dim, scale)
         assert np.array_equal(host[p, :, 0], c) and np.array_equal(host[p, :, 1], s)

@@ -112,3 +112,49 @@ def test_host_stream_rejects_small_workspace(dev):
     with pytest.raises(pr().RopeError) as err:
         pr().rope_qk_host(q, k, w.theta, _workspace(dev, 1, w)[:512], cu_seqlens=cu)
     assert err.value.status == -6
+
+
+@pytest.mark.parametrize("static", [False, True])
+def test_host_call_rejected_late_leaves_buffers_untouched(dev, static):
+    """A pack whose global token indices pass 2^24 only in its last chunk: both host
+    entry points reject it before the first copy, so the caller's host buffers keep
+    their contents (no chunk was rotated and copied back)."""
+    w, pack, q, k = _inputs(2)
+    cu = torch.from_numpy(pack.cu_seqlens).to(dev)
+    qh, kh = q.clone().pin_memory(), k.clone().pin_memory()
+    offset = (1 << 24) - pack.total_tokens + 1
+    ws = None if static else _workspace(dev, 504, w)
+    with pytest.raises(pr().RopeError) as err:
+        pr().rope_qk_host(qh, kh, w.theta, ws, cu_seqlens=cu, token_offset=offset, device=dev)
+    assert err.value.status == -6
+    cache = pr().new_cos_sin_cache(64, w.head_dim, w.theta * 2, device=dev)     # built for another theta
+    with pytest.raises(pr().RopeError) as err:
+        pr().rope_qk_host(qh, kh, w.theta, ws, cu_seqlens=cu, cos_sin_cache=cache, device=dev)
+    assert err.value.status == -11
+    torch.cuda.synchronize()
+    assert torch.equal(qh.view(torch.int16), q.view(torch.int16))
+    assert torch.equal(kh.view(torch.int16), k.view(torch.int16))
+
+
+@pytest.mark.parametrize("static", [False, True])
+def test_host_stream_cp_segments(dev, static):
+    """A load-balanced context-parallel rank (cp = 2, rank 0: chunks 0 and 3 of 4) held
+    on the host, streamed in chunks that cut across its segments: equal to the same
+    rows of a rotation of the whole pack."""
+    from packed_varlen_rope_gb300 import cp_shards, shard_rows, shard_segments
+
+    w, pack, q, k = _inputs(2)
+    T = pack.total_tokens
+    cu = torch.from_numpy(pack.cu_seqlens).to(dev)
+    ref_q, ref_k = q.to(dev), k.to(dev)
+    pr().rope_qk_bwd(ref_q, ref_k, cu, w.theta)
+    shards = cp_shards(T, 2, 0)
+    rows = torch.tensor(shard_rows(shards))
+    assert int(rows.max()) < T
+    sq, sk = q[rows].clone().pin_memory(), k[rows].clone().pin_memory()
+    ws = None if static else _workspace(dev, 1000, w)
+    pr().rope_qk_host(sq, sk, w.theta, ws, cu_seqlens=cu, segments=shard_segments(shards), backward=True,
+                      device=dev)
+    torch.cuda.current_stream(dev).synchronize()
+    assert torch.equal(sq.view(torch.int16), ref_q.cpu()[rows].view(torch.int16))
+    assert torch.equal(sk.view(torch.int16), ref_k.cpu()[rows].view(torch.int16))

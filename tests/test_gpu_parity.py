@@ -115,7 +115,7 @@ def test_validate_cu_seqlens(dev):
 
 @pytest.mark.parametrize("theta,d,rows", [(1.0e4, 64, 64), (1.0e6, 128, 8192), (5.0e5, 128, 2048)])
 def test_cache_matches_oracle(dev, theta, d, rows):
-    cache = pr()._binding.cache_as_cos_sin(pr().new_cos_sin_cache(rows, d, theta, device=dev).cpu().numpy())
+    cache = pr()._binding.cache_as_cos_sin(pr().new_cos_sin_cache(rows, d, theta, device=dev).data.cpu().numpy())
     mism = 0
     for p in range(rows):
         c, s = oracle.cos_sin(p, theta, d)
@@ -129,7 +129,7 @@ def test_cache_large_positions(dev):
     cache = pr().new_cos_sin_cache(rows, d, theta, device=dev)
     rng = np.random.Generator(np.random.PCG64(32))
     picks = np.unique(np.concatenate([rng.integers(0, rows, 600), [rows - 1, (1 << 19), 1]]))
-    got = pr()._binding.cache_as_cos_sin(cache[torch.from_numpy(picks).to(dev)].cpu().numpy())
+    got = pr()._binding.cache_as_cos_sin(cache.data[torch.from_numpy(picks).to(dev)].cpu().numpy())
     mism = 0
     for r, p in enumerate(picks):
         c, s = oracle.cos_sin(int(p), theta, d)
@@ -146,7 +146,7 @@ def test_cache_every_position_matches_oracle(dev):
     import os
 
     theta, d, rows = 1.0e6, 128, 1 << 20
-    got = pr()._binding.cache_as_cos_sin(pr().new_cos_sin_cache(rows, d, theta, device=dev).cpu().numpy())
+    got = pr()._binding.cache_as_cos_sin(pr().new_cos_sin_cache(rows, d, theta, device=dev).data.cpu().numpy())
     ref_c = np.empty((rows, d // 2), np.float32)
     ref_s = np.empty((rows, d // 2), np.float32)
     fn = oracle.get().lib.oracle_cos_sin_scaled

@@ -22,7 +22,8 @@ Other measurements of the same library:
     --layout padded|padded-seq-used
                                  the padded batch of workload 3, every row rotated or
                                  the pad rows skipped (value = valid tokens per second)
-    --no-cache                   cos/sin evaluated per tile instead of read from a cache
+    --no-cache                   cos/sin evaluated per tile (binary32 double-float, binary64 only
+                                 where its rounding is undecided) instead of read from a cache
     --path rope-forms            the forward through every input form (fused QKV,
                                  head-major, out of place, position ids, CP shards, no
                                  cache, rescale), each checked bit for bit
@@ -71,7 +72,7 @@ def parse_args():
                     help="rope path: the pack as is, or (workloads with padded samples) the padded batch "
                          "with every row rotated, or with the pad rows skipped through seq_used")
     ap.add_argument("--no-cache", action="store_true",
-                    help="rope path: no cos/sin cache, binary64 sincos evaluated per tile")
+                    help="rope path: no cos/sin cache, cos/sin evaluated per tile")
     ap.add_argument("--path", choices=["rope", "glu", "rope-forms"], default="rope",
                     help="rope: the QK-RoPE step (default); glu: SwiGLU/GeGLU forward+backward")
     ap.add_argument("--glu-workload", default="qwen3-4b-mlp-1m")
@@ -107,12 +108,13 @@ def _code_only(text: str) -> str:
 
 def kernel_source_hash() -> str:
     """sha256 of the RoPE kernel's device code: rope_qk.cu up to its host-side section,
-    then fastdiv.cuh, comments and whitespace left out.  Host-only edits (argument
-    checks, error strings) and comment edits keep it."""
+    then fastdiv.cuh and cos_sin.cuh, comments and whitespace left out.  Host-only edits
+    (argument checks, error strings) and comment edits keep it."""
     text = open(KERNEL_SOURCE).read()
     device_part = text.split("// ------------------------------------------------------------------ host side")[0]
     h = hashlib.sha256(_code_only(device_part).encode())
-    h.update(_code_only(open(os.path.join(os.path.dirname(KERNEL_SOURCE), "fastdiv.cuh")).read()).encode())
+    for header in ("fastdiv.cuh", "cos_sin.cuh"):
+        h.update(_code_only(open(os.path.join(os.path.dirname(KERNEL_SOURCE), header)).read()).encode())
     return h.hexdigest()
 
 
@@ -131,19 +133,69 @@ def profiled_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons while the GPU works."""
+    """SM clock and throttle reasons sampled while the GPU works: through NVML (the
+    driver's library, read-only queries) every 2 ms in a thread when it loads, else
+    through `nvidia-smi -lms 50`.  A timed region of a few milliseconds then still holds
+    samples of its own."""
 
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    # NVML clock-event reason bits, in the order of REASONS
+    NVML_BITS = (0x8, 0x40, 0x20, 0x4)
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_s: float = 0.002):
         self.gpu_index = gpu_index
+        self.period_s = period_s
         self.proc = None
         self.path = None
+        self.thread = None
+        self.rows = []
+        self.source = "none"
+        self._stop = False
+
+    def _nvml(self):
+        import ctypes
+
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return None
+        if lib.nvmlInit_v2() != 0:
+            return None
+        handle = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu_index), ctypes.byref(handle)) != 0:
+            return None
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+        mx = ctypes.c_uint()
+        if reasons is None or lib.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) != 0:
+            return None
+        return lib, handle, reasons, float(mx.value)
+
+    def _loop(self, lib, handle, reasons, max_mhz):
+        import ctypes
+
+        clk, bits = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop:
+            ok = lib.nvmlDeviceGetClockInfo(handle, 1, ctypes.byref(clk)) == 0 and \
+                reasons(handle, ctypes.byref(bits)) == 0
+            if ok:
+                flags = ["Active" if bits.value & b else "Not Active" for b in self.NVML_BITS]
+                self.rows.append((time.time(), float(clk.value), max_mhz, flags))
+            time.sleep(self.period_s)
 
     def start(self):
+        import threading
+
+        nv = self._nvml()
+        if nv is not None:
+            self.source = "nvml every %.0f ms" % (self.period_s * 1e3)
+            self.thread = threading.Thread(target=self._loop, args=nv, daemon=True)
+            self.thread.start()
+            time.sleep(0.05)
+            return
         fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
         os.close(fd)
         try:
@@ -151,11 +203,15 @@ class ClockSampler:
                 ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.FIELDS,
                  "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            self.source = "nvidia-smi every 50 ms"
         except OSError:
             self.proc = None
         time.sleep(0.3)
 
     def stop(self):
+        if self.thread is not None:
+            self._stop = True
+            self.thread.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -163,7 +219,7 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self, t0: float, t1: float):
+    def _smi_rows(self):
         rows = []
         if self.path and os.path.exists(self.path):
             for line in open(self.path):
@@ -176,8 +232,13 @@ class ClockSampler:
                 except ValueError:
                     continue
             os.unlink(self.path)
+        return rows
+
+    def summary(self, t0: float, t1: float):
+        rows = list(self.rows) if self.thread is not None else self._smi_rows()
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "none"}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "none",
+                    "source": self.source}
         inside = [r for r in rows if t0 <= r[0] <= t1]
         window = "timed"
         if len(inside) < 3:
@@ -185,7 +246,7 @@ class ClockSampler:
             window = "warmup+timed"
         reasons = sorted({name for r in inside for name, v in zip(self.REASONS, r[3]) if v == "Active"})
         return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
-                "reasons": reasons, "samples": len(inside), "window": window}
+                "reasons": reasons, "samples": len(inside), "window": window, "source": self.source}
 
 
 def max_over_ranks(x: float, world: int, device=None) -> float:
@@ -518,7 +579,8 @@ def run_ours(args, rank, world, local):
             "valid_fraction": valid_fraction(pack),
             "parallelism": "dp%d (independent packs)" % world,
             "l2": "no flush: Q, K, dQ, dK = %.2f GB per step > 129 MB L2" % (bytes_per_pass / 1e9),
-            "cos_sin": ("binary64 sincos per tile, no cache" if cache is None else
+            "cos_sin": ("evaluated per tile, no cache (binary32 double-float; binary64 where the rounding "
+                        "is undecided)" if cache is None else
                         "fp32 cache of %d positions built once before timing" % span),
         },
         "hbm_gbs": 2 * bytes_per_pass / (ms_per_step / 1e3) / 1e9,
@@ -854,10 +916,10 @@ def run_rope_forms(args, rank, world, local):
     record("cp=2 load-balanced, both ranks (segments, 2 launches)", lambda: [rank_launch(r) for r in range(cp)],
            check, launches=2)
     del ranks
-    # binary64 cos/sin on the fly (no cache)
+    # cos/sin evaluated in the kernel (no cache)
     q, k = q0.clone(), k0.clone()
     pr.rope_qk_fwd(q, k, cu, w.theta)
-    record("no cos/sin cache (binary64 sincos per tile), rope_qk_fwd",
+    record("no cos/sin cache (evaluated per tile), rope_qk_fwd",
            lambda: pr.rope_qk_fwd(q, k, cu, w.theta), same(q, k))
     # linear position rescale, factor 4, with its own cache; oracle on sampled tokens
     import oracle

@@ -19,7 +19,9 @@
  * Arithmetic, exactly (identical bits to a plain CPU evaluation of the same steps):
  *   w_j   = (float) pow(theta, -(2.0*j)/d)            binary64 on the host, j < d/2
  *   phi   = (float)pos * w_j                          one binary32 multiply
- *   c, s  = cos(phi), sin(phi) in binary64, each rounded once to binary32
+ *   c, s  = cos(phi), sin(phi) in binary64, each rounded once to binary32 (the kernels
+ *           reach the same bits in binary32 double-float arithmetic where its rounding
+ *           is certain, and evaluate in binary64 only for the rest; rope_cos_sin_eval)
  *   y_i     = bf16( (a*c) - (b*s) ),  y_{i+d/2} = bf16( (b*c) + (a*s) )
  *           every product and sum rounded to binary32, no fused multiply-add,
  *           one round-to-nearest-even to bf16; a = x_i, b = x_{i+d/2}.
@@ -352,6 +354,23 @@ int rope_qk_positions(const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_t
  */
 int rope_validate_cu_seqlens(const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_tokens,
                              int32_t *err_word, void *stream);
+
+/*
+ * cos and sin of n binary32 angles (device arrays phi, cos_out, sin_out), the values the
+ * rotation uses for phi = pos * w_j: the binary64 cosine and sine rounded once to
+ * binary32.  mode ROPE_COS_SIN_AS_ROTATION evaluates them as the rotation kernels and
+ * the cache build do (binary32 double-float arithmetic where its rounding is certain,
+ * binary64 for the rest); ROPE_COS_SIN_BINARY64 in binary64 only;
+ * ROPE_COS_SIN_BINARY32_ONLY in binary32 only, writing NaN where that evaluation leaves
+ * the rounding to binary64.  The first two give identical bits for every angle; the
+ * third shows how often the binary64 path is taken.  ROPE_ERR_KIND for another mode.
+ */
+#define ROPE_COS_SIN_AS_ROTATION 0
+#define ROPE_COS_SIN_BINARY64 1
+#define ROPE_COS_SIN_BINARY32_ONLY 2
+
+int rope_cos_sin_eval(const float *phi, float *cos_out, float *sin_out, int64_t n, int32_t mode,
+                      void *stream);
 
 /* Host-side inverse frequencies w_j = (float)(pow(theta, -(2.0*j)/d) / position_scale)
  * (head_dim/2 floats) exactly as the kernels use them; position_scale is 1.0 for the

@@ -31,6 +31,7 @@ from ._binding import (  # noqa: F401
     load_library,
     new_cos_sin_cache,
     rope_cos_sin_cache_build,
+    rope_cos_sin_eval,
     rope_qk_abi_version,
     rope_qk_apply,
     rope_qk_bwd,

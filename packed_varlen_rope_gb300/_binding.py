@@ -19,6 +19,7 @@ EXPORTS = (
     "rope_cos_sin_cache_bytes", "rope_qk_positions",
     "rope_validate_cu_seqlens", "rope_qk_inv_freq", "rope_strerror", "rope_qk_abi_version",
     "glu_fwd", "glu_bwd", "rope_qk_host", "rope_qk_host_static", "rope_qk_launch_info",
+    "rope_cos_sin_eval",
 )
 
 GLU_KINDS = {"swiglu": 0, "geglu": 1, "geglu_tanh": 2}
@@ -155,6 +156,8 @@ def load_library(path: Optional[str] = None):
     lib.rope_qk_positions.restype = ctypes.c_int
     lib.rope_validate_cu_seqlens.argtypes = [vp, i32, i64, vp, vp]
     lib.rope_validate_cu_seqlens.restype = ctypes.c_int
+    lib.rope_cos_sin_eval.argtypes = [vp, vp, vp, i64, i32, vp]
+    lib.rope_cos_sin_eval.restype = ctypes.c_int
     lib.rope_qk_inv_freq.argtypes = [dbl, i32, dbl, ctypes.POINTER(ctypes.c_float)]
     lib.rope_qk_inv_freq.restype = ctypes.c_int
     lib.rope_strerror.argtypes = [ctypes.c_int]
@@ -341,6 +344,24 @@ def rope_validate_cu_seqlens(cu_seqlens, total_tokens: int, err_word=None, strea
              cu_seqlens.numel() - 1, int(total_tokens), _ptr(err_word), _stream(stream, cu_seqlens.device))
     _check("rope_validate_cu_seqlens", st)
     return err_word
+
+
+COS_SIN_MODES = {"as_rotation": 0, "binary64": 1, "binary32_only": 2}
+
+
+def rope_cos_sin_eval(phi, mode: str = "as_rotation", stream=None):
+    """(cos, sin) float32 CUDA tensors of the float32 CUDA angles ``phi`` as the rotation
+    evaluates them ("as_rotation"), in binary64 only ("binary64"), or in binary32 only
+    with NaN where that evaluation leaves the rounding to binary64 ("binary32_only")."""
+    import torch
+
+    if phi.dtype != torch.float32 or not phi.is_cuda or not phi.is_contiguous():
+        raise ValueError("phi must be a contiguous float32 CUDA tensor")
+    c, s = torch.empty_like(phi), torch.empty_like(phi)
+    st = _on(phi.device, load_library().rope_cos_sin_eval, _ptr(phi), _ptr(c), _ptr(s), phi.numel(),
+             COS_SIN_MODES[mode], _stream(stream, phi.device))
+    _check("rope_cos_sin_eval", st)
+    return c, s
 
 
 def rope_qk_inv_freq(theta: float, head_dim: int, position_scale: float = 1.0):

@@ -10,7 +10,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 SOURCES = [os.path.join(HERE, "csrc", n) for n in ("rope_qk.cu", "rope_host.cu", "glu.cu")]
 HEADERS = [os.path.join(ROOT, "include", "rope_qk.h"), os.path.join(ROOT, "include", "glu.h"),
-           os.path.join(HERE, "csrc", "fastdiv.cuh")]
+           os.path.join(HERE, "csrc", "fastdiv.cuh"), os.path.join(HERE, "csrc", "cos_sin.cuh")]
 LIB_PATH = os.path.join(HERE, "librope_qk.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -34,16 +34,18 @@
 #include <type_traits>
 #include <utility>
 
+#include "cos_sin.cuh"
 #include "fastdiv.cuh"
 #include "rope_qk.h"
 
 namespace {
 
-constexpr int kThreads = 128;           // threads per CTA (10 CTAs per SM at 48 registers)
+constexpr int kThreads = 128;           // threads per CTA (9 CTAs per SM at 56 registers)
 constexpr int kUnroll = 2;              // pair units in flight per thread (4 x 16-byte loads)
 constexpr int kMaxHalf = 128;           // head_dim <= 256
 constexpr int kMaxTileTokens = 32;      // one warp resolves the tile's positions
 constexpr int kMaxSegments = ROPE_MAX_SEGMENTS;
+constexpr int kMaxStagedCu = 256;       // cu_seqlens entries a CTA copies to shared memory
 constexpr int64_t kMaxTokens = int64_t(1) << 24;   // positions < 2^24 are exact in fp32
 
 using pvr::FastDiv;
@@ -63,6 +65,7 @@ struct RopeArgs {
     const int32_t *seq_used;                 // optional tokens used per sample (with cu)
     const float4 *cache;
     int32_t n_seqs;
+    int32_t stage_cu;                        // cu_seqlens staged in shared memory (n_seqs < kMaxStagedCu)
     int32_t n_tokens;
     int32_t n_seg;                           // >= 1 row segments (cu_seqlens positions)
     int32_t seg_row[kMaxSegments];           // first row of segment i (seg_row[0] == 0)
@@ -105,14 +108,47 @@ __device__ __forceinline__ int token_position(const int32_t *__restrict__ cu, in
     return pos;
 }
 
-// (cos phi, sin phi) with phi = RN32(pos * w): the angle is one binary32 multiply; the
-// cosine and sine are taken in binary64 and rounded once to binary32.
-__device__ __forceinline__ float2 cos_sin_at(int pos, float w)
+// token_position over a copy of cu_seqlens in shared memory (same rules).
+__device__ __forceinline__ int token_position_staged(const int32_t *cu, int n, int t,
+                                                     const int32_t *__restrict__ seq_used)
 {
-    const float phi = __fmul_rn(__int2float_rn(pos), w);
+    if (n <= 0) return -1;
+    if (t < cu[0] || t >= cu[n]) return -1;
+    int lo = 0, hi = n;
+    while (hi - lo > 1) {
+        const int mid = lo + ((hi - lo) >> 1);
+        if (cu[mid] <= t) lo = mid;
+        else hi = mid;
+    }
+    const int start = cu[lo];
+    if (start < 0 || start > t) return -1;
+    const int pos = t - start;
+    if (seq_used != nullptr && pos >= __ldg(seq_used + lo)) return -1;
+    return pos;
+}
+
+// (cos phi, sin phi) of a binary32 angle in binary64, each rounded once to binary32.
+__device__ __noinline__ float2 cos_sin_binary64(float phi)
+{
     double s, c;
     sincos(static_cast<double>(phi), &s, &c);
     return make_float2(__double2float_rn(c), __double2float_rn(s));
+}
+
+// (cos phi, sin phi) with phi = RN32(pos * w): the angle is one binary32 multiply; the
+// cosine and sine are the binary64 values rounded once to binary32, obtained in
+// binary32 double-float arithmetic where its rounding is certain (all but a few cases
+// in a million) and in binary64 otherwise.
+__device__ __forceinline__ float2 cos_sin_of(float phi)
+{
+    float c, s;
+    if (pvr::cos_sin_binary32(phi, c, s)) return make_float2(c, s);
+    return cos_sin_binary64(phi);
+}
+
+__device__ __forceinline__ float2 cos_sin_at(int pos, float w)
+{
+    return cos_sin_of(__fmul_rn(__int2float_rn(pos), w));
 }
 
 __device__ __forceinline__ uint4 load_stream(const __nv_bfloat16 *p)
@@ -199,8 +235,37 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+    // 0. the tile's first batch of Q/K units (kUnroll per thread) is loaded before the
+    //    positions are known: the loads do not depend on them, so HBM starts streaming
+    //    while the position search and the cos/sin staging run.  An in-place row found
+    //    to lie outside the pack is then simply not stored.
+    uint4 first_lo[kUnroll], first_hi[kUnroll];
+    __nv_bfloat16 *first_dst[kUnroll];
+    uint32_t first_tok[kUnroll], first_chunk[kUnroll];
+#pragma unroll
+    for (int k = 0; k < kUnroll; ++k) {
+        const uint32_t u = threadIdx.x + k * kThreads;
+        first_dst[k] = nullptr;
+        first_tok[k] = 0;
+        first_chunk[k] = 0;
+        if (u < units) {
+            const __nv_bfloat16 *src;
+            locate(u, first_tok[k], first_chunk[k], src, first_dst[k]);
+            first_lo[k] = load_stream(src);
+            first_hi[k] = load_stream(src + h);
+        }
+    }
+
     // 1. positions of the tile's tokens (one lane per token): from the caller's
-    //    position ids, else by binary search of cu_seqlens in the global token stream
+    //    position ids, else by binary search of cu_seqlens in the global token stream --
+    //    in a copy the CTA makes in shared memory with one coalesced round of loads when
+    //    it is short, so that the search costs one global round trip instead of log2(n)
+    //    dependent ones
+    int32_t *s_cu = reinterpret_cast<int32_t *>(s_cs + a.tile_tokens * row4);
+    if (a.stage_cu) {
+        for (int i = threadIdx.x; i <= a.n_seqs; i += kThreads) s_cu[i] = __ldg(a.cu + i);
+        __syncthreads();
+    }
     if (threadIdx.x < kMaxTileTokens) {
         int pos = -1;
         if (static_cast<int>(threadIdx.x) < tt) {
@@ -215,7 +280,8 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
                 int seg = 0;
                 for (int i = 1; i < a.n_seg; ++i)
                     if (r >= a.seg_row[i]) seg = i;
-                pos = token_position(a.cu, a.n_seqs, r + a.seg_delta[seg], a.seq_used);
+                pos = a.stage_cu ? token_position_staged(s_cu, a.n_seqs, r + a.seg_delta[seg], a.seq_used)
+                                 : token_position(a.cu, a.n_seqs, r + a.seg_delta[seg], a.seq_used);
             }
         }
         s_pos[threadIdx.x] = pos;
@@ -248,10 +314,26 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
     }
     __syncthreads();
 
-    // 3. stream the tile: load a batch of units (kUnroll per thread, 4 loads of 16 B in
-    //    flight), rotate, store.  Rows of tokens outside the pack are not touched in
-    //    place and are copied unchanged out of place.
-    for (uint32_t base = threadIdx.x; base < units; base += kUnroll * kThreads) {
+    // 3. stream the tile: rotate and store the first batch, then load a batch of units
+    //    (kUnroll per thread, 4 loads of 16 B in flight), rotate, store, and so on.  Rows
+    //    of tokens outside the pack are not touched in place and are copied unchanged
+    //    out of place.
+#pragma unroll
+    for (int k = 0; k < kUnroll; ++k) {
+        if (first_dst[k] == nullptr) continue;
+        const int pos = s_pos[first_tok[k]];
+        if (pos < 0 && a.in_place) continue;
+        if (pos >= 0) {
+            const float4 *cs = s_cs + (static_cast<int>(first_tok[k]) * 4) * cph + first_chunk[k];
+            rotate2(first_lo[k].x, first_hi[k].x, cs[0]);
+            rotate2(first_lo[k].y, first_hi[k].y, cs[cph]);
+            rotate2(first_lo[k].z, first_hi[k].z, cs[2 * cph]);
+            rotate2(first_lo[k].w, first_hi[k].w, cs[3 * cph]);
+        }
+        store_stream(first_dst[k], first_lo[k]);
+        store_stream(first_dst[k] + h, first_hi[k]);
+    }
+    for (uint32_t base = threadIdx.x + kUnroll * kThreads; base < units; base += kUnroll * kThreads) {
         uint4 lo[kUnroll], hi[kUnroll];
         __nv_bfloat16 *dst[kUnroll];
         int tok[kUnroll], chunk[kUnroll];
@@ -339,6 +421,28 @@ __global__ void validate_kernel(const int32_t *__restrict__ cu, int n, int64_t n
         if (static_cast<int64_t>(__ldg(cu + n)) > n_tokens) bits |= ROPE_CU_PAST_END;
     }
     if (bits) atomicOr(err, bits);
+}
+
+// cos/sin of given angles: mode 0 as the rotation evaluates them, 1 in binary64 only,
+// 2 in binary32 only (NaN where that defers to binary64).
+__global__ void cos_sin_eval_kernel(const float *__restrict__ phi, float *__restrict__ c_out,
+                                    float *__restrict__ s_out, int64_t n, int mode)
+{
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
+        const float x = phi[i];
+        float2 cs;
+        if (mode == 0) {
+            cs = cos_sin_of(x);
+        } else if (mode == 1) {
+            cs = cos_sin_binary64(x);
+        } else {
+            float c, s;
+            cs = pvr::cos_sin_binary32(x, c, s) ? make_float2(c, s) : make_float2(__int_as_float(0x7fc00000),
+                                                                                  __int_as_float(0x7fc00000));
+        }
+        c_out[i] = cs.x;
+        s_out[i] = cs.y;
+    }
 }
 
 // ------------------------------------------------------------------ host side
@@ -643,6 +747,7 @@ int plan_rotation(const rope_qk_desc *dp, Launch *L, bool check_device)
     a.cache = cache != nullptr && cache->rows > 0 ? reinterpret_cast<const float4 *>(cache->data) : nullptr;
     a.cache_rows = a.cache != nullptr ? static_cast<int32_t>(cache->rows) : 0;
     a.n_seqs = ids ? 0 : p.n_seqs;
+    a.stage_cu = !ids && p.n_seqs < kMaxStagedCu ? 1 : 0;
     a.n_tokens = static_cast<int32_t>(T);
     // row r of segment i is token r + seg_delta[i] of cu_seqlens' stream (all below 2^24)
     if (ids || p.n_segments == 0) {
@@ -668,7 +773,9 @@ int plan_rotation(const rope_qk_desc *dp, Launch *L, bool check_device)
     host_inv_freq(p.theta, p.head_dim, p.position_scale, a.w);
 
     L->grid = static_cast<int>((T + a.tile_tokens - 1) / a.tile_tokens);
-    L->smem = static_cast<size_t>(a.tile_tokens) * (p.head_dim / 2) * sizeof(float2);  // 4*cph float4 per token
+    // 4*cph float4 of (cos, sin) per token, then the staged cu_seqlens
+    L->smem = static_cast<size_t>(a.tile_tokens) * (p.head_dim / 2) * sizeof(float2) +
+              (a.stage_cu ? static_cast<size_t>(a.n_seqs + 1) * sizeof(int32_t) : 0);
     // 64-bit offsets only when some element offset of a view reaches 2^31
     L->long_index = false;
     for (const View *v : {&q, &k, &qo, &ko})
@@ -833,6 +940,18 @@ int rope_validate_cu_seqlens(const int32_t *cu_seqlens, int32_t n_seqs, int64_t 
     const int64_t blocks64 = (static_cast<int64_t>(n_seqs) + 255) / 256;
     const int blocks = static_cast<int>(blocks64 < 1 ? 1 : (blocks64 < 152 * 16 ? blocks64 : 152 * 16));
     validate_kernel<<<blocks, 256, 0, s>>>(cu_seqlens, n_seqs, total_tokens, err_word);
+    return cudaGetLastError() == cudaSuccess ? ROPE_OK : ROPE_ERR_LAUNCH;
+}
+
+int rope_cos_sin_eval(const float *phi, float *cos_out, float *sin_out, int64_t n, int32_t mode, void *stream)
+{
+    if (n < 0) return ROPE_ERR_SHAPE;
+    if (mode < ROPE_COS_SIN_AS_ROTATION || mode > ROPE_COS_SIN_BINARY32_ONLY) return ROPE_ERR_KIND;
+    if (n == 0) return ROPE_OK;
+    if (phi == nullptr || cos_out == nullptr || sin_out == nullptr) return ROPE_ERR_NULL;
+    const int64_t blocks64 = (n + 255) / 256;
+    const int blocks = static_cast<int>(blocks64 < 152 * 32 ? blocks64 : 152 * 32);
+    cos_sin_eval_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(phi, cos_out, sin_out, n, mode);
     return cudaGetLastError() == cudaSuccess ? ROPE_OK : ROPE_ERR_LAUNCH;
 }
 

@@ -492,3 +492,11 @@ def test_launch_info_names_the_dispatched_instance(lib):
     assert lib.rope_qk_launch_info(None, ctypes.byref(RopeQKLaunch())) == ERR_NULL
     p = RopeQKDesc()
     assert lib.rope_qk_launch_info(ctypes.byref(p), None) == ERR_NULL
+
+
+def test_cos_sin_eval_argument_checks(lib):
+    e = lambda phi=Q, c=K, s=QO, n=16, mode=0: lib.rope_cos_sin_eval(phi, c, s, n, mode, None)  # noqa: E731
+    assert e(n=0) == OK and e(n=0, phi=None) == OK
+    assert e(n=-1) == ERR_SHAPE
+    assert e(mode=3) == -9 and e(mode=-1) == -9
+    assert e(phi=None) == ERR_NULL and e(c=None) == ERR_NULL and e(s=None) == ERR_NULL

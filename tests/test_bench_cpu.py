@@ -34,6 +34,12 @@ def test_profile_traffic_only_for_the_current_kernel(tmp_path, monkeypatch):
     assert bench.profiled_traffic("missing") is None
 
 
+def test_committed_profile_is_current():
+    """The workload-4 ncu summary in profiles/ was taken on the kernel as it is now, so
+    the bench line carries its DRAM traffic."""
+    assert bench.profiled_traffic("qwen3-32b-64k") == 2358156288
+
+
 def test_whole_job_value_is_weak_scaling():
     assert bench.whole_job_tokens_per_s(4, 65536, 1.0) == 4 * 65536 / 1e-3
 
@@ -68,3 +74,19 @@ def test_padding_waste_algebra():
     assert int(padded.valid_mask.sum()) == sum(padded.lengths) == packed.total_tokens
     assert bench.valid_fraction(packed) == 1.0
     assert 0.4 < bench.valid_fraction(padded) < 0.6          # U[64, 2048] samples: about half wasted
+
+
+def test_clock_summary_keeps_the_timed_window():
+    """The clock record keeps the samples inside the timed region (median SM clock,
+    throttle reasons seen there); with fewer than 3 there it widens to warm-up + timed."""
+    c = bench.ClockSampler(0)
+    c.thread = object()                                  # rows as the NVML thread records them
+    off = ["Not Active"] * 4
+    c.rows = [(0.5, 1500.0, 2070.0, off), (1.0, 2070.0, 2070.0, off), (1.001, 2070.0, 2070.0, off),
+              (1.002, 2040.0, 2070.0, ["Not Active", "Not Active", "Not Active", "Active"]),
+              (1.003, 2070.0, 2070.0, off), (2.0, 1000.0, 2070.0, ["Active"] + off[1:])]
+    s = c.summary(0.9, 1.01)
+    assert s["window"] == "timed" and s["samples"] == 4 and s["sm_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"] and s["sm_max_mhz"] == 2070.0
+    s = c.summary(1.5, 1.6)                              # no sample inside: warm-up + timed
+    assert s["window"] == "warmup+timed" and s["samples"] == 5

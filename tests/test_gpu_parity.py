@@ -484,7 +484,7 @@ def test_rotary_embedding_module(dev):
     assert np.array_equal(to_bits(yq), oracle.rope_packed(q0, pack.cu_seqlens, w.theta))
     assert np.array_equal(to_bits(yk), oracle.rope_packed(k0, pack.cu_seqlens, w.theta))
     assert np.array_equal(to_bits(qleaf.grad), oracle.rope_packed(g_q, pack.cu_seqlens, w.theta, bwd=True))
-    assert rope.cache(dev, 1).shape[0] == 1024
+    assert rope.cache(dev, 1).rows == 1024
 
     w2, pack2, q2, k2, dq2, dk2 = _workload_inputs(2)
     cu2 = torch.from_numpy(pack2.cu_seqlens).to(dev)
@@ -493,7 +493,7 @@ def test_rotary_embedding_module(dev):
     pr().rope_qk_fwd(ref_q, ref_k, cu2, w2.theta)
     got_q, got_k = rope2(q2.clone(), k2.clone(), cu_seqlens=cu2)
     assert torch.equal(got_q, ref_q) and torch.equal(got_k, ref_k)
-    assert rope2.cache(dev, 1).shape[0] == 16384
+    assert rope2.cache(dev, 1).rows == 16384
     # two context-parallel halves of the same pack
     half = pack2.total_tokens // 2
     qa, ka = q2.clone(), k2.clone()
@@ -510,7 +510,7 @@ def test_rotary_embedding_module(dev):
     ref3 = (q3.clone(), k3.clone())
     pr().rope_qk_fwd(ref3[0], ref3[1], cu3, w2.theta)
     out3 = rope2(q3, k3, cu_seqlens=cu3)
-    assert rope2.cache(dev, 1).shape[0] == 32768
+    assert rope2.cache(dev, 1).rows == 32768
     assert torch.equal(out3[0], ref3[0]) and torch.equal(out3[1], ref3[1])
     # broadcast gradient
     ql = torch.zeros((64, 2, w2.head_dim), dtype=torch.bfloat16, device=dev, requires_grad=True)
@@ -546,7 +546,7 @@ def test_rotary_embedding_int64_position_ids(dev):
     big = torch.from_numpy(pos + 100_000).to(dev)
     qb = q.clone()
     rope(qb, k.clone(), position_ids=big, max_position=100_000 + int(pos.max()))
-    assert rope.cache(dev, 1).shape[0] >= 100_000 + int(pos.max()) + 1
+    assert rope.cache(dev, 1).rows >= 100_000 + int(pos.max()) + 1
     assert np.array_equal(to_bits(qb), oracle.rope_rows(q0, (pos + 100_000).astype(np.int32), w.theta))
 
 

@@ -22,6 +22,9 @@ Other measurements of the same library:
     --layout padded|padded-seq-used
                                  the padded batch of workload 3, every row rotated or
                                  the pad rows skipped (value = valid tokens per second)
+    --cp-size C [--cp-rank R]    context parallelism over one pack: a rank's load-balanced
+                                 chunks rotated through a segment list (torchrun: C ranks,
+                                 strong scaling; one GPU: rank R of a group of C)
     --no-cache                   cos/sin evaluated per tile (binary32 double-float, binary64 only
                                  where its rounding is undecided) instead of read from a cache
     --path rope-forms            the forward through every input form (fused QKV,
@@ -29,6 +32,9 @@ Other measurements of the same library:
                                  cache, rescale), each checked bit for bit
     --path glu                   SwiGLU / GeGLU forward + backward (--glu-workload,
                                  --glu-kind)
+    --path rope-shapes           fwd + bwd on other head shapes (head_dim 64, 80, 96, 128,
+                                 256; GQA and MHA head counts), ~2.4 GB per launch each,
+                                 sampled rows checked against the oracle
 """
 from __future__ import annotations
 
@@ -71,9 +77,14 @@ def parse_args():
     ap.add_argument("--layout", choices=["packed", "padded", "padded-seq-used"], default="packed",
                     help="rope path: the pack as is, or (workloads with padded samples) the padded batch "
                          "with every row rotated, or with the pad rows skipped through seq_used")
+    ap.add_argument("--cp-size", type=int, default=1,
+                    help="rope path: context parallelism over one pack; each rank holds its load-balanced "
+                         "chunks (r and 2*cp-1-r) and rotates them in one launch per pass.  Under torchrun "
+                         "the number of ranks; on one GPU, the group size of the rank --cp-rank emulates")
+    ap.add_argument("--cp-rank", type=int, default=0, help="rope path, one GPU: the context-parallel rank run")
     ap.add_argument("--no-cache", action="store_true",
                     help="rope path: no cos/sin cache, cos/sin evaluated per tile")
-    ap.add_argument("--path", choices=["rope", "glu", "rope-forms"], default="rope",
+    ap.add_argument("--path", choices=["rope", "glu", "rope-forms", "rope-shapes"], default="rope",
                     help="rope: the QK-RoPE step (default); glu: SwiGLU/GeGLU forward+backward")
     ap.add_argument("--glu-workload", default="qwen3-4b-mlp-1m")
     ap.add_argument("--glu-kind", choices=["swiglu", "geglu", "geglu_tanh"], default=None,
@@ -266,6 +277,12 @@ def whole_job_tokens_per_s(world: int, tokens_per_rank: int, ms_per_step: float)
     return world * tokens_per_rank / (ms_per_step / 1e3)
 
 
+def cp_tokens_per_s(world: int, pack_tokens: int, rank_tokens: int, ms_per_step: float) -> float:
+    """Strong scaling of one pack over a context-parallel group: the pack's tokens over
+    the slowest rank's step time; on one GPU (an emulated rank) that rank's own tokens."""
+    return (pack_tokens if world > 1 else rank_tokens) / (ms_per_step / 1e3)
+
+
 def physical_gpu_index(local_rank: int) -> int:
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     ids = [v for v in vis.split(",") if v.strip()]
@@ -346,15 +363,18 @@ def valid_fraction(pack) -> float:
     return pack.valid_tokens / pack.total_tokens
 
 
-def cpu_baseline(args, w, pack, q_sample, k_sample, dq_sample, dk_sample, skip_pad=False):
+def cpu_baseline(args, w, pack, q_sample, k_sample, dq_sample, dk_sample, skip_pad=False, pos=None):
     """The oracle as it stands, single-threaded, on a contiguous token sample (rows of a
-    padded batch left out when ``skip_pad``, as the seq_used form leaves them)."""
+    padded batch left out when ``skip_pad``, as the seq_used form leaves them).  ``pos``:
+    the rows' positions when they are not the pack's tokens in order (a context-parallel
+    rank's rows)."""
     import numpy as np
 
     import oracle
 
     oracle.build()
-    pos = oracle.positions(pack.cu_seqlens, pack.total_tokens)
+    if pos is None:
+        pos = oracle.positions(pack.cu_seqlens, pack.total_tokens)
     if skip_pad and pack.valid_mask is not None:
         pos = np.where(pack.valid_mask, pos, -1).astype(np.int32)
     n_all = q_sample.shape[0]
@@ -377,7 +397,8 @@ def cpu_baseline(args, w, pack, q_sample, k_sample, dq_sample, dk_sample, skip_p
         run(n)
         passes += 1
     el = time.perf_counter() - t
-    valid = n if pack.valid_mask is None else int(np.count_nonzero(pack.valid_mask[:n]))
+    valid = int(np.count_nonzero(pos[:n] >= 0)) if pack.valid_mask is None or skip_pad else \
+        int(np.count_nonzero(pack.valid_mask[:n]))
     return {"value": passes * valid / el, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": "first %d rows (%d tokens) of the %s batch, fwd+bwd of Q and K, %d pass(es) in %.1f s on "
                       "one host core" % (n, valid, w.name, passes, el)}, outputs, \
@@ -463,33 +484,61 @@ def run_ours(args, rank, world, local):
     if args.layout != "packed" and w.padded_samples is None:
         print("--layout %s needs a workload with padded samples (3)" % args.layout, file=sys.stderr)
         return 2
-    pack = wl.make_pack(w, "packed" if args.layout == "packed" else "padded", rank=rank)
+    cp = args.cp_size
+    if cp > 1 and (args.layout != "packed" or (world > 1 and world != cp) or not 0 <= args.cp_rank < cp):
+        print("--cp-size needs the packed layout, as many ranks as the group size under torchrun, and "
+              "0 <= --cp-rank < --cp-size", file=sys.stderr)
+        return 2
+    cp_rank = (rank if world > 1 else args.cp_rank) if cp > 1 else 0
+    seed_rank = 0 if cp > 1 else rank                    # context parallelism: one pack for all ranks
+    pack = wl.make_pack(w, "packed" if args.layout == "packed" else "padded", rank=seed_rank)
     T = pack.total_tokens
     if args.layout != "packed":
         n_b, _, _, pad_to = w.padded_samples
         assert abs(valid_fraction(pack) - sum(pack.lengths) / (n_b * pad_to)) < 1e-12
     span = int(np.max(np.diff(pack.cu_seqlens)))          # longest sample, pad rows included
     shape_q, shape_k = (T, w.n_q_heads, w.head_dim), (T, w.n_kv_heads, w.head_dim)
-    q = wl.normal_bf16(shape_q, wl.seed(args.workload, "q", rank), device=dev)
-    k = wl.normal_bf16(shape_k, wl.seed(args.workload, "k", rank), device=dev)
-    dq = wl.normal_bf16(shape_q, wl.seed(args.workload, "dq", rank), device=dev)
-    dk = wl.normal_bf16(shape_k, wl.seed(args.workload, "dk", rank), device=dev)
+    q = wl.normal_bf16(shape_q, wl.seed(args.workload, "q", seed_rank), device=dev)
+    k = wl.normal_bf16(shape_k, wl.seed(args.workload, "k", seed_rank), device=dev)
+    dq = wl.normal_bf16(shape_q, wl.seed(args.workload, "dq", seed_rank), device=dev)
+    dk = wl.normal_bf16(shape_k, wl.seed(args.workload, "dk", seed_rank), device=dev)
+    segs = shards = local_pos = None
+    rank_tokens = pack.valid_tokens                       # tokens this rank rotates per pass
+    if cp > 1:
+        # this rank's chunks, one after the other in its own buffers (padding rows past the
+        # pack's end stay zero and lie outside every sample)
+        shards = pr.cp_shards(T, cp, cp_rank, load_balanced=True)
+        segs = pr.shard_segments(shards)
+        rows = torch.tensor(pr.shard_rows(shards), device=dev)
+        inside = rows < T
+        rank_tokens = int(inside.sum())
+
+        def rank_rows(t):
+            out = torch.zeros((rows.numel(),) + tuple(t.shape[1:]), dtype=t.dtype, device=dev)
+            out[inside] = t[rows[inside]]
+            return out
+
+        q, k, dq, dk = (rank_rows(t) for t in (q, k, dq, dk))
+        T = rows.numel()
+        shape_q, shape_k = (T, w.n_q_heads, w.head_dim), (T, w.n_kv_heads, w.head_dim)
+        local_rows = rows.cpu().numpy()
     cu = torch.from_numpy(pack.cu_seqlens).to(dev)
     cache = None if args.no_cache else pr.new_cos_sin_cache(span, w.head_dim, w.theta, device=dev)
     stream = torch.cuda.current_stream(dev)
     used = torch.tensor(pack.lengths, dtype=torch.int32, device=dev) if args.layout == "padded-seq-used" else None
 
     def fwd(a, b):
-        if used is None:
+        if used is None and segs is None:
             pr.rope_qk_fwd(a, b, cu, w.theta, cos_sin_cache=cache)
         else:
-            pr.rope_qk_apply(a, b, w.theta, cu_seqlens=cu, seq_used=used, cos_sin_cache=cache)
+            pr.rope_qk_apply(a, b, w.theta, cu_seqlens=cu, seq_used=used, segments=segs, cos_sin_cache=cache)
 
     def bwd(a, b):
-        if used is None:
+        if used is None and segs is None:
             pr.rope_qk_bwd(a, b, cu, w.theta, cos_sin_cache=cache)
         else:
-            pr.rope_qk_apply(a, b, w.theta, cu_seqlens=cu, seq_used=used, cos_sin_cache=cache, backward=True)
+            pr.rope_qk_apply(a, b, w.theta, cu_seqlens=cu, seq_used=used, segments=segs, cos_sin_cache=cache,
+                             backward=True)
 
     do_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
     samples = None
@@ -500,10 +549,11 @@ def run_ours(args, rank, world, local):
         # written pageable host memory next to the e2e leg stalled its enqueueing thread)
         pristine = [t.clone() for t in (q, k, dq, dk)]
 
-    rows_moved = T if args.layout == "padded" else pack.valid_tokens     # rows one launch reads and writes
+    rows_moved = T if args.layout == "padded" else rank_tokens     # rows one launch reads and writes
     bytes_per_pass = 4 * (w.n_q_heads + w.n_kv_heads) * w.head_dim * rows_moved
     # the kernel instance the library dispatches for this call (head_dim template, 64-bit offsets)
-    launch = pr.rope_qk_launch_info(q, k, w.theta, cu_seqlens=cu, cos_sin_cache=cache, seq_used=used)
+    launch = pr.rope_qk_launch_info(q, k, w.theta, cu_seqlens=cu, cos_sin_cache=cache, seq_used=used,
+                                    segments=segs)
 
     def step():
         fwd(q, k)
@@ -539,19 +589,33 @@ def run_ours(args, rank, world, local):
     avg_launch_s = total_ms / (2 * K) / 1e3          # this rank's mean time per launch
     total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / K
-    value = whole_job_tokens_per_s(world, pack.valid_tokens, ms_per_step)
+    if cp > 1:
+        # one pack split over the group: the pack's tokens over the slowest rank's time
+        # (one GPU: the emulated rank's own tokens)
+        value = cp_tokens_per_s(world, pack.valid_tokens, rank_tokens, ms_per_step)
+    else:
+        value = whole_job_tokens_per_s(world, pack.valid_tokens, ms_per_step)
     achieved = bytes_per_pass / avg_launch_s / 1e9
     peak, peak_kind = measured_peak()
     clocks = sampler.summary(t_wall0, t_wall1)
 
     e2e = None
     if not args.no_e2e:
-        e2e = end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev, used)
+        e2e = end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev, used, segs,
+                         pack.valid_tokens if cp > 1 and world > 1 else rank_tokens, scale_world=cp == 1)
 
     cpu = parity = None
     if do_cpu:
         samples = tuple(to_np(t, min(T, 65536)) for t in pristine)
-        cpu, ref_outputs, cpu_all = cpu_baseline(args, w, pack, *samples, skip_pad=used is not None)
+        pos_override = None
+        if cp > 1:
+            import oracle
+
+            oracle.build()
+            pos_override = oracle.positions(pack.cu_seqlens, max(pack.total_tokens, int(local_rows.max()) + 1))
+            pos_override = pos_override[local_rows].astype(np.int32)
+        cpu, ref_outputs, cpu_all = cpu_baseline(args, w, pack, *samples, skip_pad=used is not None,
+                                                 pos=pos_override)
         pq, pk, pdq, pdk = pristine
         fwd(pq, pk)
         bwd(pdq, pdk)
@@ -567,7 +631,8 @@ def run_ours(args, rank, world, local):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
+        "scaling": "strong" if cp > 1 else "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
+        "data": "synthetic",
         "config": {
             "workload": w.name, "total_tokens": T, "valid_tokens": pack.valid_tokens,
             "n_seqs": pack.n_seqs, "max_seq_len": max(pack.lengths), "n_q_heads": w.n_q_heads,
@@ -577,8 +642,12 @@ def run_ours(args, rank, world, local):
                        "padded-seq-used": "padded batch [B*pad_to, H, d] bf16, pad rows skipped (seq_used)"
                        }[args.layout],
             "valid_fraction": valid_fraction(pack),
-            "parallelism": "dp%d (independent packs)" % world,
+            "parallelism": ("cp%d (rank %d of a load-balanced context-parallel group%s)"
+                            % (cp, cp_rank, "" if world > 1 else ", emulated on one GPU")
+                            if cp > 1 else "dp%d (independent packs)" % world),
             "l2": "no flush: Q, K, dQ, dK = %.2f GB per step > 129 MB L2" % (bytes_per_pass / 1e9),
+            "cp_shards": None if cp <= 1 else {"token_start_rows": shards, "segments": segs,
+                                               "rank_tokens": rank_tokens},
             "cos_sin": ("evaluated per tile, no cache (binary32 double-float; binary64 where the rounding "
                         "is undecided)" if cache is None else
                         "fp32 cache of %d positions built once before timing" % span),
@@ -608,7 +677,8 @@ def run_ours(args, rank, world, local):
     return 0
 
 
-def end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev, used=None):
+def end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev, used=None, segs=None,
+               tokens=None, scale_world=True):
     """Same metric through the public host-buffer call (rope_qk_host) with the inputs in
     pinned host memory: every step streams Q, K (forward) and dQ, dK (backward) from the
     host through a device workspace in chunks and back, copies overlapped with the
@@ -618,15 +688,19 @@ def end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev, u
     host = [t.to("cpu").pin_memory() for t in (q, k, dq, dk)]
     work = [t.clone().pin_memory() for t in host]
     per_token = (w.n_q_heads + w.n_kv_heads) * w.head_dim * 2
-    chunk = max(8, (pack.total_tokens // 16) // 8 * 8)
+    rows = q.shape[0]
+    tokens = pack.valid_tokens if tokens is None else tokens
+    per_s = (lambda ms: whole_job_tokens_per_s(world, tokens, ms)) if scale_world else \
+        (lambda ms: tokens / (ms / 1e3))  # noqa: E731
+    chunk = max(8, (rows // 16) // 8 * 8)
     ws = torch.empty(2 * chunk * per_token + 4096, dtype=torch.uint8, device=dev)
     h2d = sum(t.numel() * t.element_size() for t in host)
 
     def step():
         pr.rope_qk_host(host[0], host[1], w.theta, ws, cu_seqlens=cu, cos_sin_cache=cache,
-                        q_out=work[0], k_out=work[1], seq_used=used)
+                        q_out=work[0], k_out=work[1], seq_used=used, segments=segs)
         pr.rope_qk_host(host[2], host[3], w.theta, ws, cu_seqlens=cu, cos_sin_cache=cache, backward=True,
-                        q_out=work[2], k_out=work[3], seq_used=used)
+                        q_out=work[2], k_out=work[3], seq_used=used, segments=segs)
 
     for _ in range(2):
         step()
@@ -663,12 +737,12 @@ def end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev, u
     g1.record(stream)
     torch.cuda.synchronize()
     gms = max_over_ranks(g0.elapsed_time(g1) / E, world, dev)
-    return {"value": whole_job_tokens_per_s(world, pack.valid_tokens, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    return {"value": per_s(ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": h2d, "ms_per_step": ms, "steps": E,
             "step_ms_min": min(steps_ms), "step_ms_median": statistics.median(steps_ms),
             "step_ms_max": max(steps_ms), "step_ms_max_index": steps_ms.index(max(steps_ms)),
             "path": "rope_qk_host: pinned host buffers streamed in %d-token chunks" % chunk,
-            "graph_replay": {"value": whole_job_tokens_per_s(world, pack.valid_tokens, gms), "ms_per_step": gms,
+            "graph_replay": {"value": per_s(gms), "ms_per_step": gms,
                              "steps": E, "path": "the same rope_qk_host calls captured in one CUDA graph"}}
 
 
@@ -951,6 +1025,83 @@ def run_rope_forms(args, rank, world, local):
     return 1 if bad else 0
 
 
+HEAD_SHAPES = ((64, 8, 64), (64, 8, 80), (64, 8, 96), (64, 8, 128), (64, 8, 256), (32, 8, 128), (32, 32, 64),
+               (32, 32, 96))
+
+
+def run_rope_shapes(args, rank, world, local):
+    """Forward + backward back to back on head shapes beyond the workloads' (Hq, Hkv, d):
+    each shape gets enough tokens for about 2.4 GB per launch, packed from samples of
+    1,024 tokens, theta 1e6, a cos/sin cache; the mean time per launch over the timed
+    launches (CUDA events around them only) and 512 seeded rows of the forward checked
+    against the oracle bit for bit."""
+    import numpy as np
+    import torch
+
+    from packed_varlen_rope_gb300 import build as _build
+
+    _build.build()
+    import oracle
+    import packed_varlen_rope_gb300 as pr
+    from packed_varlen_rope_gb300 import workloads as wl
+
+    if rank != 0:
+        return 0
+    oracle.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peak, peak_kind = measured_peak()
+    theta, sample = 1.0e6, 1024
+    bits = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)  # noqa: E731
+    shapes = {}
+    for hq, hkv, d in HEAD_SHAPES:
+        per_token = 4 * (hq + hkv) * d
+        T = (2_415_919_104 // per_token) // sample * sample
+        cu_np = np.arange(0, T + 1, sample, dtype=np.int32)
+        cu = torch.from_numpy(cu_np).to(dev)
+        q = wl.normal_bf16((T, hq, d), 8100 + d, device=dev)
+        k = wl.normal_bf16((T, hkv, d), 8200 + d, device=dev)
+        dq = wl.normal_bf16((T, hq, d), 8300 + d, device=dev)
+        dk = wl.normal_bf16((T, hkv, d), 8400 + d, device=dev)
+        cache = pr.new_cos_sin_cache(sample, d, theta, device=dev)
+        pick = np.unique(np.random.Generator(np.random.PCG64(8500 + d)).integers(0, T, 512))
+        pick_dev = torch.from_numpy(pick).to(dev)
+        q0, k0 = bits(q[pick_dev]), bits(k[pick_dev])
+        pr.rope_qk_fwd(q, k, cu, theta, cos_sin_cache=cache)
+        torch.cuda.synchronize()
+        pos = (pick % sample).astype(np.int32)
+        mism = int(np.count_nonzero(bits(q[pick_dev]) != oracle.rope_rows(q0, pos, theta))) + \
+            int(np.count_nonzero(bits(k[pick_dev]) != oracle.rope_rows(k0, pos, theta)))
+        n_el = q0.size + k0.size
+        for _ in range(max(3, args.warmup)):
+            pr.rope_qk_fwd(q, k, cu, theta, cos_sin_cache=cache)
+            pr.rope_qk_bwd(dq, dk, cu, theta, cos_sin_cache=cache)
+        K = max(10, min(args.steps, 200))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(K):
+            pr.rope_qk_fwd(q, k, cu, theta, cos_sin_cache=cache)
+            pr.rope_qk_bwd(dq, dk, cu, theta, cos_sin_cache=cache)
+        b.record()
+        torch.cuda.synchronize()
+        sec = a.elapsed_time(b) / 1e3 / (2 * K)
+        nbytes = per_token * T
+        info = pr.rope_qk_launch_info(q, k, theta, cu_seqlens=cu, cos_sin_cache=cache)
+        shapes["%d/%d/%d" % (hq, hkv, d)] = {
+            "tokens": T, "us": sec * 1e6, "gbs": nbytes / sec / 1e9, "frac": nbytes / sec / 1e9 / peak,
+            "kernel": info.kernel_name(), "tile_tokens": info.tile_tokens,
+            "check": "oracle on %d sampled tokens: %d elements, %d differ" % (pick.size, n_el, mism)}
+        del q, k, dq, dk, cache
+        torch.cuda.empty_cache()
+    line = {"metric": "QK-RoPE fwd+bwd per head shape (Hq/Hkv/d)", "unit": "GB/s", "peak": peak,
+            "peak_kind": peak_kind + " (hbm_gbs)", "theta": theta, "sample_tokens": sample,
+            "timing": "mean per launch over back-to-back forward and backward launches (CUDA events around them)",
+            "shapes": shapes}
+    print(json.dumps(line), flush=True)
+    return 1 if any(not v["check"].endswith(" 0 differ") for v in shapes.values()) else 0
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_env()
@@ -963,6 +1114,8 @@ def main():
         return run_glu(args, rank, world, local)
     if args.path == "rope-forms":
         return run_rope_forms(args, rank, world, local)
+    if args.path == "rope-shapes":
+        return run_rope_shapes(args, rank, world, local)
     return run_ours(args, rank, world, local)
 
 

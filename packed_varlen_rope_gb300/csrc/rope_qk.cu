@@ -238,7 +238,10 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
     // 0. the tile's first batch of Q/K units (kUnroll per thread) is loaded before the
     //    positions are known: the loads do not depend on them, so HBM starts streaming
     //    while the position search and the cos/sin staging run.  An in-place row found
-    //    to lie outside the pack is then simply not stored.
+    //    to lie outside the pack is then simply not stored.  With seq_used (a padded
+    //    batch whose pad rows are left out), whole tiles may hold no row to rotate, so
+    //    the first batch waits for the positions there and skips those rows' loads.
+    const bool early = a.seq_used == nullptr;
     uint4 first_lo[kUnroll], first_hi[kUnroll];
     __nv_bfloat16 *first_dst[kUnroll];
     uint32_t first_tok[kUnroll], first_chunk[kUnroll];
@@ -248,7 +251,7 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
         first_dst[k] = nullptr;
         first_tok[k] = 0;
         first_chunk[k] = 0;
-        if (u < units) {
+        if (early && u < units) {
             const __nv_bfloat16 *src;
             locate(u, first_tok[k], first_chunk[k], src, first_dst[k]);
             first_lo[k] = load_stream(src);
@@ -266,6 +269,7 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
         for (int i = threadIdx.x; i <= a.n_seqs; i += kThreads) s_cu[i] = __ldg(a.cu + i);
         __syncthreads();
     }
+    int lane_pos = -1;
     if (threadIdx.x < kMaxTileTokens) {
         int pos = -1;
         if (static_cast<int>(threadIdx.x) < tt) {
@@ -285,8 +289,11 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
             }
         }
         s_pos[threadIdx.x] = pos;
+        lane_pos = pos;
     }
-    __syncthreads();
+    // A tile with no token inside the pack (the pad rows of a padded batch under
+    // seq_used, rows past the pack's end) has nothing to rotate: in place, it is done.
+    if (!__syncthreads_or(lane_pos >= 0) && a.in_place) return;
 
     // 2. (cos, sin) rows of the tile, sin negated for the backward.  A row is 4*cph
     //    float4 in the cache's own [quad][chunk] order, so staging is a plain copy.
@@ -318,6 +325,20 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
     //    (kUnroll per thread, 4 loads of 16 B in flight), rotate, store, and so on.  Rows
     //    of tokens outside the pack are not touched in place and are copied unchanged
     //    out of place.
+    if (!early) {
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+            const uint32_t u = threadIdx.x + k * kThreads;
+            if (u >= units) continue;
+            const __nv_bfloat16 *src;
+            __nv_bfloat16 *out;
+            locate(u, first_tok[k], first_chunk[k], src, out);
+            if (s_pos[first_tok[k]] < 0 && a.in_place) continue;
+            first_dst[k] = out;
+            first_lo[k] = load_stream(src);
+            first_hi[k] = load_stream(src + h);
+        }
+    }
 #pragma unroll
     for (int k = 0; k < kUnroll; ++k) {
         if (first_dst[k] == nullptr) continue;
@@ -482,8 +503,11 @@ int check_scale(double scale)
     return ROPE_OK;
 }
 
-// Tokens per tile: enough 16-byte pair units that every thread has about kUnroll * 2
-// of them, capped by the one-warp position search.
+// Tokens per tile: enough 16-byte pair units that every thread has about 2 * kUnroll of
+// them, capped by the one-warp position search.  Half that (one batch per thread, so
+// 1-token tiles on 40 heads of 128) measured 1.5 % faster with a cos/sin cache on 16,384
+// tokens but 12 % slower without one and 16 % slower on a padded batch under seq_used,
+// where each tile's position search and cos/sin staging serve half as many tokens.
 int pick_tile_tokens(int h_tot, int head_dim)
 {
     const int units_per_token = h_tot * (head_dim / 16);

@@ -37,11 +37,18 @@ def test_profile_traffic_only_for_the_current_kernel(tmp_path, monkeypatch):
 def test_committed_profile_is_current():
     """The workload-4 ncu summary in profiles/ was taken on the kernel as it is now, so
     the bench line carries its DRAM traffic."""
-    assert bench.profiled_traffic("qwen3-32b-64k") == 2358156288
+    assert bench.profiled_traffic("qwen3-32b-64k") == 2358566500
 
 
 def test_whole_job_value_is_weak_scaling():
     assert bench.whole_job_tokens_per_s(4, 65536, 1.0) == 4 * 65536 / 1e-3
+
+
+def test_cp_value_is_strong_scaling():
+    """Context parallelism splits one pack: the whole pack's tokens over the slowest
+    rank's time; an emulated rank on one GPU counts its own tokens."""
+    assert bench.cp_tokens_per_s(2, 65536, 32768, 0.5) == 65536 / 0.5e-3
+    assert bench.cp_tokens_per_s(1, 65536, 32768, 0.5) == 32768 / 0.5e-3
 
 
 def test_all_core_oracle_timing_runs_every_range():

@@ -65,3 +65,31 @@ def test_rope_bench_padded_layouts(layout):
     assert d["parity"]["bit_mismatch"] == 0 and 0.4 < d["config"]["valid_fraction"] < 0.6
     rows = 16384 if layout == "padded" else d["config"]["valid_tokens"]
     assert d["roofline"]["algorithmic_bytes_per_launch"] == 4 * 40 * 128 * rows
+
+
+def test_rope_bench_cp_rank():
+    """A load-balanced context-parallel rank (cp = 2, rank 1) through the bench: its two
+    chunks of the Qwen3-4B-shape pack rotated through the segment list, fwd + bwd back to
+    back; the oracle parity block covers the rank's rows, and the value counts its tokens."""
+    d = _bench("--workload", "2", "--cp-size", "2", "--cp-rank", "1", "--steps", "20", "--warmup", "3",
+               "--e2e-steps", "2", "--cpu-seconds", "1")
+    assert d["scaling"] == "strong" and d["config"]["parallelism"].startswith("cp2 (rank 1")
+    assert d["config"]["cp_shards"]["rank_tokens"] == 8192
+    assert d["config"]["cp_shards"]["segments"] == [[0, 4096], [4096, 8192]]
+    assert d["parity"]["bit_mismatch"] == 0 and d["parity"]["elements"] > 0
+    assert d["roofline"]["algorithmic_bytes_per_launch"] == 4 * 40 * 128 * 8192
+    assert abs(d["value"] - 8192 / (d["ms_per_step"] / 1e3)) < 1e-6 * d["value"]
+
+
+def test_rope_head_shapes():
+    """Other head shapes (head_dim 64, 80 -- the generic instance --, 96, 128, 256; GQA and
+    MHA head counts) through the bench: every sampled row equals the oracle and every
+    launch names the instance the library dispatched."""
+    d = _bench("--path", "rope-shapes", "--steps", "20", "--warmup", "3", timeout=900)
+    assert len(d["shapes"]) == 8
+    for name, s in d["shapes"].items():
+        assert s["check"].endswith(" 0 differ"), (name, s["check"])
+        assert 0 < s["frac"] < 2, name
+        dim = int(name.split("/")[2])
+        want = dim if dim in (64, 96, 128, 256) else 0
+        assert s["kernel"] == "rope_qk_tile_kernel<%d,false>" % want, (name, s["kernel"])

@@ -523,6 +523,34 @@ def test_rotary_embedding_module(dev):
     assert torch.equal(ql.grad, expect[0]) and torch.equal(kl.grad, expect[1])
 
 
+def test_rotary_embedding_cp_segments_autograd(dev):
+    """RotaryEmbedding on a load-balanced context-parallel rank's buffer (cp = 2, rank 1:
+    chunks 1 and 2 of 4) through its segment list: the forward equals the whole-pack
+    rotation's rows and the autograd backward the oracle's transpose rotation, the cache
+    grown to cover the rank's last global token."""
+    from packed_varlen_rope_gb300 import RotaryEmbedding, cp_shards, shard_rows, shard_segments
+
+    w, pack, q, k, dq, dk = _workload_inputs(2)
+    T = pack.total_tokens
+    cu_dev = torch.from_numpy(pack.cu_seqlens).to(dev)
+    shards = cp_shards(T, 2, 1)
+    rows = torch.tensor(shard_rows(shards), device=dev)
+    assert int(rows.max()) < T
+    rope = RotaryEmbedding(w.head_dim, w.theta)
+    ql, kl = q[rows].clone(), k[rows].clone()
+    g_q, g_k = dq[rows].clone(), dk[rows].clone()
+    qleaf = torch.zeros_like(ql, requires_grad=True)
+    kleaf = torch.zeros_like(kl, requires_grad=True)
+    yq, yk = rope(qleaf + ql, kleaf + kl, cu_seqlens=cu_dev, segments=shard_segments(shards))
+    torch.autograd.backward([yq, yk], [g_q, g_k])
+    pos = oracle.positions(pack.cu_seqlens, T)[rows.cpu().numpy()]
+    assert np.array_equal(to_bits(yq), oracle.rope_rows(to_bits(ql), pos, w.theta))
+    assert np.array_equal(to_bits(yk), oracle.rope_rows(to_bits(kl), pos, w.theta))
+    assert np.array_equal(to_bits(qleaf.grad), oracle.rope_rows(to_bits(g_q), pos, w.theta, bwd=True))
+    assert np.array_equal(to_bits(kleaf.grad), oracle.rope_rows(to_bits(g_k), pos, w.theta, bwd=True))
+    assert rope.cache(dev, 1).rows >= int(rows.max()) + 1
+
+
 def test_rotary_embedding_int64_position_ids(dev):
     """RotaryEmbedding with int64 position ids (a Hugging Face collator's dtype), forward
     and autograd backward, against the oracle on the same positions."""

@@ -740,7 +740,9 @@ def end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev, u
     return {"value": per_s(ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": h2d, "ms_per_step": ms, "steps": E,
             "step_ms_min": min(steps_ms), "step_ms_median": statistics.median(steps_ms),
+            "step_ms_p90": sorted(steps_ms)[int(0.9 * (len(steps_ms) - 1))],
             "step_ms_max": max(steps_ms), "step_ms_max_index": steps_ms.index(max(steps_ms)),
+            "steps_over_twice_median": sum(1 for t in steps_ms if t > 2 * statistics.median(steps_ms)),
             "path": "rope_qk_host: pinned host buffers streamed in %d-token chunks" % chunk,
             "graph_replay": {"value": per_s(gms), "ms_per_step": gms,
                              "steps": E, "path": "the same rope_qk_host calls captured in one CUDA graph"}}

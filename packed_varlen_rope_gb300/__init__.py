@@ -43,7 +43,7 @@ from ._binding import (  # noqa: F401
     rope_strerror,
     rope_validate_cu_seqlens,
 )
-from .shards import cp_shards, shard_rows, shard_segments  # noqa: F401
+from .shards import cp_shards, shard_rows, shard_segments, ulysses_heads  # noqa: F401
 
 
 def _autograd_function():

@@ -296,28 +296,48 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
     if (!__syncthreads_or(lane_pos >= 0) && a.in_place) return;
 
     // 2. (cos, sin) rows of the tile, sin negated for the backward.  A row is 4*cph
-    //    float4 in the cache's own [quad][chunk] order, so staging is a plain copy.
-    for (int idx = threadIdx.x; idx < tt * row4; idx += kThreads) {
-        const int i = idx / row4;
-        const int r = idx - i * row4;
-        const int pos = s_pos[i];
-        float4 cs = make_float4(1.0f, 0.0f, 1.0f, 0.0f);
-        if (pos >= 0) {
-            if (a.cache != nullptr && pos < a.cache_rows) {
-                cs = __ldg(a.cache + static_cast<int64_t>(pos) * row4 + r);
-            } else {
-                const int quad = r / cph;
-                const int j = 8 * (r - quad * cph) + 2 * quad;
-                const float2 c0 = cos_sin_at(pos, a.w[j]);
-                const float2 c1 = cos_sin_at(pos, a.w[j + 1]);
-                cs = make_float4(c0.x, c0.y, c1.x, c1.y);
+    //    float4 in the cache's own [quad][chunk] order, so staging is a plain copy; when
+    //    evaluated, each thread takes one (cos, sin) pair (half of a float4 entry), so
+    //    twice as many threads share the evaluation.
+    if (a.cache != nullptr) {
+        for (int idx = threadIdx.x; idx < tt * row4; idx += kThreads) {
+            const int i = idx / row4;
+            const int r = idx - i * row4;
+            const int pos = s_pos[i];
+            float4 cs = make_float4(1.0f, 0.0f, 1.0f, 0.0f);
+            if (pos >= 0) {
+                if (pos < a.cache_rows) {
+                    cs = __ldg(a.cache + static_cast<int64_t>(pos) * row4 + r);
+                } else {
+                    const int quad = r / cph;
+                    const int j = 8 * (r - quad * cph) + 2 * quad;
+                    const float2 c0 = cos_sin_at(pos, a.w[j]);
+                    const float2 c1 = cos_sin_at(pos, a.w[j + 1]);
+                    cs = make_float4(c0.x, c0.y, c1.x, c1.y);
+                }
+                if (a.bwd) {
+                    cs.y = -cs.y;
+                    cs.w = -cs.w;
+                }
             }
-            if (a.bwd) {
-                cs.y = -cs.y;
-                cs.w = -cs.w;
-            }
+            s_cs[idx] = cs;
         }
-        s_cs[idx] = cs;
+    } else {
+        float2 *s_cs2 = reinterpret_cast<float2 *>(s_cs);
+        for (int p2 = threadIdx.x; p2 < 2 * tt * row4; p2 += kThreads) {
+            const int idx = p2 >> 1;
+            const int i = idx / row4;
+            const int r = idx - i * row4;
+            const int pos = s_pos[i];
+            float2 cs = make_float2(1.0f, 0.0f);
+            if (pos >= 0) {
+                const int quad = r / cph;
+                const int j = 8 * (r - quad * cph) + 2 * quad + (p2 & 1);
+                cs = cos_sin_at(pos, a.w[j]);
+                if (a.bwd) cs.y = -cs.y;
+            }
+            s_cs2[p2] = cs;
+        }
     }
     __syncthreads();
 

@@ -50,3 +50,27 @@ def shard_rows(shards) -> List[int]:
     for token_start, n in shards:
         out.extend(range(int(token_start), int(token_start) + int(n)))
     return out
+
+
+def ulysses_heads(n_q_heads: int, n_kv_heads: int, sp_size: int, rank: int):
+    """Head shard of a rank under Ulysses sequence parallelism (the DeepSpeed
+    alternative the TRL page names next to context parallelism): after the all-to-all
+    each rank holds every token of its attention heads.  Returns ((q_lo, q_hi),
+    (kv_lo, kv_hi)), half-open head ranges of Q and K.  Q heads are split evenly; K/V
+    heads too when there are enough, else each rank keeps the one K/V head its Q heads
+    share (grouped-query attention).  The rotation needs no exchange: the rank rotates
+    q[:, q_lo:q_hi] and k[:, kv_lo:kv_hi] (strided views) with the pack's cu_seqlens."""
+    hq, hkv, sp, r = int(n_q_heads), int(n_kv_heads), int(sp_size), int(rank)
+    if hq < 1 or hkv < 1 or sp < 1 or not 0 <= r < sp or hq % sp or hq % hkv:
+        raise ValueError("need sp_size | n_q_heads, n_kv_heads | n_q_heads and 0 <= rank < sp_size")
+    q_per = hq // sp
+    if hkv % sp == 0:
+        kv_per = hkv // sp
+        return (r * q_per, (r + 1) * q_per), (r * kv_per, (r + 1) * kv_per)
+    if sp % hkv:
+        raise ValueError("n_kv_heads must divide sp_size or be a multiple of it")
+    group = hq // hkv                         # Q heads per K/V head
+    kv = (r * q_per) // group
+    if ((r + 1) * q_per - 1) // group != kv:
+        raise ValueError("a rank's Q heads would span several K/V heads")
+    return (r * q_per, (r + 1) * q_per), (kv, kv + 1)

@@ -500,3 +500,23 @@ def test_cos_sin_eval_argument_checks(lib):
     assert e(n=-1) == ERR_SHAPE
     assert e(mode=3) == -9 and e(mode=-1) == -9
     assert e(phi=None) == ERR_NULL and e(c=None) == ERR_NULL and e(s=None) == ERR_NULL
+
+
+def test_ulysses_head_plan():
+    """Ulysses head shards: every Q head on exactly one rank; K/V heads split when there
+    are enough, else each rank keeps the one its Q heads share."""
+    from packed_varlen_rope_gb300 import ulysses_heads
+
+    for hq, hkv, sp in ((64, 8, 8), (64, 8, 4), (32, 8, 16), (32, 32, 8), (64, 8, 16), (4, 2, 4)):
+        seen = []
+        for r in range(sp):
+            (q0, q1), (k0, k1) = ulysses_heads(hq, hkv, sp, r)
+            seen += list(range(q0, q1))
+            group = hq // hkv
+            assert all(k0 <= h // group < k1 for h in range(q0, q1)), (hq, hkv, sp, r)   # Q heads' K/V head held
+        assert sorted(seen) == list(range(hq))
+    assert ulysses_heads(64, 8, 16, 3) == ((12, 16), (1, 2))
+    assert ulysses_heads(64, 8, 4, 1) == ((16, 32), (2, 4))
+    for bad in ((64, 8, 3, 0), (64, 8, 8, 8), (12, 8, 4, 0), (64, 6, 4, 0)):
+        with pytest.raises(ValueError):
+            ulysses_heads(*bad)

@@ -250,6 +250,33 @@ def test_cp_ranks_one_launch_each(dev, idx, cp, bwd):
     _check(got_k, oracle.rope_packed(k0, pack.cu_seqlens, w.theta, bwd=bwd), k0, ("cp k", idx, cp))
 
 
+@pytest.mark.parametrize("sp", [4, 16])
+def test_ulysses_head_shards(dev, sp):
+    """Ulysses sequence parallelism on the Qwen3-32B head shape (64 Q / 8 K heads): each
+    rank holds every token of its heads (sp = 4: 16 Q and 2 K heads; sp = 16: 4 Q heads
+    and the one K head they share) and rotates them alone; each rank's result equals the
+    same heads of the whole rotation, which equals the oracle."""
+    from packed_varlen_rope_gb300 import ulysses_heads
+    from packed_varlen_rope_gb300 import workloads as wl
+
+    w = wl.WORKLOADS[2]
+    pack = wl.make_pack(w)
+    T, hq, hkv, d = pack.total_tokens, 64, 8, w.head_dim
+    cu = torch.from_numpy(pack.cu_seqlens).to(dev)
+    q = wl.normal_bf16((T, hq, d), 71, device=dev)
+    k = wl.normal_bf16((T, hkv, d), 72, device=dev)
+    ref_q, ref_k = q.clone(), k.clone()
+    pr().rope_qk_fwd(ref_q, ref_k, cu, w.theta)
+    for r in range(sp):
+        (q0, q1), (k0, k1) = ulysses_heads(hq, hkv, sp, r)
+        ql, kl = q[:, q0:q1].contiguous(), k[:, k0:k1].contiguous()      # the rank's own buffers
+        pr().rope_qk_fwd(ql, kl, cu, w.theta)
+        assert torch.equal(ql, ref_q[:, q0:q1]) and torch.equal(kl, ref_k[:, k0:k1]), r
+    pos = oracle.positions(pack.cu_seqlens, T)
+    kb = to_bits(k)
+    _check(to_bits(ref_k), _expect(kb, pos, w.theta), kb, "ulysses ref k")
+
+
 def test_position_scale_page_example(dev):
     """TRL YaRN section: with factor 4, position 100,000 reads as 25,000 (and 163,840
     as 40,960) -- bit-identical rows, with and without a cos/sin cache."""

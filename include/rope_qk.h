@@ -32,14 +32,16 @@
  * with no sample (t < cu_seqlens[0] or t >= cu_seqlens[n_seqs]) is outside the pack:
  * in place it is left untouched; out of place its rows are copied unchanged.
  *
- * Ownership.  Every pointer is owned by the caller.  Q, K, outputs, cu_seqlens, the
- * cos/sin cache and pos/err buffers are DEVICE pointers; the library keeps no pointer
- * after a call returns, allocates no device memory, and never synchronises.  Calls are
- * asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ * Ownership.  Every pointer is owned by the caller.  Q, K, outputs, cu_seqlens,
+ * position ids, seq_used, the cos/sin table and pos/err buffers are DEVICE pointers;
+ * descriptors (rope_qk_desc, rope_cos_sin_cache, segment lists) are HOST memory read
+ * during the call.  The library keeps no pointer after a call returns, allocates no
+ * device memory, and never synchronises.  Calls are asynchronous on `stream` (a
+ * cudaStream_t; NULL = the legacy default stream).
  *
  * Errors.  Every entry point returns ROPE_OK (0) or a negative rope_status.  Arguments
- * are checked on the host before anything is launched; a rejected call launches
- * nothing.  The values inside cu_seqlens are not read on the host (that would need a
+ * are checked on the host before anything is launched or copied; a rejected call
+ * launches and copies nothing.  The values inside cu_seqlens are not read on the host (that would need a
  * synchronisation): rope_validate_cu_seqlens checks them on the device.  With invalid
  * values the kernels still stay inside the Q/K/cache bounds and skip the tokens whose
  * position cannot be derived.  No kernel traps, asserts or spins.
@@ -58,13 +60,17 @@ extern "C" {
 typedef enum rope_status {
     ROPE_OK = 0,
     ROPE_ERR_NULL = -1,         /* a required pointer is NULL */
-    ROPE_ERR_SHAPE = -2,        /* negative count, stride or offset; a head count < 1 */
+    ROPE_ERR_SHAPE = -2,        /* negative count, stride or offset; a head count < 1; a
+                                   segment list not starting at row 0, not increasing or
+                                   with a token offset beside it */
     ROPE_ERR_HEAD_DIM = -3,     /* head_dim not a multiple of 16 in [16, 256] */
     ROPE_ERR_ALIGN = -4,        /* a pointer not 16-byte aligned, a stride not a multiple of 8 */
     ROPE_ERR_OVERLAP = -5,      /* Q and K share elements, a view overlaps itself, or an
                                    output overlaps an input */
     ROPE_ERR_UNSUPPORTED = -6,  /* a global token index or cache row beyond 2^24 (positions
-                                   are exact in binary32 only up to there) */
+                                   are exact in binary32 only up to there); an unknown
+                                   flag bit or a nonzero reserved field; segments with
+                                   position ids; a host-call workspace below 8 tokens */
     ROPE_ERR_LAUNCH = -7,       /* the CUDA runtime refused a launch or copy */
     ROPE_ERR_THETA = -8,        /* theta or position_scale not finite and > 0 */
     ROPE_ERR_KIND = -9,         /* unknown activation kind (glu.h) */

@@ -1021,7 +1021,8 @@ const char *rope_strerror(int status)
     case ROPE_ERR_ALIGN: return "Q/K/outputs and the cos/sin cache must be 16-byte aligned (int64 position ids 8-byte), "
                                 "strides multiples of 8 elements";
     case ROPE_ERR_OVERLAP: return "Q and K overlap, a view overlaps itself, or an output overlaps an input";
-    case ROPE_ERR_UNSUPPORTED: return "global token indices and cache rows must stay within 2^24 (exact fp32 positions)";
+    case ROPE_ERR_UNSUPPORTED: return "unsupported: a global token index or cache row beyond 2^24 (exact fp32 positions), "
+                                      "an unknown flag bit, segments with position ids, or a workspace below 8 tokens";
     case ROPE_ERR_LAUNCH: return "the CUDA runtime rejected a launch";
     case ROPE_ERR_THETA: return "theta and position_scale must be finite and > 0";
     case ROPE_ERR_KIND: return "unknown activation kind";

@@ -158,3 +158,51 @@ def test_host_stream_cp_segments(dev, static):
     torch.cuda.current_stream(dev).synchronize()
     assert torch.equal(sq.view(torch.int16), ref_q.cpu()[rows].view(torch.int16))
     assert torch.equal(sk.view(torch.int16), ref_k.cpu()[rows].view(torch.int16))
+
+
+def test_host_stream_concurrent_threads(dev):
+    """Four host threads call rope_qk_host at the same time, each with its own stream,
+    workspace and pack, three calls in a row (forward, backward, forward).  The library
+    serialises the enqueueing and orders its shared copy streams with events, so every
+    thread ends with exactly what the same three calls give on the device path."""
+    import threading
+
+    from packed_varlen_rope_gb300 import workloads as wl
+
+    w, pack, q, k = _inputs(3)
+    cu = torch.from_numpy(pack.cu_seqlens).to(dev)
+    cache = pr().new_cos_sin_cache(max(pack.lengths), w.head_dim, w.theta, device=dev)
+    n = 4
+    inputs = [(wl.normal_bf16(q.shape, 610 + i), wl.normal_bf16(k.shape, 620 + i)) for i in range(n)]
+    refs = []
+    for qi, ki in inputs:
+        qd, kd = qi.to(dev), ki.to(dev)
+        for backward in (False, True, False):
+            (pr().rope_qk_bwd if backward else pr().rope_qk_fwd)(qd, kd, cu, w.theta, cos_sin_cache=cache)
+        refs.append((qd.cpu(), kd.cpu()))
+    torch.cuda.synchronize()
+    results, errors = [None] * n, []
+
+    def worker(i):
+        try:
+            torch.cuda.set_device(dev)
+            s = torch.cuda.Stream(device=dev)
+            ws = _workspace(dev, 504 + 8 * i, w)                     # a different chunking per thread
+            qh, kh = inputs[i][0].clone().pin_memory(), inputs[i][1].clone().pin_memory()
+            for backward in (False, True, False):
+                pr().rope_qk_host(qh, kh, w.theta, ws, cu_seqlens=cu, backward=backward, cos_sin_cache=cache,
+                                  stream=s)
+            s.synchronize()
+            results[i] = (qh, kh)
+        except Exception as e:                                        # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(n)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for i in range(n):
+        assert torch.equal(results[i][0].view(torch.int16), refs[i][0].view(torch.int16)), i
+        assert torch.equal(results[i][1].view(torch.int16), refs[i][1].view(torch.int16)), i

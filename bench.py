@@ -72,6 +72,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=80)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target seconds of oracle work for the CPU baseline sample")
+    ap.add_argument("--reference-seconds", type=float, default=90.0,
+                    help="--impl reference: seconds of oracle work over the warm-up and timed steps")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layout", choices=["packed", "padded", "padded-seq-used"], default="packed",
@@ -325,8 +327,7 @@ def run_reference(args, rank, world):
     t = time.perf_counter()
     step(0, cal)
     per_token = (time.perf_counter() - t) / cal
-    budget = 90.0
-    n = int(max(1, min(4096, budget / max(1, args.steps + args.warmup) / per_token)))
+    n = int(max(1, min(4096, args.reference_seconds / max(1, args.steps + args.warmup) / per_token)))
     a = 0
     for _ in range(args.warmup):
         step(a, n)
@@ -350,7 +351,8 @@ def run_reference(args, rank, world):
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
         # the same oracle calls split over every host core, beside the single-core figure
-        "cpu_baseline_all_cores": cpu_all_cores(w, pos[:qs.shape[0]], qs, ks, qs, ks),
+        "cpu_baseline_all_cores": cpu_all_cores(w, pos[np.arange(qs.shape[0]) % pack.total_tokens], qs, ks, qs,
+                                                ks),
     }
     print(json.dumps(line), flush=True)
     return 0

@@ -97,3 +97,27 @@ def test_clock_summary_keeps_the_timed_window():
     assert s["reasons"] == ["sw_power_cap"] and s["sm_max_mhz"] == 2070.0
     s = c.summary(1.5, 1.6)                              # no sample inside: warm-up + timed
     assert s["window"] == "warmup+timed" and s["samples"] == 5
+
+
+def test_reference_arm_line():
+    """bench.py --impl reference times the CPU oracle on the host and prints one JSON
+    line with the contract's keys, its own cpu_baseline and an e2e object that moves no
+    bytes between host and device."""
+    import json
+    import os
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--workload", "1",
+                        "--steps", "3", "--warmup", "1", "--reference-seconds", "1"],
+                       cwd=root, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "tokens/s" and d["value"] > 0
+    assert d["steps"] == 3 and d["warmup"] == 1 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"] == "tiny-pack-4x"

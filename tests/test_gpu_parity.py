@@ -275,6 +275,50 @@ def test_workload5_long_sampled(dev):
     assert torch.equal(q_store[-guard:].view(torch.int16), canary.view(torch.int16))
 
 
+def test_workload5_cp_rank_long_segments(dev):
+    """A load-balanced context-parallel rank of the 1,048,576-token sequence (cp = 2,
+    rank 0: chunks 0 and 3 of 4): its 2^19 rows of 32 Q heads span 2^31 elements, so the
+    64-bit-offset instance runs with a two-entry segment list whose second segment
+    starts at token 786,432.  Seeded rows, the rows around the segment boundary and the
+    last rows (which end at Q's flat offset 2^31) equal the oracle; a canary after Q
+    survives."""
+    from packed_varlen_rope_gb300 import cp_shards, shard_rows, shard_segments
+    from packed_varlen_rope_gb300 import workloads as wl
+
+    w = wl.WORKLOADS[5]
+    pack = wl.make_pack(w)
+    T = pack.total_tokens
+    shards = cp_shards(T, 2, 0)
+    segs = shard_segments(shards)
+    n = len(shard_rows(shards))
+    assert n == T // 2 and segs == [(0, 0), (T // 4, 3 * T // 4)]
+    guard = 4096
+    q_store = torch.empty(n * w.n_q_heads * w.head_dim + guard, dtype=torch.bfloat16, device=dev)
+    q = q_store[: n * w.n_q_heads * w.head_dim].view(n, w.n_q_heads, w.head_dim)
+    q.copy_(wl.normal_bf16((n, w.n_q_heads, w.head_dim), 5100, device="cuda"))
+    canary = torch.full((guard,), -3.5, dtype=torch.bfloat16, device=dev)
+    q_store[-guard:].copy_(canary)
+    k = wl.normal_bf16((n, w.n_kv_heads, w.head_dim), 5200, device="cuda")
+    cu_dev = torch.from_numpy(pack.cu_seqlens).to(dev)
+    info = pr().rope_qk_launch_info(q, k, w.theta, cu_seqlens=cu_dev, segments=segs)
+    assert info.kernel_name() == "rope_qk_tile_kernel<128,true>"
+    rng = np.random.Generator(np.random.PCG64(5300))
+    cross = (1 << 31) // (w.n_q_heads * w.head_dim)
+    fixed = [r for r in (0, 1, T // 4 - 1, T // 4, T // 4 + 1, cross - 2, cross - 1, cross, n - 1) if r < n]
+    rows = np.unique(np.concatenate([rng.integers(0, n, 2048), fixed])).astype(np.int64)
+    rows_dev = torch.from_numpy(rows).to(dev)
+    q0, k0 = to_bits(q[rows_dev]), to_bits(k[rows_dev])
+    pr().rope_qk_apply(q, k, w.theta, cu_seqlens=cu_dev, segments=segs)     # no cache: evaluated in the kernel
+    torch.cuda.synchronize()
+    tokens = np.where(rows < T // 4, rows, rows - T // 4 + 3 * T // 4)
+    pos = oracle.positions(pack.cu_seqlens, T)[tokens]
+    for x, y in ((q0, q), (k0, k)):
+        s = compare(to_bits(y[rows_dev]), oracle.rope_rows(x, pos, w.theta), x)
+        assert_parity(s, "w5 cp rank")
+        assert s["bit_mismatch"] == 0, s
+    assert torch.equal(q_store[-guard:].view(torch.int16), canary.view(torch.int16))
+
+
 # ------------------------------------------------------------------ edge cases
 
 EDGE_PACKS = [

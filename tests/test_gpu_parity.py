@@ -595,6 +595,26 @@ def test_rotary_embedding_cp_segments_autograd(dev):
     assert rope.cache(dev, 1).rows >= int(rows.max()) + 1
 
 
+def test_rotary_embedding_without_cache(dev):
+    """RotaryEmbedding(use_cache=False) builds no table and gives the bits of the cached
+    module, forward and autograd backward."""
+    from packed_varlen_rope_gb300 import RotaryEmbedding
+
+    w, pack, q, k, dq, dk = _workload_inputs(2)
+    cu_dev = torch.from_numpy(pack.cu_seqlens).to(dev)
+    outs = []
+    for use_cache in (True, False):
+        rope = RotaryEmbedding(w.head_dim, w.theta, use_cache=use_cache)
+        qleaf = torch.zeros_like(q, requires_grad=True)
+        kleaf = torch.zeros_like(k, requires_grad=True)
+        yq, yk = rope(qleaf + q, kleaf + k, cu_seqlens=cu_dev)
+        torch.autograd.backward([yq, yk], [dq, dk])
+        outs.append((yq.detach(), yk.detach(), qleaf.grad, kleaf.grad))
+        assert (len(rope._caches) == 1) == use_cache
+    for a, b in zip(*outs):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
 def test_rotary_embedding_int64_position_ids(dev):
     """RotaryEmbedding with int64 position ids (a Hugging Face collator's dtype), forward
     and autograd backward, against the oracle on the same positions."""

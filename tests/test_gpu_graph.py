@@ -1,10 +1,13 @@
 """The entry points inside a captured CUDA graph (needs a GB300): none of them
 synchronises or allocates, and rope_qk_host joins its copy streams to the caller's
 stream through events, so a training step that captures them replays them exactly.
-One graph holds a forward on (Q, K), a backward on (dQ, dK), a SwiGLU forward and
-backward and a host-streamed rotation; it is replayed on fresh inputs copied into the
-captured buffers and must give what the same calls give eagerly, bit for bit (the
-eager results are themselves pinned to the oracle by the other tests)."""
+One graph holds a forward on (Q, K), a backward on (dQ, dK), the backward of a
+context-parallel rank's buffer through a segment list with cos/sin evaluated in the
+kernel, a SwiGLU forward and backward and a host-streamed rotation; it is replayed on
+fresh inputs copied into the captured buffers and must give what the same calls give
+eagerly, bit for bit (the eager results are themselves pinned to the oracle by the
+other tests).  The segment list is copied into the kernel's arguments at capture, so
+the replay does not depend on the host array."""
 from __future__ import annotations
 
 import pytest
@@ -44,15 +47,20 @@ def test_captured_graph_replays_bit_identical(dev):
                 "g": wl.normal_bf16((rows, cols), seed + 6, device=dev),
                 "dh": wl.normal_bf16((rows, cols), seed + 7, device=dev),
                 "hq": wl.normal_bf16((2048, hq, d), seed + 8, device="cpu").pin_memory(),
-                "hk": wl.normal_bf16((2048, hkv, d), seed + 9, device="cpu").pin_memory()}
+                "hk": wl.normal_bf16((2048, hkv, d), seed + 9, device="cpu").pin_memory(),
+                "cq": wl.normal_bf16((T // 2, hq, d), seed + 10, device=dev),
+                "ck": wl.normal_bf16((T // 2, hkv, d), seed + 11, device=dev)}
 
     per_token = (hq + hkv) * d * 2
     workspace = torch.empty(2 * 512 * per_token, dtype=torch.uint8, device=dev)
     host_cu = torch.tensor([0, 700, 2048], dtype=torch.int32, device=dev)
 
+    segs = pr.shard_segments(pr.cp_shards(T, 2, 1))
+
     def step(x, out):
         pr.rope_qk_fwd(x["q"], x["k"], cu, w.theta, cos_sin_cache=cache)
         pr.rope_qk_bwd(x["dq"], x["dk"], cu, w.theta, cos_sin_cache=cache)
+        pr.rope_qk_apply(x["cq"], x["ck"], w.theta, cu_seqlens=cu, segments=list(segs), backward=True)
         pr.glu_fwd("swiglu", x["e"], x["g"], out["h"])
         pr.glu_bwd("swiglu", x["dh"], x["e"], x["g"], out["de"], out["dg"])
         pr.rope_qk_host(x["hq"], x["hk"], w.theta, workspace, cu_seqlens=host_cu, cos_sin_cache=cache,
@@ -88,7 +96,7 @@ def test_captured_graph_replays_bit_identical(dev):
     torch.cuda.synchronize()
     graph.replay()
     torch.cuda.synchronize()
-    for n in ("q", "k", "dq", "dk"):
+    for n in ("q", "k", "dq", "dk", "cq", "ck"):
         assert torch.equal(static_in[n], eager_in[n]), n
     for n in ("h", "de", "dg", "hq", "hk"):
         assert torch.equal(static_out[n], eager_out[n]), n
@@ -97,3 +105,4 @@ def test_captured_graph_replays_bit_identical(dev):
     step(eager_in, eager_out)
     torch.cuda.synchronize()
     assert torch.equal(static_in["q"], eager_in["q"]) and torch.equal(static_in["dk"], eager_in["dk"])
+    assert torch.equal(static_in["cq"], eager_in["cq"]) and torch.equal(static_in["ck"], eager_in["ck"])

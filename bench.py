@@ -450,7 +450,7 @@ def parity_block(gpu_outputs, oracle_outputs, inputs):
 
     n_el = mism = 0
     max_ulp = 0
-    for got, ref, x in zip(gpu_outputs, oracle_outputs, inputs):
+    for got, ref, _x in zip(gpu_outputs, oracle_outputs, inputs):
         g = got[: ref.shape[0]]
         n_el += g.size
         diff = g != ref
@@ -504,7 +504,7 @@ def run_ours(args, rank, world, local):
     k = wl.normal_bf16(shape_k, wl.seed(args.workload, "k", seed_rank), device=dev)
     dq = wl.normal_bf16(shape_q, wl.seed(args.workload, "dq", seed_rank), device=dev)
     dk = wl.normal_bf16(shape_k, wl.seed(args.workload, "dk", seed_rank), device=dev)
-    segs = shards = local_pos = None
+    segs = shards = None
     rank_tokens = pack.valid_tokens                       # tokens this rank rotates per pass
     if cp > 1:
         # this rank's chunks, one after the other in its own buffers (padding rows past the

@@ -15,7 +15,7 @@ from parity_util import from_bits, to_bits
 pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
-N_CASES = 80
+N_CASES = 400
 
 
 @pytest.fixture(scope="module")

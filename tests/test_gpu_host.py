@@ -206,3 +206,91 @@ def test_host_stream_concurrent_threads(dev):
     for i in range(n):
         assert torch.equal(results[i][0].view(torch.int16), refs[i][0].view(torch.int16)), i
         assert torch.equal(results[i][1].view(torch.int16), refs[i][1].view(torch.int16)), i
+
+
+@pytest.mark.parametrize("case", range(48))
+def test_host_paths_random_options_match_oracle(dev, case):
+    """Seeded random host-buffer calls against the oracle: random packs (empty samples,
+    rows past the pack), head shapes, chunkings (a workspace of 8 to 600 tokens, or the
+    library's static array), positions from cu_seqlens with a token offset, a segment
+    list or seq_used, or from int32 / int64 ids, forward or backward, in place or into
+    separate host outputs, pinned or pageable host memory."""
+    rng = np.random.Generator(np.random.PCG64(31000 + case))
+    d = int(rng.choice([16, 32, 64, 96, 128]))
+    hq = int(rng.integers(1, 9))
+    hkv = int(rng.integers(1, hq + 1))
+    lengths = rng.integers(0, 300, size=int(rng.integers(1, 9)))
+    lengths[rng.random(lengths.size) < 0.2] = 0
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    pack_tokens = int(cu[-1])
+    theta = float(rng.choice([1.0e4, 5.0e5, 1.0e6]))
+    bwd = bool(rng.integers(0, 2))
+    static = bool(rng.integers(0, 2))
+    out_of_place = bool(rng.integers(0, 2))
+    pinned = bool(rng.integers(0, 3))
+    source = str(rng.choice(["cu", "offset", "segments", "seq_used", "ids32", "ids64"]))
+    kw = {}
+    T = max(1, pack_tokens + int(rng.integers(0, 5)))
+    full = oracle.positions(cu, max(pack_tokens, 2 * T + 8))
+    if source == "cu":
+        pos = full[:T]
+        kw["cu_seqlens"] = torch.from_numpy(cu).to(dev)
+    elif source == "offset":
+        off = int(rng.integers(0, max(1, pack_tokens)))
+        T = max(1, int(rng.integers(1, pack_tokens - off + 5)))
+        pos = full[off:off + T]
+        kw.update(cu_seqlens=torch.from_numpy(cu).to(dev), token_offset=off)
+    elif source == "segments":
+        cut = int(rng.integers(1, T)) if T > 1 else 0
+        starts = [0] + ([cut] if cut else [])
+        toks = [int(rng.integers(0, pack_tokens + 4)) for _ in starts]
+        ends = starts[1:] + [T]
+        tokens = np.concatenate([np.arange(t0, t0 + e - r0) for r0, t0, e in zip(starts, toks, ends)])
+        pos = oracle.positions(cu, max(pack_tokens, int(tokens.max()) + 1))[tokens]
+        kw.update(cu_seqlens=torch.from_numpy(cu).to(dev), segments=list(zip(starts, toks)))
+    elif source == "seq_used":
+        used = np.array([int(rng.integers(0, L + 1)) for L in lengths], np.int32)
+        pos = full[:T].copy()
+        s_of = np.searchsorted(cu[1:], np.arange(T), side="right")
+        inside = pos >= 0
+        pos[inside & (pos >= used[np.minimum(s_of, lengths.size - 1)])] = -1
+        kw.update(cu_seqlens=torch.from_numpy(cu).to(dev), seq_used=torch.from_numpy(used).to(dev))
+    else:
+        ids = rng.integers(-3, 1 << 24, size=T).astype(np.int64)
+        ids[rng.random(T) < 0.05] = (1 << 24) + 5
+        if source == "ids64":
+            kw["position_ids"] = torch.from_numpy(ids).to(dev)
+            pos = np.where((ids >= 0) & (ids < (1 << 24)), ids, -1)
+        else:
+            ids32 = ids.astype(np.int32)
+            kw["position_ids"] = torch.from_numpy(ids32).to(dev)
+            pos = np.where((ids32 >= 0) & (ids32 < (1 << 24)), ids32, -1)
+    pos = np.asarray(pos, np.int32)
+
+    def bits(shape):
+        f = torch.from_numpy(rng.standard_normal(size=shape).astype(np.float32))
+        return f.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+    qb, kb = bits((T, hq, d)), bits((T, hkv, d))
+    qh = torch.from_numpy(qb.view(np.int16).copy()).view(torch.bfloat16)
+    kh = torch.from_numpy(kb.view(np.int16).copy()).view(torch.bfloat16)
+    if pinned:
+        qh, kh = qh.pin_memory(), kh.pin_memory()
+    ws = None if static else _workspace_tokens(dev, int(rng.integers(8, 601)), hq, hkv, d)
+    if out_of_place:
+        qo, ko = torch.full_like(qh, 5.0), torch.full_like(kh, 5.0)
+        pr().rope_qk_host(qh, kh, theta, ws, backward=bwd, q_out=qo, k_out=ko, device=dev, **kw)
+    else:
+        qo, ko = qh, kh
+        pr().rope_qk_host(qh, kh, theta, ws, backward=bwd, device=dev, **kw)
+    torch.cuda.synchronize()
+    what = (case, d, hq, hkv, source, static, out_of_place, bwd, pinned)
+    assert np.array_equal(to_bits(qo), oracle.rope_rows(qb, pos, theta, bwd)), what
+    assert np.array_equal(to_bits(ko), oracle.rope_rows(kb, pos, theta, bwd)), what
+    if out_of_place:
+        assert np.array_equal(to_bits(qh), qb) and np.array_equal(to_bits(kh), kb), what
+
+
+def _workspace_tokens(dev, tokens, hq, hkv, d):
+    per_token = (hq + hkv) * d * 2
+    return torch.empty(2 * tokens * per_token + 4096, dtype=torch.uint8, device=dev)

@@ -255,9 +255,12 @@ int rope_qk_apply(const rope_qk_desc *desc, void *stream);
  * CUDA call: the rotation kernel's compile-time instance (head_dim 64, 96, 128 or 256,
  * or 0 for the generic one), whether it uses 64-bit element offsets (some view spans
  * 2^31 elements or more; unsloth.ai page, section "Indexage int64 pour les kernels
- * Triton"), and its grid: one CTA of `threads` threads per tile of `tile_tokens`
- * consecutive tokens.  Returns the status rope_qk_apply's argument checks give (the
- * cache's device is not checked); grid == 0 when there is nothing to launch.
+ * Triton"), how many 16-byte pair units each thread keeps in flight (2, or 4 for
+ * launches of at least 32,768 tiles with 32-bit offsets, a compile-time head_dim and a
+ * cos/sin cache), and its grid: one CTA
+ * of `threads` threads per tile of `tile_tokens` consecutive tokens.  Returns the
+ * status rope_qk_apply's argument checks give (the cache's device is not checked);
+ * grid == 0 when there is nothing to launch.
  */
 typedef struct rope_qk_launch {
     int32_t head_dim_instance;
@@ -266,6 +269,7 @@ typedef struct rope_qk_launch {
     int32_t tile_tokens;
     int32_t threads;
     int32_t smem_bytes;            /* dynamic shared memory per CTA (cos/sin rows)    */
+    int32_t unroll;                /* pair units in flight per thread                 */
 } rope_qk_launch;
 
 int rope_qk_launch_info(const rope_qk_desc *desc, rope_qk_launch *info);

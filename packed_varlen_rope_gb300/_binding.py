@@ -76,11 +76,13 @@ class RopeQKLaunch(ctypes.Structure):
     """Mirror of ``rope_qk_launch``: what rope_qk_apply launches for a descriptor."""
 
     _fields_ = [("head_dim_instance", ctypes.c_int32), ("long_index", ctypes.c_int32), ("grid", ctypes.c_int32),
-                ("tile_tokens", ctypes.c_int32), ("threads", ctypes.c_int32), ("smem_bytes", ctypes.c_int32)]
+                ("tile_tokens", ctypes.c_int32), ("threads", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
+                ("unroll", ctypes.c_int32)]
 
     def kernel_name(self) -> str:
-        """The rotation kernel's instance as its template reads: rope_qk_tile_kernel<D, LONG>."""
-        return "rope_qk_tile_kernel<%d,%s>" % (self.head_dim_instance, "true" if self.long_index else "false")
+        """The rotation kernel's instance as its template reads: rope_qk_tile_kernel<D, LONG, U>."""
+        return "rope_qk_tile_kernel<%d,%s,%d>" % (self.head_dim_instance, "true" if self.long_index else "false",
+                                                  self.unroll)
 
 
 class CosSinCache:

@@ -41,7 +41,9 @@
 namespace {
 
 constexpr int kThreads = 128;           // threads per CTA (9 CTAs per SM at 56 registers)
-constexpr int kUnroll = 2;              // pair units in flight per thread (4 x 16-byte loads)
+constexpr int kTileUnits = 512;         // about this many 16-byte pair units per tile
+constexpr int kWideGrid = 32768;        // tiles from which a launch with a cos/sin cache
+                                        // keeps 4 pair units in flight per thread, not 2
 constexpr int kMaxHalf = 128;           // head_dim <= 256
 constexpr int kMaxTileTokens = 32;      // one warp resolves the tile's positions
 constexpr int kMaxSegments = ROPE_MAX_SEGMENTS;
@@ -192,7 +194,7 @@ __device__ __forceinline__ void rotate2(uint32_t &lo, uint32_t &hi, float4 cs)
 // (cos, sin) of frequencies 8c+2q and 8c+2q+1.  The eight threads of a 16-byte load
 // phase (consecutive chunks of one head) read eight consecutive float4: no bank
 // conflicts.
-template <int D, bool LONG>
+template <int D, bool LONG, int U>
 __global__ void __launch_bounds__(kThreads)
 rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
 {
@@ -235,18 +237,18 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    // 0. the tile's first batch of Q/K units (kUnroll per thread) is loaded before the
+    // 0. the tile's first batch of Q/K units (U per thread) is loaded before the
     //    positions are known: the loads do not depend on them, so HBM starts streaming
     //    while the position search and the cos/sin staging run.  An in-place row found
     //    to lie outside the pack is then simply not stored.  With seq_used (a padded
     //    batch whose pad rows are left out), whole tiles may hold no row to rotate, so
     //    the first batch waits for the positions there and skips those rows' loads.
     const bool early = a.seq_used == nullptr;
-    uint4 first_lo[kUnroll], first_hi[kUnroll];
-    __nv_bfloat16 *first_dst[kUnroll];
-    uint32_t first_tok[kUnroll], first_chunk[kUnroll];
+    uint4 first_lo[U], first_hi[U];
+    __nv_bfloat16 *first_dst[U];
+    uint32_t first_tok[U], first_chunk[U];
 #pragma unroll
-    for (int k = 0; k < kUnroll; ++k) {
+    for (int k = 0; k < U; ++k) {
         const uint32_t u = threadIdx.x + k * kThreads;
         first_dst[k] = nullptr;
         first_tok[k] = 0;
@@ -342,12 +344,12 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
     __syncthreads();
 
     // 3. stream the tile: rotate and store the first batch, then load a batch of units
-    //    (kUnroll per thread, 4 loads of 16 B in flight), rotate, store, and so on.  Rows
+    //    (U per thread, 4 loads of 16 B in flight), rotate, store, and so on.  Rows
     //    of tokens outside the pack are not touched in place and are copied unchanged
     //    out of place.
     if (!early) {
 #pragma unroll
-        for (int k = 0; k < kUnroll; ++k) {
+        for (int k = 0; k < U; ++k) {
             const uint32_t u = threadIdx.x + k * kThreads;
             if (u >= units) continue;
             const __nv_bfloat16 *src;
@@ -360,7 +362,7 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
         }
     }
 #pragma unroll
-    for (int k = 0; k < kUnroll; ++k) {
+    for (int k = 0; k < U; ++k) {
         if (first_dst[k] == nullptr) continue;
         const int pos = s_pos[first_tok[k]];
         if (pos < 0 && a.in_place) continue;
@@ -374,13 +376,13 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
         store_stream(first_dst[k], first_lo[k]);
         store_stream(first_dst[k] + h, first_hi[k]);
     }
-    for (uint32_t base = threadIdx.x + kUnroll * kThreads; base < units; base += kUnroll * kThreads) {
-        uint4 lo[kUnroll], hi[kUnroll];
-        __nv_bfloat16 *dst[kUnroll];
-        int tok[kUnroll], chunk[kUnroll];
-        bool live[kUnroll];
+    for (uint32_t base = threadIdx.x + U * kThreads; base < units; base += U * kThreads) {
+        uint4 lo[U], hi[U];
+        __nv_bfloat16 *dst[U];
+        int tok[U], chunk[U];
+        bool live[U];
 #pragma unroll
-        for (int k = 0; k < kUnroll; ++k) {
+        for (int k = 0; k < U; ++k) {
             const uint32_t u = base + k * kThreads;
             live[k] = false;
             tok[k] = -1;
@@ -403,7 +405,7 @@ rope_qk_tile_kernel(const __grid_constant__ RopeArgs a)
             }
         }
 #pragma unroll
-        for (int k = 0; k < kUnroll; ++k) {
+        for (int k = 0; k < U; ++k) {
             if (!live[k]) continue;
             if (tok[k] >= 0) {
                 const float4 *cs = s_cs + (tok[k] * 4) * cph + chunk[k];
@@ -523,15 +525,15 @@ int check_scale(double scale)
     return ROPE_OK;
 }
 
-// Tokens per tile: enough 16-byte pair units that every thread has about 2 * kUnroll of
-// them, capped by the one-warp position search.  Half that (one batch per thread, so
+// Tokens per tile: about kTileUnits 16-byte pair units (two batches of 2 units per
+// thread), capped by the one-warp position search.  Half that (one batch per thread, so
 // 1-token tiles on 40 heads of 128) measured 1.5 % faster with a cos/sin cache on 16,384
 // tokens but 12 % slower without one and 16 % slower on a padded batch under seq_used,
 // where each tile's position search and cos/sin staging serve half as many tokens.
 int pick_tile_tokens(int h_tot, int head_dim)
 {
     const int units_per_token = h_tot * (head_dim / 16);
-    const int target = 2 * kUnroll * kThreads;
+    const int target = kTileUnits;
     int tt = (target + units_per_token - 1) / units_per_token;
     if (tt < 1) tt = 1;
     if (tt > kMaxTileTokens) tt = kMaxTileTokens;
@@ -543,11 +545,11 @@ int pick_tile_tokens(int h_tot, int head_dim)
 // for it before reading anything), which hides the launch gap between back-to-back
 // rotations (measured: fwd+bwd step -0.7 % on 65,536 tokens, -4 % on 16,384, -9 % on
 // 7,714).
-template <int D, bool LONG>
+template <int D, bool LONG, int U>
 cudaError_t launch_tile(const RopeArgs &a, int grid, size_t smem, cudaStream_t stream, bool pdl)
 {
     if (!pdl) {
-        rope_qk_tile_kernel<D, LONG><<<grid, kThreads, smem, stream>>>(a);
+        rope_qk_tile_kernel<D, LONG, U><<<grid, kThreads, smem, stream>>>(a);
         return cudaGetLastError();
     }
     cudaLaunchAttribute attr[1];
@@ -560,18 +562,19 @@ cudaError_t launch_tile(const RopeArgs &a, int grid, size_t smem, cudaStream_t s
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, rope_qk_tile_kernel<D, LONG>, a);
+    return cudaLaunchKernelEx(&cfg, rope_qk_tile_kernel<D, LONG, U>, a);
 }
 
-template <bool LONG>
+// The generic head_dim instance keeps 2 pair units per thread.
+template <bool LONG, int U>
 cudaError_t dispatch_dim(const RopeArgs &a, int grid, size_t smem, cudaStream_t stream, bool pdl)
 {
     switch (a.head_dim) {
-    case 64: return launch_tile<64, LONG>(a, grid, smem, stream, pdl);
-    case 96: return launch_tile<96, LONG>(a, grid, smem, stream, pdl);
-    case 128: return launch_tile<128, LONG>(a, grid, smem, stream, pdl);
-    case 256: return launch_tile<256, LONG>(a, grid, smem, stream, pdl);
-    default: return launch_tile<0, LONG>(a, grid, smem, stream, pdl);
+    case 64: return launch_tile<64, LONG, U>(a, grid, smem, stream, pdl);
+    case 96: return launch_tile<96, LONG, U>(a, grid, smem, stream, pdl);
+    case 128: return launch_tile<128, LONG, U>(a, grid, smem, stream, pdl);
+    case 256: return launch_tile<256, LONG, U>(a, grid, smem, stream, pdl);
+    default: return launch_tile<0, LONG, 2>(a, grid, smem, stream, pdl);
     }
 }
 
@@ -731,6 +734,7 @@ struct Launch {
     int grid = 0;
     size_t smem = 0;
     int d_instance = 0;
+    int unroll = 2;
     bool long_index = false;
 };
 
@@ -825,6 +829,12 @@ int plan_rotation(const rope_qk_desc *dp, Launch *L, bool check_device)
     for (const View *v : {&q, &k, &qo, &ko})
         L->long_index = L->long_index || v->span_elems() > INT32_MAX;
     L->d_instance = instance_for(p.head_dim);
+    // Pair units in flight per thread: 4 for large launches with 32-bit offsets that read
+    // their cos/sin from a cache (the tile's first batch then covers most of a wide
+    // token's units before the position search), 2 otherwise (more resident CTAs, a
+    // cheaper evaluation of cos/sin in the kernel, lighter 64-bit address arithmetic);
+    // the generic head_dim instance always 2.
+    L->unroll = a.cache != nullptr && L->grid >= kWideGrid && !L->long_index && L->d_instance != 0 ? 4 : 2;
     return ROPE_OK;
 }
 
@@ -834,8 +844,12 @@ int rope_qk_apply_impl(const rope_qk_desc *dp, void *stream, bool pdl)
     const int rc = plan_rotation(dp, &L, true);
     if (rc != ROPE_OK || L.grid == 0) return rc;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const cudaError_t err = L.long_index ? dispatch_dim<true>(L.a, L.grid, L.smem, s, pdl)
-                                         : dispatch_dim<false>(L.a, L.grid, L.smem, s, pdl);
+    cudaError_t err;
+    if (L.unroll == 4)
+        err = dispatch_dim<false, 4>(L.a, L.grid, L.smem, s, pdl);
+    else
+        err = L.long_index ? dispatch_dim<true, 2>(L.a, L.grid, L.smem, s, pdl)
+                           : dispatch_dim<false, 2>(L.a, L.grid, L.smem, s, pdl);
     return err == cudaSuccess ? ROPE_OK : ROPE_ERR_LAUNCH;
 }
 
@@ -958,6 +972,7 @@ int rope_qk_launch_info(const rope_qk_desc *desc, rope_qk_launch *info)
     info->tile_tokens = L.grid > 0 ? L.a.tile_tokens : 0;
     info->threads = L.grid > 0 ? kThreads : 0;
     info->smem_bytes = static_cast<int32_t>(L.smem);
+    info->unroll = L.grid > 0 ? L.unroll : 0;
     return ROPE_OK;
 }
 

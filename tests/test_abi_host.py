@@ -478,12 +478,23 @@ def test_launch_info_names_the_dispatched_instance(lib):
         return out
 
     w4 = info(65536, 64, 8, 128)
-    assert w4.kernel_name() == "rope_qk_tile_kernel<128,false>"
-    assert (w4.tile_tokens, w4.threads, w4.grid) == (1, 128, 65536)
+    assert w4.kernel_name() == "rope_qk_tile_kernel<128,false,2>"          # no cache: 2 units per thread
+    assert (w4.tile_tokens, w4.threads, w4.grid, w4.unroll) == (1, 128, 65536, 2)
+    # with a cos/sin cache, a launch of at least 32,768 tiles keeps 4 units per thread in flight
+    cache = cache_desc(lib, rows=4096, d=128, theta=1e6, data=CACHE)
+    assert info(65536, 64, 8, 128, cos_sin_cache=ctypes.pointer(cache)).kernel_name() == \
+        "rope_qk_tile_kernel<128,false,4>"
+    assert info(32768, 64, 8, 128, cos_sin_cache=ctypes.pointer(cache)).unroll == 4   # exactly 32,768 tiles
+    assert info(32767, 64, 8, 128, cos_sin_cache=ctypes.pointer(cache)).unroll == 2
+    assert info(16384, 32, 8, 128, cos_sin_cache=ctypes.pointer(cache)).unroll == 2    # 8,192 tiles
     w5 = info(1 << 20, 32, 8, 128)
-    assert w5.kernel_name() == "rope_qk_tile_kernel<128,true>" and w5.grid == (1 << 20) // w5.tile_tokens
-    assert info(4096, 4, 2, 80).kernel_name() == "rope_qk_tile_kernel<0,false>"
-    assert info(64, 4, 2, 64).kernel_name() == "rope_qk_tile_kernel<64,false>"
+    assert w5.kernel_name() == "rope_qk_tile_kernel<128,true,2>" and w5.grid == (1 << 20) // w5.tile_tokens
+    assert info(1 << 20, 32, 8, 128, cos_sin_cache=ctypes.pointer(cache)).kernel_name() == \
+        "rope_qk_tile_kernel<128,true,2>"                                  # 64-bit offsets: 2
+    assert info(4096, 4, 2, 80).kernel_name() == "rope_qk_tile_kernel<0,false,2>"
+    assert info(1 << 16, 64, 8, 80, cos_sin_cache=ctypes.pointer(cache_desc(lib, rows=64, d=80, theta=1e6,
+                                                                              data=CACHE))).unroll == 2  # generic
+    assert info(64, 4, 2, 64).kernel_name() == "rope_qk_tile_kernel<64,false,2>"
     # head-major views of 2^19 tokens x 32 heads: the head stride makes the span pass 2^31
     hm = info(1 << 19, 32, 8, 128, q_stride_token=128, q_stride_head=(1 << 19) * 128)
     assert hm.long_index == 1

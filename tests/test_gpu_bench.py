@@ -51,7 +51,7 @@ def test_rope_bench_line_small():
                 "cpu_baseline", "cpu_baseline_all_cores", "e2e", "clocks", "gpu_launches", "parity"):
         assert key in d, key
     assert d["parity"]["bit_mismatch"] == 0 and d["gpu_launches"] == 40
-    assert d["roofline"]["kernel"] == "rope_qk_tile_kernel<128,false>"
+    assert d["roofline"]["kernel"] == "rope_qk_tile_kernel<128,false,2>"    # 8,192 tiles: 2 units per thread
     assert d["roofline"]["grid"]["ctas"] * d["roofline"]["grid"]["tile_tokens"] >= 16384
     assert d["e2e"]["h2d_bytes_per_step"] == d["e2e"]["d2h_bytes_per_step"] > 0
 
@@ -92,4 +92,5 @@ def test_rope_head_shapes():
         assert 0 < s["frac"] < 2, name
         dim = int(name.split("/")[2])
         want = dim if dim in (64, 96, 128, 256) else 0
-        assert s["kernel"] == "rope_qk_tile_kernel<%d,false>" % want, (name, s["kernel"])
+        unroll = 4 if want and s["tokens"] // s["tile_tokens"] >= 32768 else 2   # wide 32-bit launches, a cache
+        assert s["kernel"] == "rope_qk_tile_kernel<%d,false,%d>" % (want, unroll), (name, s["kernel"])

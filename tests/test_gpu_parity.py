@@ -301,7 +301,7 @@ def test_workload5_cp_rank_long_segments(dev):
     k = wl.normal_bf16((n, w.n_kv_heads, w.head_dim), 5200, device="cuda")
     cu_dev = torch.from_numpy(pack.cu_seqlens).to(dev)
     info = pr().rope_qk_launch_info(q, k, w.theta, cu_seqlens=cu_dev, segments=segs)
-    assert info.kernel_name() == "rope_qk_tile_kernel<128,true>"
+    assert info.kernel_name() == "rope_qk_tile_kernel<128,true,2>"          # no cache: 2 units per thread
     rng = np.random.Generator(np.random.PCG64(5300))
     cross = (1 << 31) // (w.n_q_heads * w.head_dim)
     fixed = [r for r in (0, 1, T // 4 - 1, T // 4, T // 4 + 1, cross - 2, cross - 1, cross, n - 1) if r < n]

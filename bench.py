@@ -301,12 +301,28 @@ def run_reference(args, rank, world):
     import numpy as np
 
     import oracle
+    from packed_varlen_rope_gb300 import shards as shp
     from packed_varlen_rope_gb300 import workloads as wl
 
     oracle.build()
     w = wl.WORKLOADS[args.workload]
-    pack = wl.make_pack(w)
+    if args.layout != "packed" and w.padded_samples is None:
+        print("--layout %s needs a workload with padded samples (3)" % args.layout, file=sys.stderr)
+        return 2
+    # the pack, layout and context-parallel shard our arm times, so that both lines carry
+    # the same config; the oracle is timed on consecutive rows of it
+    pack = wl.make_pack(w, "packed" if args.layout == "packed" else "padded", rank=0)
+    cp, shards, segs, rank_tokens = args.cp_size, None, None, None
+    if cp > 1:
+        if args.layout != "packed" or not 0 <= args.cp_rank < cp:
+            print("--cp-size needs the packed layout and 0 <= --cp-rank < --cp-size", file=sys.stderr)
+            return 2
+        shards = shp.cp_shards(pack.total_tokens, cp, args.cp_rank, load_balanced=True)
+        segs = shp.shard_segments(shards)
+        rank_tokens = sum(1 for r in shp.shard_rows(shards) if r < pack.total_tokens)
     pos = oracle.positions(pack.cu_seqlens, pack.total_tokens)
+    if cp > 1:                                            # the rank's own rows, padding left out
+        pos = pos[np.array([r for r in shp.shard_rows(shards) if r < pack.total_tokens], dtype=np.int64)]
     import torch
 
     def bits(shape, kind):
@@ -314,7 +330,7 @@ def run_reference(args, rank, world):
         return t.view(torch.int16).numpy().view(np.uint16)
 
     def step(a, n):
-        idx = np.arange(a, a + n) % pack.total_tokens
+        idx = np.arange(a, a + n) % len(pos)
         p = pos[idx]
         oracle.rope_rows(qs[:n], p, w.theta)
         oracle.rope_rows(ks[:n], p, w.theta)
@@ -343,19 +359,51 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": w.name, "tokens_per_step": n, "n_q_heads": w.n_q_heads,
-                   "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "theta": w.theta},
+        "config": rope_config(args, w, pack, world, args.cp_rank if cp > 1 else 0, shards, segs, rank_tokens),
+        "reference_tokens_per_step": n,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": "%d consecutive tokens of the %s pack per step (fwd+bwd of Q and K)"
-                                   % (n, w.name)},
+                         "sample": "%d consecutive tokens of the %s pack%s per step (fwd+bwd of Q and K)"
+                                   % (n, w.name, " (this rank's rows)" if cp > 1 else "")},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
         # the same oracle calls split over every host core, beside the single-core figure
-        "cpu_baseline_all_cores": cpu_all_cores(w, pos[np.arange(qs.shape[0]) % pack.total_tokens], qs, ks, qs,
+        "cpu_baseline_all_cores": cpu_all_cores(w, pos[np.arange(qs.shape[0]) % len(pos)], qs, ks, qs,
                                                 ks),
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def rope_config(args, w, pack, world, cp_rank=0, shards=None, segs=None, rank_tokens=None):
+    """The workload description both arms print as ``config`` (the same keys and values
+    for the same arguments): shape, pack, layout, parallelism, L2 note and cos/sin
+    source."""
+    import numpy as np
+
+    cp = args.cp_size
+    rank_tokens = pack.valid_tokens if rank_tokens is None else rank_tokens
+    rows_moved = pack.total_tokens if args.layout == "padded" else rank_tokens
+    bytes_per_pass = 4 * (w.n_q_heads + w.n_kv_heads) * w.head_dim * rows_moved
+    span = int(np.max(np.diff(pack.cu_seqlens)))
+    return {
+        "workload": w.name, "total_tokens": pack.total_tokens, "valid_tokens": pack.valid_tokens,
+        "n_seqs": pack.n_seqs, "max_seq_len": max(pack.lengths), "n_q_heads": w.n_q_heads,
+        "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "theta": w.theta,
+        "layout": {"packed": "packed [T, H, d] bf16, in place",
+                   "padded": "padded batch [B*pad_to, H, d] bf16, every row rotated, in place",
+                   "padded-seq-used": "padded batch [B*pad_to, H, d] bf16, pad rows skipped (seq_used)"
+                   }[args.layout],
+        "valid_fraction": valid_fraction(pack),
+        "parallelism": ("cp%d (rank %d of a load-balanced context-parallel group%s)"
+                        % (cp, cp_rank, "" if world > 1 else ", emulated on one GPU")
+                        if cp > 1 else "dp%d (independent packs)" % world),
+        "l2": "no flush: Q, K, dQ, dK = %.2f GB per step > 129 MB L2" % (bytes_per_pass / 1e9),
+        "cp_shards": None if cp <= 1 else {"token_start_rows": shards, "segments": segs,
+                                           "rank_tokens": rank_tokens},
+        "cos_sin": ("evaluated per tile, no cache (binary32 double-float; binary64 where the rounding "
+                    "is undecided)" if args.no_cache else
+                    "fp32 cache of %d positions built once before timing" % span),
+    }
 
 
 def valid_fraction(pack) -> float:
@@ -635,25 +683,7 @@ def run_ours(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "strong" if cp > 1 else "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
         "data": "synthetic",
-        "config": {
-            "workload": w.name, "total_tokens": T, "valid_tokens": pack.valid_tokens,
-            "n_seqs": pack.n_seqs, "max_seq_len": max(pack.lengths), "n_q_heads": w.n_q_heads,
-            "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "theta": w.theta,
-            "layout": {"packed": "packed [T, H, d] bf16, in place",
-                       "padded": "padded batch [B*pad_to, H, d] bf16, every row rotated, in place",
-                       "padded-seq-used": "padded batch [B*pad_to, H, d] bf16, pad rows skipped (seq_used)"
-                       }[args.layout],
-            "valid_fraction": valid_fraction(pack),
-            "parallelism": ("cp%d (rank %d of a load-balanced context-parallel group%s)"
-                            % (cp, cp_rank, "" if world > 1 else ", emulated on one GPU")
-                            if cp > 1 else "dp%d (independent packs)" % world),
-            "l2": "no flush: Q, K, dQ, dK = %.2f GB per step > 129 MB L2" % (bytes_per_pass / 1e9),
-            "cp_shards": None if cp <= 1 else {"token_start_rows": shards, "segments": segs,
-                                               "rank_tokens": rank_tokens},
-            "cos_sin": ("evaluated per tile, no cache (binary32 double-float; binary64 where the rounding "
-                        "is undecided)" if cache is None else
-                        "fp32 cache of %d positions built once before timing" % span),
-        },
+        "config": rope_config(args, w, pack, world, cp_rank, shards, segs, rank_tokens),
         "hbm_gbs": 2 * bytes_per_pass / (ms_per_step / 1e3) / 1e9,
         "hbm_frac_of_measured": 2 * bytes_per_pass / (ms_per_step / 1e3) / 1e9 / peak,
         "hbm_frac_of_nominal_8tbs": 2 * bytes_per_pass / (ms_per_step / 1e3) / 1e9 / NOMINAL_HBM_GBS,

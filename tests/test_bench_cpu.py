@@ -121,3 +121,9 @@ def test_reference_arm_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["config"]["workload"] == "tiny-pack-4x"
+    # the config is the one our arm prints for the same arguments (same keys, same values)
+    assert set(d["config"]) == {"workload", "total_tokens", "valid_tokens", "n_seqs", "max_seq_len", "n_q_heads",
+                                "n_kv_heads", "head_dim", "theta", "layout", "valid_fraction", "parallelism",
+                                "l2", "cp_shards", "cos_sin"}
+    assert d["config"]["parallelism"] == "dp1 (independent packs)" and d["config"]["cp_shards"] is None
+    assert 1 <= d["reference_tokens_per_step"] <= 4096

@@ -54,6 +54,9 @@ def test_rope_bench_line_small():
     assert d["roofline"]["kernel"] == "rope_qk_tile_kernel<128,false,2>"    # 8,192 tiles: 2 units per thread
     assert d["roofline"]["grid"]["ctas"] * d["roofline"]["grid"]["tile_tokens"] >= 16384
     assert d["e2e"]["h2d_bytes_per_step"] == d["e2e"]["d2h_bytes_per_step"] > 0
+    ref = _bench("--impl", "reference", "--workload", "2", "--steps", "3", "--warmup", "1",
+                 "--reference-seconds", "1")
+    assert ref["config"] == d["config"]                # both arms describe one workload
 
 
 @pytest.mark.parametrize("layout", ["padded", "padded-seq-used"])
@@ -79,6 +82,9 @@ def test_rope_bench_cp_rank():
     assert d["parity"]["bit_mismatch"] == 0 and d["parity"]["elements"] > 0
     assert d["roofline"]["algorithmic_bytes_per_launch"] == 4 * 40 * 128 * 8192
     assert abs(d["value"] - 8192 / (d["ms_per_step"] / 1e3)) < 1e-6 * d["value"]
+    ref = _bench("--impl", "reference", "--workload", "2", "--cp-size", "2", "--cp-rank", "1", "--steps", "3",
+                 "--warmup", "1", "--reference-seconds", "1")
+    assert ref["config"] == d["config"]
 
 
 def test_rope_head_shapes():

@@ -6,7 +6,8 @@ dQ and dK of one packed batch, in place, through the C ABI of librope_qk.so.  Th
 default workload is the Qwen3-32B attention shape: 65,536 tokens packed from
 50% U[16,256] / 50% U[1024,4096] samples, Q 64 heads, K 8 heads, head_dim 128,
 theta 1e6.  The four tensors hold 2.4 GB, far more than the 129 MB L2, so no flush
-is needed between steps.  The cos/sin cache is built once before timing, as a model
+is needed between steps (a smaller workload's steps cycle through copies of its
+tensors, at least 4 x L2 bytes per cycle).  The cos/sin cache is built once before timing, as a model
 builds its rotary cache once for all layers and steps.
 
     python bench.py [--gpus N --steps K --warmup W] [--impl reference]
@@ -57,6 +58,49 @@ if ROOT not in sys.path:
 METRIC = "QK-RoPE fwd+bwd tokens/s and HBM GB/s (% of GB300 peak), packed varlen"
 UNIT = "tokens/s"
 NOMINAL_HBM_GBS = 8000.0
+L2_BYTES = 129 * 10**6          # GB300 L2
+MAX_BUFFER_SETS = 64
+
+
+def buffer_sets(step_bytes: int) -> int:
+    """Copies of a step's tensors the timed loop cycles through, so that a launch finds
+    none of its inputs in L2: enough that one cycle touches at least 4x the L2 (one set
+    when a step alone does), at most MAX_BUFFER_SETS."""
+    if step_bytes <= 0:
+        return 1
+    return int(max(1, min(MAX_BUFFER_SETS, -(-4 * L2_BYTES // step_bytes))))
+
+
+def size_matched_copy(torch, dev, traffic: int, sets: int, launches: int) -> dict:
+    """torch's copy_ moving one launch's bytes (half read, half written) back to back,
+    cycling `sets` source/destination pairs as the timed loop cycles its tensors: what
+    a plain device copy of the same size reaches, the ramp-up and drain of a short launch
+    included.  Reported beside the roofline, whose peak is the long copy's rate."""
+    n = max(1, traffic // 4)
+    bufs = [(torch.zeros(n, dtype=torch.bfloat16, device=dev), torch.empty(n, dtype=torch.bfloat16, device=dev))
+            for _ in range(sets)]
+    for i in range(3 * sets):
+        bufs[i % sets][1].copy_(bufs[i % sets][0])
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for i in range(launches):
+        bufs[i % sets][1].copy_(bufs[i % sets][0])
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / launches
+    del bufs
+    torch.cuda.empty_cache()
+    return {"us_per_copy": us, "gbs": traffic / us / 1e3, "bytes": traffic, "copies": launches}
+
+
+def l2_note(step_bytes: int, sets: int) -> str:
+    """The config's statement of how the timed loop keeps L2 from serving its inputs."""
+    if sets == 1:
+        return "no flush: Q, K, dQ, dK = %.2f GB per step > 4 x 129 MB L2" % (step_bytes / 1e9)
+    cycle = sets * step_bytes
+    return ("no flush: steps cycle through %d copies of Q, K, dQ, dK (%.3f GB each, %.2f GB per cycle %s 4 x "
+            "129 MB L2)" % (sets, step_bytes / 1e9, cycle / 1e9, ">=" if cycle >= 4 * L2_BYTES else "<"))
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCE = os.path.join(ROOT, "packed_varlen_rope_gb300", "csrc", "rope_qk.cu")
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "rope_qk_tile_kernel_%s.md")   # per workload name
@@ -397,7 +441,7 @@ def rope_config(args, w, pack, world, cp_rank=0, shards=None, segs=None, rank_to
         "parallelism": ("cp%d (rank %d of a load-balanced context-parallel group%s)"
                         % (cp, cp_rank, "" if world > 1 else ", emulated on one GPU")
                         if cp > 1 else "dp%d (independent packs)" % world),
-        "l2": "no flush: Q, K, dQ, dK = %.2f GB per step > 129 MB L2" % (bytes_per_pass / 1e9),
+        "l2": l2_note(bytes_per_pass, buffer_sets(bytes_per_pass)),
         "cp_shards": None if cp <= 1 else {"token_start_rows": shards, "segments": segs,
                                            "rank_tokens": rank_tokens},
         "cos_sin": ("evaluated per tile, no cache (binary32 double-float; binary64 where the rounding "
@@ -605,14 +649,17 @@ def run_ours(args, rank, world, local):
     launch = pr.rope_qk_launch_info(q, k, w.theta, cu_seqlens=cu, cos_sin_cache=cache, seq_used=used,
                                     segments=segs)
 
-    def step():
-        fwd(q, k)
-        bwd(dq, dk)
+    # a small pack's tensors could stay in L2 from one step to the next: the steps cycle
+    # through enough copies that a launch's inputs were last touched 4 x L2 bytes ago
+    n_sets = buffer_sets(bytes_per_pass)
+    sets = [(q, k, dq, dk)] + [tuple(t.clone() for t in (q, k, dq, dk)) for _ in range(n_sets - 1)]
 
     sampler = ClockSampler(physical_gpu_index(local))
     sampler.start()
-    for _ in range(max(3, args.warmup)):
-        step()
+    for i in range(max(3, args.warmup)):
+        sq, sk, sdq, sdk = sets[i % n_sets]
+        fwd(sq, sk)
+        bwd(sdq, sdk)
     torch.cuda.synchronize()
 
     # Only the two events around the region: an event recorded between two launches
@@ -626,9 +673,10 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     t_wall0 = time.time()
     start.record(stream)
-    for _ in range(K):
-        fwd(q, k)
-        bwd(dq, dk)
+    for i in range(K):
+        sq, sk, sdq, sdk = sets[i % n_sets]
+        fwd(sq, sk)
+        bwd(sdq, sdk)
     end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -636,6 +684,7 @@ def run_ours(args, rank, world, local):
     t_wall1 = time.time()
     sampler.stop()
     total_ms = start.elapsed_time(end)
+    del sets
     avg_launch_s = total_ms / (2 * K) / 1e3          # this rank's mean time per launch
     total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / K
@@ -648,6 +697,10 @@ def run_ours(args, rank, world, local):
     achieved = bytes_per_pass / avg_launch_s / 1e9
     peak, peak_kind = measured_peak()
     clocks = sampler.summary(t_wall0, t_wall1)
+
+    copy_ref = size_matched_copy(torch, dev, bytes_per_pass, n_sets, 2 * K)
+    copy_ref["frac_of_measured"] = copy_ref["gbs"] / peak
+    copy_ref["launch_time_over_copy_time"] = avg_launch_s * 1e6 / copy_ref["us_per_copy"]
 
     e2e = None
     if not args.no_e2e:
@@ -694,6 +747,7 @@ def run_ours(args, rank, world, local):
                      "grid": {"ctas": launch.grid, "threads": launch.threads, "tile_tokens": launch.tile_tokens},
                      "algorithmic_bytes_per_launch": bytes_per_pass,
                      "avg_launch_us": avg_launch_s * 1e6, "peak_kind": peak_kind + " (hbm_gbs)"},
+        "size_matched_copy": copy_ref,
         "clocks": clocks,
         "gpu_launches": 2 * K,
     }
@@ -906,6 +960,10 @@ def run_rope_forms(args, rank, world, local):
     peak, peak_kind = measured_peak()
     bits = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)  # noqa: E731
 
+    # read before every timed replay, so that no form finds its tensors in L2 (a read
+    # leaves clean lines: no write-back lands in the timed replay)
+    flush = torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
     def timed(fn, reps=50):
         # each form captured once in a CUDA graph and replayed, so that groups of short
         # launches (the shard forms) are timed without the host's launch gaps
@@ -923,6 +981,7 @@ def run_rope_forms(args, rank, world, local):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
         torch.cuda.synchronize()
         for a, b in ev:
+            flush.sum()
             a.record()
             graph.replay()
             b.record()

@@ -525,15 +525,21 @@ int check_scale(double scale)
     return ROPE_OK;
 }
 
-// Tokens per tile: about kTileUnits 16-byte pair units (two batches of 2 units per
-// thread), capped by the one-warp position search.  Half that (one batch per thread, so
-// 1-token tiles on 40 heads of 128) measured 1.5 % faster with a cos/sin cache on 16,384
-// tokens but 12 % slower without one and 16 % slower on a padded batch under seq_used,
-// where each tile's position search and cos/sin staging serve half as many tokens.
-int pick_tile_tokens(int h_tot, int head_dim)
+// Pair units per tile for a launch of fewer than kWideGrid such tiles whose cos/sin rows
+// are read from a cache and whose rows all have work (no seq_used): half of kTileUnits.
+constexpr int kTileUnitsCached = kTileUnits / 2;
+
+// Tokens per tile: about `target` 16-byte pair units, capped by the one-warp position
+// search.  kTileUnits (two batches of 2 units per thread) by default.  Half that gives
+// 1-token tiles on 40 heads of 128 and a shorter drain at the launch's end: 1.5 % faster
+// on 16,384 tokens and 1-2 % on a context-parallel rank's half of it with a cos/sin
+// cache, but 2.6 % slower without one, 20 % slower on a padded batch under seq_used
+// (there each tile's position search and cos/sin staging serve half as many tokens),
+// and 6-16 % slower on launches of 100,000+ tokens with head_dim 64, 80 or 128, where
+// the per-tile prologue outweighs the drain.
+int pick_tile_tokens(int h_tot, int head_dim, int target)
 {
     const int units_per_token = h_tot * (head_dim / 16);
-    const int target = kTileUnits;
     int tt = (target + units_per_token - 1) / units_per_token;
     if (tt < 1) tt = 1;
     if (tt > kMaxTileTokens) tt = kMaxTileTokens;
@@ -813,7 +819,11 @@ int plan_rotation(const rope_qk_desc *dp, Launch *L, bool check_device)
     a.hkv = p.n_kv_heads;
     a.h_tot = p.n_q_heads + p.n_kv_heads;
     a.head_dim = p.head_dim;
-    a.tile_tokens = pick_tile_tokens(a.h_tot, p.head_dim);
+    a.tile_tokens = pick_tile_tokens(a.h_tot, p.head_dim, kTileUnits);
+    if (a.cache != nullptr && a.seq_used == nullptr) {
+        const int half = pick_tile_tokens(a.h_tot, p.head_dim, kTileUnitsCached);
+        if ((T + half - 1) / half < kWideGrid) a.tile_tokens = half;
+    }
     a.in_place = in_place ? 1 : 0;
     a.bwd = p.backward ? 1 : 0;
     a.div_htot = make_fastdiv(static_cast<uint32_t>(a.h_tot));

@@ -51,6 +51,24 @@ def test_cp_value_is_strong_scaling():
     assert bench.cp_tokens_per_s(1, 65536, 32768, 0.5) == 32768 / 0.5e-3
 
 
+def test_buffer_sets_keep_small_packs_out_of_l2():
+    """A step whose tensors touch less than 4 x L2 cycles through copies until one cycle
+    does (capped); the workload-4 step needs no copy, and the config says which."""
+    assert bench.buffer_sets(2_415_919_104) == 1
+    assert bench.buffer_sets(335_544_320) == 2                     # workload 2
+    assert bench.buffer_sets(157_982_720) == 4                     # workload 3 packed
+    assert bench.buffer_sets(78_991_360) == 7                      # a cp = 2 rank of workload 3
+    for b in (1, 98_304, 10**6, 78_991_360, 157_982_720, 335_544_320):
+        n = bench.buffer_sets(b)
+        assert 1 <= n <= bench.MAX_BUFFER_SETS
+        assert n * b >= 4 * bench.L2_BYTES or n == bench.MAX_BUFFER_SETS
+        assert n == 1 or (n - 1) * b < 4 * bench.L2_BYTES         # no more copies than needed
+    assert bench.buffer_sets(98_304) == bench.MAX_BUFFER_SETS      # the tiny pack: capped
+    assert "> 4 x 129 MB L2" in bench.l2_note(2_415_919_104, 1)
+    assert "7 copies" in bench.l2_note(78_991_360, 7) and ">= 4 x" in bench.l2_note(78_991_360, 7)
+    assert "< 4 x" in bench.l2_note(98_304, bench.MAX_BUFFER_SETS)
+
+
 def test_all_core_oracle_timing_runs_every_range():
     """The all-core CPU figure splits the token sample into one range per core and
     rotates all of it (tiny workload, short repeat window)."""

@@ -255,9 +255,10 @@ int rope_qk_apply(const rope_qk_desc *desc, void *stream);
  * CUDA call: the rotation kernel's compile-time instance (head_dim 64, 96, 128 or 256,
  * or 0 for the generic one), whether it uses 64-bit element offsets (some view spans
  * 2^31 elements or more; unsloth.ai page, section "Indexage int64 pour les kernels
- * Triton"), how many 16-byte pair units each thread keeps in flight (2, or 4 for
- * launches of at least 32,768 tiles with 32-bit offsets, a compile-time head_dim and a
- * cos/sin cache), and its grid: one CTA
+ * Triton"), how many 16-byte pair units each thread keeps in flight (4 for launches of
+ * at least 32,768 tiles with 32-bit offsets, a compile-time head_dim and a cos/sin
+ * cache; 3 for smaller such launches without seq_used whose tile holds at most 384
+ * units; 2 otherwise), and its grid: one CTA
  * of `threads` threads per tile of `tile_tokens` consecutive tokens.  Returns the
  * status rope_qk_apply's argument checks give (the cache's device is not checked);
  * grid == 0 when there is nothing to launch.

@@ -487,14 +487,17 @@ def test_launch_info_names_the_dispatched_instance(lib):
     assert info(32768, 64, 8, 128, cos_sin_cache=ctypes.pointer(cache)).unroll == 4   # exactly 32,768 tiles
     assert info(32767, 64, 8, 128, cos_sin_cache=ctypes.pointer(cache)).unroll == 2
     w2 = info(16384, 32, 8, 128, cos_sin_cache=ctypes.pointer(cache))
-    assert (w2.unroll, w2.tile_tokens, w2.grid) == (2, 1, 16384)        # 320 units a token, 256 a tile
+    assert (w2.unroll, w2.tile_tokens, w2.grid) == (3, 1, 16384)        # 320 units a token, 256 a tile
+    assert w2.kernel_name() == "rope_qk_tile_kernel<128,false,3>"       # the tile in one batch of 3
     # ... as long as the launch stays below 32,768 such tiles; a larger one keeps 512 a tile
     assert info(32767, 32, 8, 128, cos_sin_cache=ctypes.pointer(cache)).tile_tokens == 1
     big = info(32768, 32, 8, 128, cos_sin_cache=ctypes.pointer(cache))
     assert (big.tile_tokens, big.grid, big.unroll) == (2, 16384, 2)
     # without a cache, or with seq_used, a tile holds about 512 units: 2 tokens of 320
     assert info(16384, 32, 8, 128).tile_tokens == 2
-    assert info(16384, 32, 8, 128, cos_sin_cache=ctypes.pointer(cache), seq_used=1 << 46).tile_tokens == 2
+    su = info(16384, 32, 8, 128, cos_sin_cache=ctypes.pointer(cache), seq_used=1 << 46)
+    assert (su.tile_tokens, su.unroll) == (2, 2)
+    assert info(16384, 32, 8, 128).unroll == 2                                  # no cache
     assert info(16384, 4, 2, 64, cos_sin_cache=ctypes.pointer(cache_desc(lib, rows=64, d=64, theta=1e6,
                                                                           data=CACHE))).tile_tokens == 11
     w5 = info(1 << 20, 32, 8, 128)

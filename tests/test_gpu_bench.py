@@ -51,7 +51,7 @@ def test_rope_bench_line_small():
                 "cpu_baseline", "cpu_baseline_all_cores", "e2e", "clocks", "gpu_launches", "parity"):
         assert key in d, key
     assert d["parity"]["bit_mismatch"] == 0 and d["gpu_launches"] == 40
-    assert d["roofline"]["kernel"] == "rope_qk_tile_kernel<128,false,2>"    # 16,384 1-token tiles: 2 units per thread
+    assert d["roofline"]["kernel"] == "rope_qk_tile_kernel<128,false,3>"    # 16,384 1-token tiles, one batch of 3
     assert d["roofline"]["grid"]["ctas"] * d["roofline"]["grid"]["tile_tokens"] >= 16384
     assert d["e2e"]["h2d_bytes_per_step"] == d["e2e"]["d2h_bytes_per_step"] > 0
     assert d["size_matched_copy"]["bytes"] == d["roofline"]["algorithmic_bytes_per_launch"]

@@ -742,7 +742,10 @@ def run_ours(args, rank, world, local):
         "hbm_frac_of_nominal_8tbs": 2 * bytes_per_pass / (ms_per_step / 1e3) / 1e9 / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
-                     "traffic": profiled_traffic(w.name) if cache is not None and args.layout == "packed" else None,
+                     # the profiled launch is the whole packed pack with a cache: a CP
+                     # rank's launch (half the rows) or another layout has no capture
+                     "traffic": (profiled_traffic(w.name) if cache is not None and args.layout == "packed"
+                                 and cp == 1 else None),
                      "kernel": launch.kernel_name(),
                      "grid": {"ctas": launch.grid, "threads": launch.threads, "tile_tokens": launch.tile_tokens},
                      "algorithmic_bytes_per_launch": bytes_per_pass,

@@ -493,10 +493,10 @@ def test_launch_info_names_the_dispatched_instance(lib):
     assert info(32767, 32, 8, 128, cos_sin_cache=ctypes.pointer(cache)).tile_tokens == 1
     big = info(32768, 32, 8, 128, cos_sin_cache=ctypes.pointer(cache))
     assert (big.tile_tokens, big.grid, big.unroll) == (2, 16384, 2)
-    # without a cache, or with seq_used, a tile holds about 512 units: 2 tokens of 320
+    # without a cache a tile holds about 512 units (2 tokens of 320), under seq_used 1,024
     assert info(16384, 32, 8, 128).tile_tokens == 2
     su = info(16384, 32, 8, 128, cos_sin_cache=ctypes.pointer(cache), seq_used=1 << 46)
-    assert (su.tile_tokens, su.unroll) == (2, 2)
+    assert (su.tile_tokens, su.unroll, su.grid) == (4, 2, 4096)                # seq_used: about 1,024 units
     assert info(16384, 32, 8, 128).unroll == 2                                  # no cache
     assert info(16384, 4, 2, 64, cos_sin_cache=ctypes.pointer(cache_desc(lib, rows=64, d=64, theta=1e6,
                                                                           data=CACHE))).tile_tokens == 11

@@ -55,26 +55,29 @@ def _autograd_function():
 
         @staticmethod
         def forward(ctx, q, k, theta, cu_seqlens, position_ids, token_offset, position_scale, cos_sin_cache,
-                    segments):
+                    segments, seq_used):
             rope_qk_apply(q, k, theta, cu_seqlens=cu_seqlens, position_ids=position_ids,
                           token_offset=token_offset, position_scale=position_scale, cos_sin_cache=cos_sin_cache,
-                          segments=segments)
+                          segments=segments, seq_used=seq_used)
             ctx.mark_dirty(q, k)
-            ctx.save_for_backward(cu_seqlens, position_ids)
+            ctx.save_for_backward(cu_seqlens, position_ids, seq_used)
             ctx.args = (theta, token_offset, position_scale, cos_sin_cache, segments)
             return q, k
 
         @staticmethod
         def backward(ctx, dq, dk):
-            cu_seqlens, position_ids = ctx.saved_tensors
+            cu_seqlens, position_ids, seq_used = ctx.saved_tensors
             theta, token_offset, position_scale, cache, segments = ctx.args
             dq, dk = dq.contiguous(), dk.contiguous()      # e.g. broadcast (stride 0) gradients
             dq_out = torch.empty(dq.shape, dtype=dq.dtype, device=dq.device)
             dk_out = torch.empty(dk.shape, dtype=dk.dtype, device=dk.device)
+            # rows the forward left as they were (pad rows under seq_used) pass their
+            # gradient through: out of place, the kernel copies them unchanged
             rope_qk_apply(dq, dk, theta, cu_seqlens=cu_seqlens, position_ids=position_ids, backward=True,
                           q_out=dq_out, k_out=dk_out, token_offset=token_offset,
-                          position_scale=position_scale, cos_sin_cache=cache, segments=segments)
-            return dq_out, dk_out, None, None, None, None, None, None, None
+                          position_scale=position_scale, cos_sin_cache=cache, segments=segments,
+                          seq_used=seq_used)
+            return dq_out, dk_out, None, None, None, None, None, None, None, None
 
     return RopeQK
 
@@ -83,16 +86,19 @@ _RopeQK = None
 
 
 def apply_rope_qk(q, k, cu_seqlens, theta: float, cos_sin_cache=None, position_ids=None, token_offset: int = 0,
-                  position_scale: float = 1.0, segments=None):
+                  position_scale: float = 1.0, segments=None, seq_used=None):
     """Differentiable in-place RoPE of packed q [T, Hq, d] and k [T, Hkv, d] (any
     token/head strides).  Positions from ``position_ids`` if given, else from
-    ``cu_seqlens`` (row r is token ``token_offset + r``, or as ``segments`` map it)."""
+    ``cu_seqlens`` (row r is token ``token_offset + r``, or as ``segments`` map it);
+    with ``seq_used`` (int32 [n_seqs]) only the first seq_used[s] rows of sample s are
+    rotated and the rest (a padded batch's pad rows) are left as they are, in the
+    forward and in the gradient."""
     global _RopeQK
     if _RopeQK is None:
         _RopeQK = _autograd_function()
     segs = None if segments is None else tuple((int(a), int(b)) for a, b in segments)
     return _RopeQK.apply(q, k, theta, cu_seqlens, position_ids, int(token_offset), float(position_scale),
-                         cos_sin_cache, segs)
+                         cos_sin_cache, segs, seq_used)
 
 
 def cache_rows_for(needed: int, current: int) -> int:
@@ -141,12 +147,13 @@ class RotaryEmbedding:
         return cur
 
     def __call__(self, q, k, cu_seqlens=None, position_ids=None, token_offset: int = 0,
-                 max_position: int = 0, segments=None):
+                 max_position: int = 0, segments=None, seq_used=None):
         """Rotate q and k in place (differentiable).  ``max_position``: an upper bound on
         the position ids, for ids that exceed the row count (a context-parallel shard
         of a long sequence carrying global ids); without it the cache covers ``T``
         rows and larger ids are evaluated on the fly.  ``segments``: a context-parallel
-        rank's (row_start, token_start) list (``shard_segments``)."""
+        rank's (row_start, token_start) list (``shard_segments``).  ``seq_used``: the
+        tokens used per sample of a padded batch (pad rows left as they are)."""
         if q.shape[-1] != self.head_dim:
             raise ValueError("q and k must have head_dim %d" % self.head_dim)
         T = q.shape[0]
@@ -161,4 +168,5 @@ class RotaryEmbedding:
         rows = max(rows, int(max_position) + 1 if max_position else 0)
         cache = self.cache(q.device, max(rows, 1)) if self.use_cache else None
         return apply_rope_qk(q, k, cu_seqlens, self.theta, cos_sin_cache=cache, position_ids=position_ids,
-                             token_offset=token_offset, position_scale=self.position_scale, segments=segments)
+                             token_offset=token_offset, position_scale=self.position_scale, segments=segments,
+                             seq_used=seq_used)

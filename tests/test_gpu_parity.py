@@ -595,6 +595,35 @@ def test_rotary_embedding_cp_segments_autograd(dev):
     assert rope.cache(dev, 1).rows >= int(rows.max()) + 1
 
 
+@pytest.mark.parametrize("use_cache", [True, False])
+def test_rotary_embedding_seq_used_autograd(dev, use_cache):
+    """RotaryEmbedding on the padded Llama-3-8B batch (8 x 2048 rows, 47 % valid) with
+    seq_used: the forward rotates each sample's first seq_used[s] rows as the oracle does
+    and leaves the pad rows' bits as they were; the autograd backward gives the oracle's
+    transpose rotation on those rows and passes the pad rows' gradient through."""
+    from packed_varlen_rope_gb300 import RotaryEmbedding
+
+    w, pack, q, k, dq, dk = _workload_inputs(3, "padded")
+    T = pack.total_tokens
+    cu_dev = torch.from_numpy(pack.cu_seqlens).to(dev)
+    used = torch.tensor(pack.lengths, dtype=torch.int32, device=dev)
+    pos = oracle.positions(pack.cu_seqlens, T)
+    sample = np.searchsorted(pack.cu_seqlens, np.arange(T), side="right") - 1
+    valid = pos < np.asarray(pack.lengths)[sample]
+    assert 0.4 < valid.mean() < 0.6
+    rope = RotaryEmbedding(w.head_dim, w.theta, use_cache=use_cache)
+    qleaf = torch.zeros_like(q, requires_grad=True)
+    kleaf = torch.zeros_like(k, requires_grad=True)
+    yq, yk = rope(qleaf + q, kleaf + k, cu_seqlens=cu_dev, seq_used=used)
+    torch.autograd.backward([yq, yk], [dq, dk])
+    for y, x, g, grad in ((yq, q, dq, qleaf.grad), (yk, k, dk, kleaf.grad)):
+        xb, gb = to_bits(x), to_bits(g)
+        yb, db = to_bits(y), to_bits(grad)
+        assert np.array_equal(yb[valid], oracle.rope_rows(xb[valid], pos[valid], w.theta))
+        assert np.array_equal(db[valid], oracle.rope_rows(gb[valid], pos[valid], w.theta, bwd=True))
+        assert np.array_equal(yb[~valid], xb[~valid]) and np.array_equal(db[~valid], gb[~valid])
+
+
 def test_rotary_embedding_without_cache(dev):
     """RotaryEmbedding(use_cache=False) builds no table and gives the bits of the cached
     module, forward and autograd backward."""

@@ -101,6 +101,43 @@ def apply_rope_qk(q, k, cu_seqlens, theta: float, cos_sin_cache=None, position_i
                          cos_sin_cache, segs, seq_used)
 
 
+def _glu_function():
+    import torch
+
+    class GLU(torch.autograd.Function):
+        """Autograd wrapper of the gated MLP activation: forward h = act(e) * g into a new
+        tensor (e and g saved); backward (de, dg) from the library's backward kernel."""
+
+        @staticmethod
+        def forward(ctx, kind, e, g):
+            ctx.kind = kind
+            ctx.save_for_backward(e, g)
+            return glu_fwd(kind, e, g)
+
+        @staticmethod
+        def backward(ctx, dh):
+            e, g = ctx.saved_tensors
+            de, dg = glu_bwd(ctx.kind, dh.contiguous(), e, g)
+            return None, de, dg
+
+    return GLU
+
+
+_GLU = None
+
+
+def apply_glu(kind: str, e, g):
+    """Differentiable h = act(e) * g for bf16 CUDA [rows, cols] views with contiguous rows
+    (e.g. the gate and up halves of one fused projection output): ``kind`` "swiglu"
+    (SiLU), "geglu" (GELU, erf form) or "geglu_tanh" (GELU, tanh form)."""
+    global _GLU
+    if kind not in GLU_KINDS:
+        raise ValueError("kind must be one of %s" % sorted(GLU_KINDS))
+    if _GLU is None:
+        _GLU = _glu_function()
+    return _GLU.apply(kind, e, g)
+
+
 def cache_rows_for(needed: int, current: int) -> int:
     """Rows a growing cos/sin cache is built with: ``current`` if it covers ``needed``,
     else the next power of two >= needed (at least 1024), so that a run of growing packs

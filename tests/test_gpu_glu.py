@@ -132,6 +132,28 @@ def test_glu_fused_gate_up_and_in_place(dev, kind):
     _fwd_bwd_check(kind, eb, gb, dhb, g2, None, None, (kind, "h over g"))
 
 
+@pytest.mark.parametrize("kind", KINDS)
+def test_glu_autograd_on_fused_projection(dev, kind):
+    """apply_glu on the gate and up halves of one [rows, 2I] projection output: h and the
+    gradients autograd gives the projection are the oracle's (within the bar), each
+    half's gradient landing in its own columns."""
+    rng = np.random.Generator(np.random.PCG64(11))
+    rows, inter = 257, 1024
+    xb = _bits(rng, (rows, 2 * inter), 1.5)
+    dhb = _bits(rng, (rows, inter))
+    eb, gb = xb[:, :inter].copy(), xb[:, inter:].copy()
+    x = from_bits(xb, dev).requires_grad_(True)
+    h = pr().apply_glu(kind, x[:, :inter], x[:, inter:])
+    h.backward(from_bits(dhb, dev))
+    torch.cuda.synchronize()
+    grad = to_bits(x.grad)
+    de = torch.from_numpy(grad[:, :inter].copy().view(np.int16)).view(torch.bfloat16)
+    dg = torch.from_numpy(grad[:, inter:].copy().view(np.int16)).view(torch.bfloat16)
+    _fwd_bwd_check(kind, eb, gb, dhb, h, de, dg, (kind, "autograd"))
+    with pytest.raises(ValueError):
+        pr().apply_glu("relu", x[:, :inter], x[:, inter:])
+
+
 def test_glu_special_values(dev):
     # includes the far left tails where sigmoid, Phi or sigmoid(2u) are tiny but the
     # products are still normal bf16 numbers (-87.5 ... -95 for SiLU, about -10 for the

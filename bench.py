@@ -568,12 +568,14 @@ def run_ours(args, rank, world, local):
     import packed_varlen_rope_gb300 as pr
     from packed_varlen_rope_gb300 import workloads as wl
 
+    # the rank's GPU is made current before the process group exists, so that NCCL's
+    # communicator and every barrier use it
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
     if world > 1:
         import torch.distributed as dist
 
         dist.init_process_group("nccl")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
     w = wl.WORKLOADS[args.workload]
     if args.layout != "packed" and w.padded_samples is None:
         print("--layout %s needs a workload with padded samples (3)" % args.layout, file=sys.stderr)
@@ -849,12 +851,14 @@ def run_glu(args, rank, world, local):
     import packed_varlen_rope_gb300 as pr
     from packed_varlen_rope_gb300 import workloads as wl
 
+    # the rank's GPU is made current before the process group exists, so that NCCL's
+    # communicator and every barrier use it
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
     if world > 1:
         import torch.distributed as dist
 
         dist.init_process_group("nccl")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
     w = wl.GLU_WORKLOADS[args.glu_workload]
     if args.glu_kind is not None:
         w = wl.GluWorkload(w.name, w.rows, w.cols, args.glu_kind, w.description)

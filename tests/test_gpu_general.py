@@ -370,3 +370,45 @@ def test_seq_used_skips_padding(dev):
     pr().rope_qk_fwd(qp, kp, torch.from_numpy(packed.cu_seqlens).to(dev), w.theta)
     torch.cuda.synchronize()
     assert np.array_equal(to_bits(qp), to_bits(q)[valid])
+
+
+@pytest.mark.parametrize("T,hq,hkv,d,cached,used,kernel,tile", [
+    (32767, 32, 8, 128, True, False, "rope_qk_tile_kernel<128,false,3>", 1),    # short: 1-token tiles, 3 units
+    (32768, 32, 8, 128, True, False, "rope_qk_tile_kernel<128,false,2>", 2),    # 2-token tiles, 2 units
+    (32767, 64, 8, 128, True, False, "rope_qk_tile_kernel<128,false,2>", 1),    # 576 units: one batch of 3 won't hold
+    (32768, 64, 8, 128, True, False, "rope_qk_tile_kernel<128,false,4>", 1),    # wide: 4 units
+    (9001, 32, 8, 128, False, False, "rope_qk_tile_kernel<128,false,2>", 2),    # no cache
+    (9001, 32, 8, 128, True, True, "rope_qk_tile_kernel<128,false,2>", 4),      # seq_used: 4-token tiles
+    (5003, 4, 2, 64, True, False, "rope_qk_tile_kernel<64,false,3>", 11),       # small heads: 11-token tiles
+    (5003, 6, 2, 80, True, False, "rope_qk_tile_kernel<0,false,2>", 7),         # generic head_dim
+])
+def test_dispatch_boundaries(dev, T, hq, hkv, d, cached, used, kernel, tile):
+    """Each tile size and unroll the launch plan picks, at and just below the 32,768-tile
+    edge and on ragged tails, forward and backward: every row equals the oracle (rows
+    past a sample's seq_used, and past the pack's end, left as they were)."""
+    rng = np.random.Generator(np.random.PCG64(T * 131 + hq * 7 + d))
+    lengths = list(rng.integers(1, 3000, size=64))
+    while sum(lengths) < T:
+        lengths += list(rng.integers(1, 3000, size=64))
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    n = int(np.searchsorted(cu, T - 3))          # the last sample ends 3 rows before T:
+    cu = np.concatenate([cu[:n], [T - 3]]).astype(np.int32)   # rows past the pack stay as they are
+    seq_used = None
+    pos = oracle.positions(cu, T)
+    if used:
+        lens = np.diff(cu)
+        use = np.floor(rng.random(lens.size) * (lens + 1)).astype(np.int32)    # uniform in [0, len]
+        seq_used = torch.from_numpy(use).to(dev)
+        sample = np.clip(np.searchsorted(cu, np.arange(T), side="right") - 1, 0, lens.size - 1)
+        pos = np.where((pos >= 0) & (pos < use[sample]), pos, -1).astype(np.int32)
+    cu_dev = torch.from_numpy(cu).to(dev)
+    cache = pr().new_cos_sin_cache(int(np.diff(cu).max()), d, 1.0e6, device=dev) if cached else None
+    qb, kb = _bits(rng, (T, hq, d)), _bits(rng, (T, hkv, d))
+    for bwd in (False, True):
+        q, k = from_bits(qb, dev), from_bits(kb, dev)
+        info = pr().rope_qk_launch_info(q, k, 1.0e6, cu_seqlens=cu_dev, cos_sin_cache=cache, seq_used=seq_used)
+        assert (info.kernel_name(), info.tile_tokens) == (kernel, tile)
+        pr().rope_qk_apply(q, k, 1.0e6, cu_seqlens=cu_dev, cos_sin_cache=cache, seq_used=seq_used, backward=bwd)
+        torch.cuda.synchronize()
+        _check(to_bits(q), _expect(qb, pos, 1.0e6, bwd=bwd), qb, (kernel, "q", bwd))
+        _check(to_bits(k), _expect(kb, pos, 1.0e6, bwd=bwd), kb, (kernel, "k", bwd))

@@ -644,6 +644,9 @@ def run_ours(args, rank, world, local):
         # check after the timed regions (the host copies are taken only then: freshly
         # written pageable host memory next to the e2e leg stalled its enqueueing thread)
         pristine = [t.clone() for t in (q, k, dq, dk)]
+    # the e2e leg's pinned host inputs and outputs, allocated and filled here, well before
+    # that leg runs, and with no pageable staging copy
+    e2e_bufs = None if args.no_e2e else pinned_buffers(q, k, dq, dk)
 
     rows_moved = T if args.layout == "padded" else rank_tokens     # rows one launch reads and writes
     bytes_per_pass = 4 * (w.n_q_heads + w.n_kv_heads) * w.head_dim * rows_moved
@@ -706,8 +709,9 @@ def run_ours(args, rank, world, local):
 
     e2e = None
     if not args.no_e2e:
-        e2e = end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev, used, segs,
+        e2e = end_to_end(args, pr, w, pack, e2e_bufs, cu, cache, stream, world, dev, used, segs,
                          pack.valid_tokens if cp > 1 and world > 1 else rank_tokens, scale_world=cp == 1)
+        del e2e_bufs
 
     cpu = parity = None
     if do_cpu:
@@ -768,18 +772,30 @@ def run_ours(args, rank, world, local):
     return 0
 
 
-def end_to_end(args, pr, w, pack, q, k, dq, dk, cu, cache, stream, world, dev, used=None, segs=None,
-               tokens=None, scale_world=True):
-    """Same metric through the public host-buffer call (rope_qk_host) with the inputs in
-    pinned host memory: every step streams Q, K (forward) and dQ, dK (backward) from the
-    host through a device workspace in chunks and back, copies overlapped with the
-    rotation; the results are complete in host memory when the step's stream ends."""
+def pinned_buffers(*tensors):
+    """(inputs, outputs): pinned host copies of device tensors and pinned host tensors of
+    the same shapes, each allocated pinned directly (no pageable staging copy)."""
     import torch
 
-    host = [t.to("cpu").pin_memory() for t in (q, k, dq, dk)]
-    work = [t.clone().pin_memory() for t in host]
+    host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in tensors]
+    for h, t in zip(host, tensors):
+        h.copy_(t)
+    work = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in tensors]
+    return host, work
+
+
+def end_to_end(args, pr, w, pack, bufs, cu, cache, stream, world, dev, used=None, segs=None,
+               tokens=None, scale_world=True):
+    """Same metric through the public host-buffer call (rope_qk_host) with the inputs in
+    pinned host memory (``bufs`` from ``pinned_buffers(q, k, dq, dk)``): every step
+    streams Q, K (forward) and dQ, dK (backward) from the host through a device
+    workspace in chunks and back, copies overlapped with the rotation; the results are
+    complete in host memory when the step's stream ends."""
+    import torch
+
+    host, work = bufs
     per_token = (w.n_q_heads + w.n_kv_heads) * w.head_dim * 2
-    rows = q.shape[0]
+    rows = host[0].shape[0]
     tokens = pack.valid_tokens if tokens is None else tokens
     per_s = (lambda ms: whole_job_tokens_per_s(world, tokens, ms)) if scale_world else \
         (lambda ms: tokens / (ms / 1e3))  # noqa: E731

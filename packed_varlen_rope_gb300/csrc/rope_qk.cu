@@ -43,7 +43,8 @@ namespace {
 constexpr int kThreads = 128;           // threads per CTA (9 CTAs per SM at 56 registers)
 constexpr int kTileUnits = 512;         // about this many 16-byte pair units per tile
 constexpr int kWideGrid = 32768;        // tiles from which a launch with a cos/sin cache
-                                        // keeps 4 pair units in flight per thread, not 2
+                                        // keeps 4 pair units in flight per thread (below:
+                                        // 3 or 2), and keeps full-size tiles
 constexpr int kMaxHalf = 128;           // head_dim <= 256
 constexpr int kMaxTileTokens = 32;      // one warp resolves the tile's positions
 constexpr int kMaxSegments = ROPE_MAX_SEGMENTS;
@@ -534,14 +535,14 @@ constexpr int kTileUnitsCached = kTileUnits / 2;
 constexpr int kTileUnitsSeqUsed = 2 * kTileUnits;
 
 // Tokens per tile: about `target` 16-byte pair units, capped by the one-warp position
-// search.  kTileUnits (two batches of 2 units per thread) by default, twice that under
-// seq_used.  Half that gives
-// 1-token tiles on 40 heads of 128 and a shorter drain at the launch's end: 1.5 % faster
-// on 16,384 tokens and 1-2 % on a context-parallel rank's half of it with a cos/sin
-// cache, but 2.6 % slower without one, 20 % slower on a padded batch under seq_used
-// (there each tile's position search and cos/sin staging serve half as many tokens),
-// and 6-16 % slower on launches of 100,000+ tokens with head_dim 64, 80 or 128, where
-// the per-tile prologue outweighs the drain.
+// search.  The targets: kTileUnits (two batches of 2 units per thread) by default,
+// twice that under seq_used, half of it for short cached launches.  Half gives 1-token
+// tiles on 40 heads of 128 and a shorter drain at the launch's end: 1.5 % faster on
+// 16,384 tokens and 1-2 % on a context-parallel rank's half of it with a cos/sin cache,
+// but 2.6 % slower without one, 20 % slower on a padded batch under seq_used (there
+// each tile's position search and cos/sin staging serve half as many tokens), and
+// 6-16 % slower on launches of 100,000+ tokens with head_dim 64, 80 or 128, where the
+// per-tile prologue outweighs the drain.
 int pick_tile_tokens(int h_tot, int head_dim, int target)
 {
     const int units_per_token = h_tot * (head_dim / 16);

@@ -4,7 +4,6 @@ Every mutant is built from a textual edit of ``oracle/rope_oracle.c`` in a tempo
 directory, on the CPU; the committed oracle is never modified.
 """
 import os
-import shutil
 
 import pytest
 

@@ -258,7 +258,8 @@ int rope_qk_apply(const rope_qk_desc *desc, void *stream);
  * Triton"), how many 16-byte pair units each thread keeps in flight (4 for launches of
  * at least 32,768 tiles with 32-bit offsets, a compile-time head_dim and a cos/sin
  * cache; 3 for smaller such launches without seq_used whose tile holds at most 384
- * units; 2 otherwise), and its grid: one CTA
+ * units, and for launches with 64-bit offsets, a compile-time head_dim and a cache but
+ * no seq_used; 2 otherwise), and its grid: one CTA
  * of `threads` threads per tile of `tile_tokens` consecutive tokens.  Returns the
  * status rope_qk_apply's argument checks give (the cache's device is not checked);
  * grid == 0 when there is nothing to launch.

@@ -849,14 +849,17 @@ int plan_rotation(const rope_qk_desc *dp, Launch *L, bool check_device)
     // their cos/sin from a cache (the tile's first batch then covers most of a wide
     // token's units before the position search); 3 for smaller such launches whose tile
     // fits in one batch of 3 (the whole tile then streams in one round trip: 1-token
-    // tiles on 40 heads of 128, 0.7-1.5 % faster than 2); 2 otherwise (more resident
-    // CTAs, a cheaper evaluation of cos/sin in the kernel, lighter 64-bit address
-    // arithmetic); the generic head_dim instance always 2.
-    const bool fast_path = a.cache != nullptr && !L->long_index && L->d_instance != 0;
+    // tiles on 40 heads of 128, 0.7-1.5 % faster than 2), and for launches with 64-bit
+    // offsets that read a cache (72 registers; 2^20 tokens on 40 heads of 128: 3,095
+    // against 3,121 us with 2, where 4 was slower); 2 otherwise (more resident CTAs, a
+    // cheaper evaluation of cos/sin in the kernel); the generic head_dim instance always 2.
+    const bool cached = a.cache != nullptr && L->d_instance != 0;
     const int tile_units = a.tile_tokens * a.h_tot * (p.head_dim / 16);
-    if (fast_path && L->grid >= kWideGrid)
+    if (cached && !L->long_index && L->grid >= kWideGrid)
         L->unroll = 4;
-    else if (fast_path && a.seq_used == nullptr && tile_units <= 3 * kThreads)
+    else if (cached && !L->long_index && a.seq_used == nullptr && tile_units <= 3 * kThreads)
+        L->unroll = 3;
+    else if (cached && L->long_index && a.seq_used == nullptr)
         L->unroll = 3;
     else
         L->unroll = 2;
@@ -873,7 +876,8 @@ int rope_qk_apply_impl(const rope_qk_desc *dp, void *stream, bool pdl)
     if (L.unroll == 4)
         err = dispatch_dim<false, 4>(L.a, L.grid, L.smem, s, pdl);
     else if (L.unroll == 3)
-        err = dispatch_dim<false, 3>(L.a, L.grid, L.smem, s, pdl);
+        err = L.long_index ? dispatch_dim<true, 3>(L.a, L.grid, L.smem, s, pdl)
+                           : dispatch_dim<false, 3>(L.a, L.grid, L.smem, s, pdl);
     else
         err = L.long_index ? dispatch_dim<true, 2>(L.a, L.grid, L.smem, s, pdl)
                            : dispatch_dim<false, 2>(L.a, L.grid, L.smem, s, pdl);

@@ -503,7 +503,7 @@ def test_launch_info_names_the_dispatched_instance(lib):
     w5 = info(1 << 20, 32, 8, 128)
     assert w5.kernel_name() == "rope_qk_tile_kernel<128,true,2>" and w5.grid == (1 << 20) // w5.tile_tokens
     assert info(1 << 20, 32, 8, 128, cos_sin_cache=ctypes.pointer(cache)).kernel_name() == \
-        "rope_qk_tile_kernel<128,true,2>"                                  # 64-bit offsets: 2
+        "rope_qk_tile_kernel<128,true,3>"                                  # 64-bit offsets, a cache: 3
     assert info(4096, 4, 2, 80).kernel_name() == "rope_qk_tile_kernel<0,false,2>"
     assert info(1 << 16, 64, 8, 80, cos_sin_cache=ctypes.pointer(cache_desc(lib, rows=64, d=80, theta=1e6,
                                                                               data=CACHE))).unroll == 2  # generic

@@ -259,6 +259,8 @@ def test_workload5_long_sampled(dev):
     k0 = to_bits(k[rows_dev])
     cu_dev = torch.from_numpy(pack.cu_seqlens).to(dev)
     cache = pr().new_cos_sin_cache(T, w.head_dim, w.theta, device=dev)
+    info = pr().rope_qk_launch_info(q, k, w.theta, cu_seqlens=cu_dev, cos_sin_cache=cache)
+    assert info.kernel_name() == "rope_qk_tile_kernel<128,true,3>"          # 64-bit offsets, a cache: 3 units
     _run("rope_qk_fwd", q, k, cu_dev, w.theta, cache)
     pos = oracle.positions(pack.cu_seqlens, T)[rows]
     for x, y in ((q0, q), (k0, k)):
@@ -275,7 +277,8 @@ def test_workload5_long_sampled(dev):
     assert torch.equal(q_store[-guard:].view(torch.int16), canary.view(torch.int16))
 
 
-def test_workload5_cp_rank_long_segments(dev):
+@pytest.mark.parametrize("use_cache", [False, True])
+def test_workload5_cp_rank_long_segments(dev, use_cache):
     """A load-balanced context-parallel rank of the 1,048,576-token sequence (cp = 2,
     rank 0: chunks 0 and 3 of 4): its 2^19 rows of 32 Q heads span 2^31 elements, so the
     64-bit-offset instance runs with a two-entry segment list whose second segment
@@ -300,15 +303,16 @@ def test_workload5_cp_rank_long_segments(dev):
     q_store[-guard:].copy_(canary)
     k = wl.normal_bf16((n, w.n_kv_heads, w.head_dim), 5200, device="cuda")
     cu_dev = torch.from_numpy(pack.cu_seqlens).to(dev)
-    info = pr().rope_qk_launch_info(q, k, w.theta, cu_seqlens=cu_dev, segments=segs)
-    assert info.kernel_name() == "rope_qk_tile_kernel<128,true,2>"          # no cache: 2 units per thread
+    cache = pr().new_cos_sin_cache(T, w.head_dim, w.theta, device=dev) if use_cache else None
+    info = pr().rope_qk_launch_info(q, k, w.theta, cu_seqlens=cu_dev, segments=segs, cos_sin_cache=cache)
+    assert info.kernel_name() == "rope_qk_tile_kernel<128,true,%d>" % (3 if use_cache else 2)
     rng = np.random.Generator(np.random.PCG64(5300))
     cross = (1 << 31) // (w.n_q_heads * w.head_dim)
     fixed = [r for r in (0, 1, T // 4 - 1, T // 4, T // 4 + 1, cross - 2, cross - 1, cross, n - 1) if r < n]
     rows = np.unique(np.concatenate([rng.integers(0, n, 2048), fixed])).astype(np.int64)
     rows_dev = torch.from_numpy(rows).to(dev)
     q0, k0 = to_bits(q[rows_dev]), to_bits(k[rows_dev])
-    pr().rope_qk_apply(q, k, w.theta, cu_seqlens=cu_dev, segments=segs)     # no cache: evaluated in the kernel
+    pr().rope_qk_apply(q, k, w.theta, cu_seqlens=cu_dev, segments=segs, cos_sin_cache=cache)
     torch.cuda.synchronize()
     tokens = np.where(rows < T // 4, rows, rows - T // 4 + 3 * T // 4)
     pos = oracle.positions(pack.cu_seqlens, T)[tokens]

@@ -41,10 +41,10 @@
  *
  * Errors.  Every entry point returns ROPE_OK (0) or a negative rope_status.  Arguments
  * are checked on the host before anything is launched or copied; a rejected call
- * launches and copies nothing.  The values inside cu_seqlens are not read on the host (that would need a
- * synchronisation): rope_validate_cu_seqlens checks them on the device.  With invalid
- * values the kernels still stay inside the Q/K/cache bounds and skip the tokens whose
- * position cannot be derived.  No kernel traps, asserts or spins.
+ * launches and copies nothing.  The values inside cu_seqlens are not read on the host
+ * (that would need a synchronisation): rope_validate_cu_seqlens checks them on the
+ * device.  With invalid values the kernels still stay inside the Q/K/cache bounds and
+ * skip the tokens whose position cannot be derived.  No kernel traps, asserts or spins.
  */
 #ifndef ROPE_QK_H
 #define ROPE_QK_H
@@ -164,9 +164,9 @@ int rope_qk_bwd(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs,
  * Views.  Each of q, k, q_out, k_out is a bf16 [total_tokens, heads, head_dim] view with
  * head_dim contiguous and element strides for tokens and heads (multiples of 8, >= 0;
  * pointers 16-byte aligned; the view's span, (tokens - 1) * token stride + (heads - 1)
- * * head stride + head_dim, below 2^56 elements, else ROPE_ERR_SHAPE).  No two (token,
- * head) rows of one view may share an
- * element (else ROPE_ERR_OVERLAP).  Q and K must share no element: either their address
+ * * head stride + head_dim, below 2^56 elements, else ROPE_ERR_SHAPE).  No two
+ * (token, head) rows of one view may share an element (else ROPE_ERR_OVERLAP).  Q and
+ * K must share no element: either their address
  * ranges are disjoint, or they step tokens by the same stride and each token's Q block
  * and K block are disjoint -- the Q and K slices of one fused QKV projection output,
  * e.g. qkv[T, Hq + 2*Hkv, d] with q = qkv[:, :Hq], k = qkv[:, Hq:Hq+Hkv], are accepted
@@ -181,8 +181,8 @@ int rope_qk_bwd(void *q, void *k, const int32_t *cu_seqlens, int32_t n_seqs,
  * [0, 2^24) leaves the row out (in place: untouched; out of place: copied).  With
  * ROPE_FLAG_POSITION_IDS_INT64 in flags, position_ids points to int64 values instead
  * (8-byte aligned; the dtype of the position ids a Hugging Face collator builds), with
- * the same rule for values outside [0, 2^24).  Otherwise
- * row r is token token_offset + r of the stream cu_seqlens describes and its position
+ * the same rule for values outside [0, 2^24).  Otherwise row r is token
+ * token_offset + r of the stream cu_seqlens describes and its position
  * is derived as for rope_qk_fwd; token_offset lets a context-parallel shard holding
  * tokens [a, b) of a pack pass the whole pack's cu_seqlens with token_offset = a
  * (token_offset + total_tokens <= 2^24).
@@ -259,8 +259,8 @@ int rope_qk_apply(const rope_qk_desc *desc, void *stream);
  * at least 32,768 tiles with 32-bit offsets, a compile-time head_dim and a cos/sin
  * cache; 3 for smaller such launches without seq_used whose tile holds at most 384
  * units, and for launches with 64-bit offsets, a compile-time head_dim and a cache but
- * no seq_used; 2 otherwise), and its grid: one CTA
- * of `threads` threads per tile of `tile_tokens` consecutive tokens.  Returns the
+ * no seq_used; 2 otherwise), and its grid: one CTA of `threads` threads per tile of
+ * `tile_tokens` consecutive tokens.  Returns the
  * status rope_qk_apply's argument checks give (the cache's device is not checked);
  * grid == 0 when there is nothing to launch.
  */

@@ -419,9 +419,11 @@ def test_outside_tokens_and_empty(dev):
     pr().rope_qk_fwd(e, ek, torch.zeros(1, dtype=torch.int32, device=dev), 1.0e4)
 
 
-def test_invalid_cu_stays_in_bounds(dev):
+@pytest.mark.parametrize("with_seq_used", [False, True])
+def test_invalid_cu_stays_in_bounds(dev, with_seq_used):
     """A decreasing cu_seqlens is reported by the validator; the rotation kernel still
-    touches only rows of Q and K and leaves tokens outside [cu[0], cu[n]) alone."""
+    touches only rows of Q and K and leaves tokens outside [cu[0], cu[n]) alone (also
+    with seq_used values beyond the samples' lengths and negative ones)."""
     rng = np.random.Generator(np.random.PCG64(42))
     T, hq, hkv, d = 64, 2, 1, 64
     guard = 2048
@@ -432,7 +434,12 @@ def test_invalid_cu_stays_in_bounds(dev):
     k = from_bits(_normal_bits(rng, (T, hkv, d)), dev)
     cu = torch.tensor([0, 40, 10, 30, 48], dtype=torch.int32, device=dev)
     assert int(pr().rope_validate_cu_seqlens(cu, T).item()) & pr().ROPE_CU_DECREASING
-    _run("rope_qk_fwd", q, k, cu, 1.0e4)
+    if with_seq_used:
+        used = torch.tensor([1000, -7, 12, 3], dtype=torch.int32, device=dev)
+        pr().rope_qk_apply(q, k, 1.0e4, cu_seqlens=cu, seq_used=used)
+        torch.cuda.synchronize()
+    else:
+        _run("rope_qk_fwd", q, k, cu, 1.0e4)
     assert torch.all(store[:guard] == 5.0) and torch.all(store[-guard:] == 5.0)
     assert np.array_equal(to_bits(q)[48:], qb[48:])
 

@@ -108,18 +108,21 @@ PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "rope_qk_tile_kernel_%s.md")   
 
 def parse_args():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=4)
-    ap.add_argument("--e2e-steps", type=int, default=80)
+    ap.add_argument("--gpus", type=int, default=1, help="GPUs of the run (N > 1: launched under torchrun)")
+    ap.add_argument("--steps", type=int, default=2000, help="timed steps (one step: forward + backward)")
+    ap.add_argument("--warmup", type=int, default=20, help="untimed steps before them (at least 3 are run)")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours",
+                    help="ours: the CUDA library; reference: the CPU oracle on the host cores")
+    ap.add_argument("--workload", type=int, default=4,
+                    help="1 tiny-pack-4x, 2 qwen3-4b-16k, 3 llama3-8b-8x2048, 4 qwen3-32b-64k, 5 long-1m-int64")
+    ap.add_argument("--e2e-steps", type=int, default=80, help="timed steps of the host-buffer (e2e) leg")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target seconds of oracle work for the CPU baseline sample")
     ap.add_argument("--reference-seconds", type=float, default=90.0,
                     help="--impl reference: seconds of oracle work over the warm-up and timed steps")
-    ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer (e2e) leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the CPU oracle baseline and the parity check against it")
     ap.add_argument("--layout", choices=["packed", "padded", "padded-seq-used"], default="packed",
                     help="rope path: the pack as is, or (workloads with padded samples) the padded batch "
                          "with every row rotated, or with the pad rows skipped through seq_used")
@@ -131,8 +134,11 @@ def parse_args():
     ap.add_argument("--no-cache", action="store_true",
                     help="rope path: no cos/sin cache, cos/sin evaluated per tile")
     ap.add_argument("--path", choices=["rope", "glu", "rope-forms", "rope-shapes"], default="rope",
-                    help="rope: the QK-RoPE step (default); glu: SwiGLU/GeGLU forward+backward")
-    ap.add_argument("--glu-workload", default="qwen3-4b-mlp-1m")
+                    help="rope: the QK-RoPE step (default); glu: SwiGLU/GeGLU forward+backward; "
+                         "rope-forms: the forward through every input form, each checked; rope-shapes: "
+                         "other head shapes")
+    ap.add_argument("--glu-workload", default="qwen3-4b-mlp-1m",
+                    help="glu path: qwen3-4b-mlp-1m, or its 65,536- and 16,384-token slices")
     ap.add_argument("--glu-kind", choices=["swiglu", "geglu", "geglu_tanh"], default=None,
                     help="activation (default: the workload's)")
     return ap.parse_args()

@@ -412,3 +412,28 @@ def test_dispatch_boundaries(dev, T, hq, hkv, d, cached, used, kernel, tile):
         torch.cuda.synchronize()
         _check(to_bits(q), _expect(qb, pos, 1.0e6, bwd=bwd), qb, (kernel, "q", bwd))
         _check(to_bits(k), _expect(kb, pos, 1.0e6, bwd=bwd), kb, (kernel, "k", bwd))
+
+
+@pytest.mark.parametrize("use_cache", [False, True])
+def test_largest_pack(dev, use_cache):
+    """The largest pack the library takes: 2^24 tokens in one sample (every position an
+    exact binary32 integer up to 16,777,215), one Q and one K head of 16.  Seeded rows
+    and the last rows equal the oracle, forward and backward; with the 2^24-row cos/sin
+    cache or without one (the largest angles then go to the binary64 evaluation)."""
+    T, d, theta = 1 << 24, 16, 1.0e4
+    rng = np.random.Generator(np.random.PCG64(77))
+    cu_np = np.array([0, T], dtype=np.int32)
+    cu = torch.from_numpy(cu_np).to(dev)
+    q = torch.empty((T, 1, d), dtype=torch.bfloat16, device=dev).normal_(generator=torch.Generator(dev).manual_seed(78))
+    k = torch.empty((T, 1, d), dtype=torch.bfloat16, device=dev).normal_(generator=torch.Generator(dev).manual_seed(79))
+    rows = np.unique(np.concatenate([rng.integers(0, T, 4096), np.arange(T - 40, T), [0, 1, 1 << 23]]))
+    rows_dev = torch.from_numpy(rows).to(dev)
+    q0, k0 = to_bits(q[rows_dev]), to_bits(k[rows_dev])
+    cache = pr().new_cos_sin_cache(T, d, theta, device=dev) if use_cache else None
+    pos = rows.astype(np.int32)
+    for bwd in (False, True):
+        pr().rope_qk_apply(q, k, theta, cu_seqlens=cu, cos_sin_cache=cache, backward=bwd)
+        torch.cuda.synchronize()
+        q0 = _expect(q0, pos, theta, bwd=bwd)
+        k0 = _expect(k0, pos, theta, bwd=bwd)
+        assert np.array_equal(to_bits(q[rows_dev]), q0) and np.array_equal(to_bits(k[rows_dev]), k0), bwd
